@@ -1,0 +1,298 @@
+/*
+ * ttt_oracle.c -- fp64 CPU oracle for the Test-Time-Training (TTT) layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or load
+ * this file; only the test-suite, the smoke check and the benchmark's CPU-baseline
+ * leg do.  It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes (the definition, token by token, in the "primal" form):
+ *   hidden state = weights W of an inner model f(x; W), reset to W0 for every
+ *   (batch, head) sequence ("Fast weights 与 TTT layers", section 4: fast weights
+ *   are reset at each sequence boundary);
+ *   reconstruction loss  l_t(W) = 1/2 || f(k_t; W) - v_t ||^2
+ *   ("Fast weights 与 TTT layers", opening formula; "TTT：Test-Time Training",
+ *   section TTT / MSE loss);
+ *   mini-batch gradient descent: the sequence is cut into consecutive blocks of b
+ *   tokens; every token of a block takes its gradient at the W the previous block
+ *   left, and W moves by -eta_s * grad l_s for each token s in order, so the
+ *   running W after token t holds the cumulative sum of the block's writes
+ *   ("Learning to (Learn at Test Time)" walkthrough, section 1.2.2, formula 6 and
+ *   the cumsum / gradient-operator channels);
+ *   output rule z_t = f(q_t; W_t) (same walkthrough, section 1.2, formula 1/5;
+ *   "TTT：Test-Time Training", section TTT general form).
+ *   causal = 1: W_t includes the writes of all tokens s <= t of t's block.
+ *   causal = 0: every query of a block reads the W at the end of that block
+ *   (b = T gives the single full-batch step of the vision variant, ViT3 article,
+ *   observation 2).
+ *
+ * Inner models (walkthrough section 2.2.1; ViT3 article observation 4):
+ *   linear: f(x; W) = x W, W in R^{d x d} (row convention, x is a 1 x d row).
+ *   mlp   : f(x) = SiLU(x W1 + c1) W2 + c2, W1 d x m, c1 1 x m, W2 m x d, c2 1 x d,
+ *           SiLU(h) = h * sigma(h).
+ * Gradients are written out by hand from the chain rule:
+ *   linear mse: e = k W - v,   dW = k^T e
+ *   linear dot (negative dot-product loss l = -(k W) v^T, "TTT：Test-Time Training",
+ *              section "如何理解"): dW = -k^T v
+ *   mlp: h = k W1 + c1, a = SiLU(h), e = a W2 + c2 - v,
+ *        dW2 = a^T e, dc2 = e, g = (e W2^T) * SiLU'(h), dW1 = k^T g, dc1 = g,
+ *        SiLU'(h) = sigma(h) (1 + h (1 - sigma(h))).
+ *
+ * Layouts: all arrays are C-contiguous double.  q, k, v, z: [B,H,T,d];
+ * eta: [B,H,T] or NULL (then eta_scalar is used for every token);
+ * W0 (linear) [.., H, d, d] with batch stride w0_bstride elements (0 = shared over
+ * the batch); W_out [B,H,d,d] or NULL.  MLP: W1 [.., H, d, m], c1 [.., H, m],
+ * W2 [.., H, m, d], c2 [.., H, d]; per_batch = 0 means one parameter set per head
+ * shared over the batch ([H,...]), 1 means one per (batch, head) ([B,H,...]);
+ * outputs [B,H,...] or NULL.
+ * Returns 0 on success, -1 on bad arguments.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ linear */
+
+typedef struct {
+    int B, H, T, d, b, causal, loss;
+    const double *q, *k, *v, *eta;
+    double eta_scalar;
+    const double *W0;
+    long long w0_bstride;
+    double *z, *W_out;
+    int next;               /* next (batch, head) chain to process */
+    pthread_mutex_t lock;
+} linear_job;
+
+static void linear_chain(const linear_job *J, int bh)
+{
+    const int T = J->T, d = J->d, b = J->b;
+    const int bi = bh / J->H, hi = bh % J->H;
+    const double *q = J->q + (size_t)bh * T * d;
+    const double *k = J->k + (size_t)bh * T * d;
+    const double *v = J->v + (size_t)bh * T * d;
+    const double *eta = J->eta ? J->eta + (size_t)bh * T : NULL;
+    double *z = J->z + (size_t)bh * T * d;
+    const double *W0 = J->W0 + (size_t)bi * J->w0_bstride + (size_t)hi * d * d;
+
+    double *W = malloc(sizeof(double) * d * d);    /* running weights          */
+    double *Ws = malloc(sizeof(double) * d * d);   /* block's gradient point   */
+    double *e = malloc(sizeof(double) * d);
+    memcpy(W, W0, sizeof(double) * d * d);
+
+    for (int n0 = 0; n0 < T; n0 += b) {
+        const int n1 = (n0 + b < T) ? n0 + b : T;
+        memcpy(Ws, W, sizeof(double) * d * d);
+        for (int t = n0; t < n1; ++t) {
+            const double *kt = k + (size_t)t * d, *vt = v + (size_t)t * d;
+            const double et = eta ? eta[t] : J->eta_scalar;
+            if (J->loss == 0) {
+                /* e = k_t Ws - v_t */
+                for (int j = 0; j < d; ++j) {
+                    double s = 0.0;
+                    for (int i = 0; i < d; ++i) s += kt[i] * Ws[i * d + j];
+                    e[j] = s - vt[j];
+                }
+            } else {
+                /* gradient of -(k W) v^T is -k^T v: use e = -v */
+                for (int j = 0; j < d; ++j) e[j] = -vt[j];
+            }
+            /* W -= eta_t k_t^T e */
+            for (int i = 0; i < d; ++i)
+                for (int j = 0; j < d; ++j) W[i * d + j] -= et * kt[i] * e[j];
+            if (J->causal) {
+                const double *qt = q + (size_t)t * d;
+                for (int j = 0; j < d; ++j) {
+                    double s = 0.0;
+                    for (int i = 0; i < d; ++i) s += qt[i] * W[i * d + j];
+                    z[(size_t)t * d + j] = s;
+                }
+            }
+        }
+        if (!J->causal) {
+            for (int t = n0; t < n1; ++t) {
+                const double *qt = q + (size_t)t * d;
+                for (int j = 0; j < d; ++j) {
+                    double s = 0.0;
+                    for (int i = 0; i < d; ++i) s += qt[i] * W[i * d + j];
+                    z[(size_t)t * d + j] = s;
+                }
+            }
+        }
+    }
+    if (J->W_out) memcpy(J->W_out + (size_t)bh * d * d, W, sizeof(double) * d * d);
+    free(W); free(Ws); free(e);
+}
+
+static void *linear_worker(void *arg)
+{
+    linear_job *J = (linear_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        const int bh = J->next++;
+        pthread_mutex_unlock(&J->lock);
+        if (bh >= J->B * J->H) break;
+        linear_chain(J, bh);
+    }
+    return NULL;
+}
+
+int ttt_oracle_linear(int B, int H, int T, int d, int b, int causal, int loss,
+                      const double *q, const double *k, const double *v,
+                      const double *eta, double eta_scalar,
+                      const double *W0, long long w0_bstride,
+                      double *z, double *W_out, int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || d <= 0 || b <= 0 || !W0 || (T > 0 && (!q || !k || !v || !z)))
+        return -1;
+    if (loss != 0 && loss != 1) return -1;
+    linear_job J = {B, H, T, d, b, causal ? 1 : 0, loss, q, k, v, eta, eta_scalar,
+                    W0, w0_bstride, z, W_out, 0};
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads < 1) nthreads = 1;
+    pthread_t *th = malloc(sizeof(pthread_t) * nthreads);
+    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, linear_worker, &J);
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    return 0;
+}
+
+/* --------------------------------------------------------------------- mlp */
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+typedef struct {
+    int B, H, T, d, m, b, causal;
+    const double *q, *k, *v, *eta;
+    double eta_scalar;
+    const double *W1, *c1, *W2, *c2;
+    int per_batch;
+    double *z, *W1o, *c1o, *W2o, *c2o;
+    int next;
+    pthread_mutex_t lock;
+} mlp_job;
+
+/* z = SiLU(x W1 + c1) W2 + c2 with scratch h (length m) */
+static void mlp_forward(int d, int m, const double *x, const double *W1, const double *c1,
+                        const double *W2, const double *c2, double *h, double *out)
+{
+    for (int j = 0; j < m; ++j) {
+        double s = c1[j];
+        for (int i = 0; i < d; ++i) s += x[i] * W1[i * m + j];
+        h[j] = s * sigmoid(s);
+    }
+    for (int j = 0; j < d; ++j) {
+        double s = c2[j];
+        for (int i = 0; i < m; ++i) s += h[i] * W2[i * d + j];
+        out[j] = s;
+    }
+}
+
+static void mlp_chain(const mlp_job *J, int bh)
+{
+    const int T = J->T, d = J->d, m = J->m, b = J->b;
+    const int hi = bh % J->H;
+    const size_t hp = J->per_batch ? (size_t)bh : (size_t)hi;   /* parameter-set index */
+    const double *q = J->q + (size_t)bh * T * d;
+    const double *k = J->k + (size_t)bh * T * d;
+    const double *v = J->v + (size_t)bh * T * d;
+    const double *eta = J->eta ? J->eta + (size_t)bh * T : NULL;
+    double *z = J->z + (size_t)bh * T * d;
+
+    double *W1 = malloc(sizeof(double) * d * m), *W1s = malloc(sizeof(double) * d * m);
+    double *W2 = malloc(sizeof(double) * m * d), *W2s = malloc(sizeof(double) * m * d);
+    double *c1 = malloc(sizeof(double) * m), *c1s = malloc(sizeof(double) * m);
+    double *c2 = malloc(sizeof(double) * d), *c2s = malloc(sizeof(double) * d);
+    double *h = malloc(sizeof(double) * m), *a = malloc(sizeof(double) * m);
+    double *g = malloc(sizeof(double) * m), *e = malloc(sizeof(double) * d);
+    memcpy(W1, J->W1 + hp * d * m, sizeof(double) * d * m);
+    memcpy(c1, J->c1 + hp * m, sizeof(double) * m);
+    memcpy(W2, J->W2 + hp * m * d, sizeof(double) * m * d);
+    memcpy(c2, J->c2 + hp * d, sizeof(double) * d);
+
+    for (int n0 = 0; n0 < T; n0 += b) {
+        const int n1 = (n0 + b < T) ? n0 + b : T;
+        memcpy(W1s, W1, sizeof(double) * d * m);
+        memcpy(c1s, c1, sizeof(double) * m);
+        memcpy(W2s, W2, sizeof(double) * m * d);
+        memcpy(c2s, c2, sizeof(double) * d);
+        for (int t = n0; t < n1; ++t) {
+            const double *kt = k + (size_t)t * d, *vt = v + (size_t)t * d;
+            const double et = eta ? eta[t] : J->eta_scalar;
+            /* forward at the block's gradient point */
+            for (int j = 0; j < m; ++j) {
+                double s = c1s[j];
+                for (int i = 0; i < d; ++i) s += kt[i] * W1s[i * m + j];
+                h[j] = s;
+                a[j] = s * sigmoid(s);
+            }
+            for (int j = 0; j < d; ++j) {
+                double s = c2s[j];
+                for (int i = 0; i < m; ++i) s += a[i] * W2s[i * d + j];
+                e[j] = s - vt[j];
+            }
+            /* backward: g = (e W2s^T) * SiLU'(h) */
+            for (int i = 0; i < m; ++i) {
+                double s = 0.0;
+                for (int j = 0; j < d; ++j) s += e[j] * W2s[i * d + j];
+                const double sg = sigmoid(h[i]);
+                g[i] = s * sg * (1.0 + h[i] * (1.0 - sg));
+            }
+            /* descent step of token t */
+            for (int i = 0; i < m; ++i)
+                for (int j = 0; j < d; ++j) W2[i * d + j] -= et * a[i] * e[j];
+            for (int j = 0; j < d; ++j) c2[j] -= et * e[j];
+            for (int i = 0; i < d; ++i)
+                for (int j = 0; j < m; ++j) W1[i * m + j] -= et * kt[i] * g[j];
+            for (int j = 0; j < m; ++j) c1[j] -= et * g[j];
+            if (J->causal)
+                mlp_forward(d, m, q + (size_t)t * d, W1, c1, W2, c2, h, z + (size_t)t * d);
+        }
+        if (!J->causal)
+            for (int t = n0; t < n1; ++t)
+                mlp_forward(d, m, q + (size_t)t * d, W1, c1, W2, c2, h, z + (size_t)t * d);
+    }
+    if (J->W1o) memcpy(J->W1o + (size_t)bh * d * m, W1, sizeof(double) * d * m);
+    if (J->c1o) memcpy(J->c1o + (size_t)bh * m, c1, sizeof(double) * m);
+    if (J->W2o) memcpy(J->W2o + (size_t)bh * m * d, W2, sizeof(double) * m * d);
+    if (J->c2o) memcpy(J->c2o + (size_t)bh * d, c2, sizeof(double) * d);
+    free(W1); free(W1s); free(W2); free(W2s); free(c1); free(c1s); free(c2); free(c2s);
+    free(h); free(a); free(g); free(e);
+}
+
+static void *mlp_worker(void *arg)
+{
+    mlp_job *J = (mlp_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        const int bh = J->next++;
+        pthread_mutex_unlock(&J->lock);
+        if (bh >= J->B * J->H) break;
+        mlp_chain(J, bh);
+    }
+    return NULL;
+}
+
+int ttt_oracle_mlp(int B, int H, int T, int d, int m, int b, int causal,
+                   const double *q, const double *k, const double *v,
+                   const double *eta, double eta_scalar,
+                   const double *W1, const double *c1, const double *W2, const double *c2,
+                   int per_batch,
+                   double *z, double *W1o, double *c1o, double *W2o, double *c2o,
+                   int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || d <= 0 || m <= 0 || b <= 0 || !W1 || !c1 || !W2 || !c2 ||
+        (T > 0 && (!q || !k || !v || !z)))
+        return -1;
+    mlp_job J = {B, H, T, d, m, b, causal ? 1 : 0, q, k, v, eta, eta_scalar,
+                 W1, c1, W2, c2, per_batch ? 1 : 0, z, W1o, c1o, W2o, c2o, 0};
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads < 1) nthreads = 1;
+    pthread_t *th = malloc(sizeof(pthread_t) * nthreads);
+    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, mlp_worker, &J);
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    return 0;
+}

@@ -1,0 +1,97 @@
+"""Independent restatements used to pin the oracle (test-side only).
+
+Nothing here is shared with the oracle or with the CUDA path.  Each helper is a
+different route to a value the pages fix: autograd instead of hand gradients,
+the column-convention delta rule as printed, brute-force attention sums, and the
+matrix ("dual") form of a mini-batch step.
+"""
+import numpy as np
+import torch
+
+
+def silu_t(x):
+    return x * torch.sigmoid(x)
+
+
+def f_linear(x, P):
+    return x @ P[0]
+
+
+def f_mlp(x, P):
+    W1, c1, W2, c2 = P
+    return silu_t(x @ W1 + c1) @ W2 + c2
+
+
+def definition_autograd(f, P0, q, k, v, eta, b, causal):
+    """The layer exactly as defined, one chain, fp64 torch, gradients by autograd.
+
+    W_t = W_start - grad_W( sum_{s in block, s <= t} eta_s * 1/2 ||f(k_s;W) - v_s||^2 )
+    evaluated at the block's start weights; z_t = f(q_t; W_t) (causal) or
+    f(q_t; W_end of the block) (non-causal).  q,k,v: [T,d]; eta: [T]."""
+    T = q.shape[0]
+    P = [p.clone() for p in P0]
+    z = torch.zeros(T, v.shape[1], dtype=torch.float64)
+
+    def step(Ps, lo, hi):
+        Ps = [p.detach().clone().requires_grad_(True) for p in Ps]
+        L = sum(eta[s] * 0.5 * ((f(k[s:s + 1], Ps) - v[s:s + 1]) ** 2).sum()
+                for s in range(lo, hi))
+        gs = torch.autograd.grad(L, Ps)
+        return [(p - g).detach() for p, g in zip(Ps, gs)]
+
+    for n0 in range(0, T, b):
+        n1 = min(n0 + b, T)
+        if causal:
+            for t in range(n0, n1):
+                Pt = step(P, n0, t + 1)
+                z[t] = f(q[t:t + 1], Pt)[0]
+        P_end = step(P, n0, n1)
+        if not causal:
+            for t in range(n0, n1):
+                z[t] = f(q[t:t + 1], P_end)[0]
+        P = P_end
+    return z, P
+
+
+def dual_linear(q, k, v, W0, eta, b, causal):
+    """Mini-batch step in matrix form, numpy fp64, one chain (q,k,v [T,d], eta [T]).
+    E = K W - V;  Z = Q W - M.(Q K^T) diag(eta) E;  W <- W - K^T diag(eta) E."""
+    T, d = q.shape
+    W = W0.copy()
+    z = np.zeros((T, d))
+    for n0 in range(0, T, b):
+        n1 = min(n0 + b, T)
+        Q, K, V, et = q[n0:n1], k[n0:n1], v[n0:n1], eta[n0:n1]
+        M = np.tril(np.ones((n1 - n0, n1 - n0))) if causal else np.ones((n1 - n0, n1 - n0))
+        E = K @ W - V
+        Et = et[:, None] * E
+        z[n0:n1] = Q @ W - (M * (Q @ K.T)) @ Et
+        W = W - K.T @ Et
+    return z, W
+
+
+def dual_mlp(q, k, v, W1, c1, W2, c2, eta, b, causal):
+    """TTT-MLP mini-batch step in matrix form (numpy fp64, one chain).  The "+1"
+    terms carry the bias writes: c_t = c - sum_{s<=t} eta_s * grad_c l_s."""
+    sig = lambda x: 1.0 / (1.0 + np.exp(-x))
+    T, d = q.shape
+    W1, c1, W2, c2 = W1.copy(), c1.copy(), W2.copy(), c2.copy()
+    z = np.zeros((T, d))
+    for n0 in range(0, T, b):
+        n1 = min(n0 + b, T)
+        Q, K, V, et = q[n0:n1], k[n0:n1], v[n0:n1], eta[n0:n1][:, None]
+        n = n1 - n0
+        M = np.tril(np.ones((n, n))) if causal else np.ones((n, n))
+        Hk = K @ W1 + c1
+        Ak = Hk * sig(Hk)
+        E = Ak @ W2 + c2 - V
+        D = (E @ W2.T) * (sig(Hk) * (1 + Hk * (1 - sig(Hk))))
+        Et, Dt = et * E, et * D
+        Hq = Q @ W1 + c1 - (M * (Q @ K.T + 1)) @ Dt
+        Aq = Hq * sig(Hq)
+        z[n0:n1] = Aq @ W2 + c2 - (M * (Aq @ Ak.T + 1)) @ Et
+        W2 = W2 - Ak.T @ Et
+        c2 = c2 - Et.sum(0)
+        W1 = W1 - K.T @ Dt
+        c1 = c1 - Dt.sum(0)
+    return z, (W1, c1, W2, c2)

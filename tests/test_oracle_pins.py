@@ -1,0 +1,302 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+No GPU.  Every test compares the oracle with a route that shares none of its code:
+the delta rule as the pages print it, brute-force linear attention, Theorem 1,
+autograd on the layer's definition, central finite differences, and the matrix
+("dual") form of a mini-batch step.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import _defs
+
+rng = np.random.default_rng(1234)
+
+
+def _unit(x):
+    return x / np.linalg.norm(x, axis=-1, keepdims=True)
+
+
+def _qkv(B, H, T, d, unit=True, seed=0):
+    r = np.random.default_rng(seed)
+    q, k, v = (r.standard_normal((B, H, T, d)) for _ in range(3))
+    if unit:
+        q, k = _unit(q), _unit(k)
+    return q, k, v
+
+
+def _mlp_params(H, d, m, seed=0, scale=0.3, bias=True):
+    r = np.random.default_rng(seed)
+    W1 = r.standard_normal((H, d, m)) * scale
+    W2 = r.standard_normal((H, m, d)) * scale
+    c1 = r.standard_normal((H, m)) * (0.1 if bias else 0.0)
+    c2 = r.standard_normal((H, d)) * (0.1 if bias else 0.0)
+    return W1, c1, W2, c2
+
+
+# --------------------------------------------------------------- TTT-Linear
+
+
+def test_b1_is_delta_rule_column_convention():
+    """b = 1 must equal the delta rule W_t = W_{t-1} + eta (v_t - W_{t-1} k_t) k_t^T
+    ("Fast weights 与 TTT layers", section 1, column convention f(k;W) = W k).
+    The oracle's row convention is its transpose: W_row = W_col^T."""
+    B, H, T, d = 1, 2, 23, 5
+    q, k, v = _qkv(B, H, T, d)
+    eta = rng.uniform(0.1, 1.2, (B, H, T))
+    W0 = rng.standard_normal((H, d, d)) * 0.3
+    z, Wf = oracle.linear(q, k, v, W0, b=1, causal=True, eta=eta)
+    for h in range(H):
+        Wc = W0[h].T.copy()
+        for t in range(T):
+            kt, vt = k[0, h, t][:, None], v[0, h, t][:, None]
+            Wc = Wc + eta[0, h, t] * (vt - Wc @ kt) @ kt.T
+            np.testing.assert_allclose(z[0, h, t], (Wc @ q[0, h, t][:, None])[:, 0], atol=1e-12)
+        np.testing.assert_allclose(Wf[0, h], Wc.T, atol=1e-12)
+
+
+def test_b1_unit_key_unit_rate_writes_exactly():
+    """With a unit-norm key and eta = 1, one delta-rule write makes f(k_t;W_t) = v_t
+    exactly (the repeated-write remark of "Fast weights 与 TTT layers", section 1).
+    Query = key reads that back."""
+    B, H, T, d = 2, 1, 17, 6
+    _, k, v = _qkv(B, H, T, d)
+    z, _ = oracle.linear(k, k, v, rng.standard_normal((H, d, d)), b=1, causal=True,
+                         eta_scalar=1.0)
+    np.testing.assert_allclose(z, v, atol=1e-12)
+
+
+@pytest.mark.parametrize("b,causal", [(1, True), (4, True), (7, True), (4, False), (7, False)])
+def test_dot_loss_is_linear_attention(b, causal):
+    """Negative dot-product loss: grad = -k^T v does not depend on W, so with W0 = 0
+    z_t = eta * sum_{s visible to t} (q_t . k_s) v_s, the linear-attention recurrence
+    S_t = S_{t-1} + k_t v_t^T read by q_t ("TTT：Test-Time Training", sections
+    线性注意力 and 如何理解).  Causal: s <= t; non-causal: s up to t's block end."""
+    B, H, T, d = 1, 2, 19, 4
+    q, k, v = _qkv(B, H, T, d, unit=False)
+    eta = 0.7
+    z, Wf = oracle.linear(q, k, v, np.zeros((H, d, d)), b=b, causal=causal,
+                          eta_scalar=eta, loss="dot")
+    for h in range(H):
+        for t in range(T):
+            last = t if causal else min((t // b + 1) * b, T) - 1
+            ref = sum(eta * (q[0, h, t] @ k[0, h, s]) * v[0, h, s] for s in range(last + 1))
+            np.testing.assert_allclose(z[0, h, t], ref, atol=1e-11)
+        S = sum(np.outer(k[0, h, s], v[0, h, s]) for s in range(T))
+        np.testing.assert_allclose(Wf[0, h], eta * S, atol=1e-11)
+
+
+def test_theorem1_batch_gd_zero_init_is_linear_attention():
+    """Theorem 1 (walkthrough section 2.1.1): linear inner model, batch GD (b = T),
+    W0 = 0 and the MSE loss give causal linear attention: every gradient is taken
+    at W0 = 0 where the residual is -v_s, so z_t = eta sum_{s<=t} (q_t . k_s) v_s."""
+    B, H, T, d = 2, 1, 21, 5
+    q, k, v = _qkv(B, H, T, d)
+    eta = 0.9
+    z, _ = oracle.linear(q, k, v, np.zeros((H, d, d)), b=T, causal=True, eta_scalar=eta)
+    for bi in range(B):
+        A = np.tril(q[bi, 0] @ k[bi, 0].T)
+        np.testing.assert_allclose(z[bi, 0], eta * A @ v[bi, 0], atol=1e-12)
+
+
+def test_full_batch_is_one_gd_step_linear():
+    """b = T, non-causal: W1 = W0 - grad(sum_s eta_s l_s)(W0), every query reads W1
+    (ViT3 article, observation 2; spec definition).  Gradient by autograd."""
+    B, H, T, d = 1, 2, 13, 6
+    q, k, v = _qkv(B, H, T, d)
+    eta = rng.uniform(0.2, 1.0, (B, H, T))
+    W0 = rng.standard_normal((H, d, d)) * 0.2
+    z, Wf = oracle.linear(q, k, v, W0, b=T, causal=False, eta=eta)
+    for h in range(H):
+        W = torch.tensor(W0[h], requires_grad=True)
+        K, V = torch.tensor(k[0, h]), torch.tensor(v[0, h])
+        L = (torch.tensor(eta[0, h])[:, None] * 0.5 * (K @ W - V) ** 2).sum()
+        (g,) = torch.autograd.grad(L, W)
+        W1 = (W - g).detach().numpy()
+        np.testing.assert_allclose(Wf[0, h], W1, atol=1e-12)
+        np.testing.assert_allclose(z[0, h], q[0, h] @ W1, atol=1e-12)
+
+
+@pytest.mark.parametrize("T,b,causal", [(11, 1, True), (11, 3, True), (11, 4, False),
+                                        (12, 4, True), (10, 10, True), (9, 20, False)])
+def test_linear_matches_definition_autograd(T, b, causal):
+    """Every mini-batch size, ragged tails included: the oracle equals the layer's
+    definition evaluated with autograd gradients."""
+    B, H, d = 1, 1, 4
+    q, k, v = _qkv(B, H, T, d)
+    eta = rng.uniform(0.1, 1.0, (B, H, T))
+    W0 = rng.standard_normal((H, d, d)) * 0.3
+    z, Wf = oracle.linear(q, k, v, W0, b=b, causal=causal, eta=eta)
+    t = lambda a: torch.tensor(a)
+    zr, (Wr,) = _defs.definition_autograd(_defs.f_linear, [t(W0[0])], t(q[0, 0]), t(k[0, 0]),
+                                          t(v[0, 0]), t(eta[0, 0]), b, causal)
+    np.testing.assert_allclose(z[0, 0], zr.numpy(), atol=1e-12)
+    np.testing.assert_allclose(Wf[0, 0], Wr.numpy(), atol=1e-12)
+
+
+@pytest.mark.parametrize("b,causal", [(1, True), (16, True), (5, True), (16, False), (64, False)])
+def test_linear_dual_form_equals_primal(b, causal):
+    """The matrix form of a mini-batch (dual form, walkthrough section 1.2.2: a
+    lower-triangular mask of zeros instead of explicit per-token gradients) gives
+    the same outputs as the token loop.  This pins the algebra the kernels use."""
+    B, H, T, d = 2, 3, 70, 16
+    q, k, v = _qkv(B, H, T, d)
+    eta = rng.uniform(0.1, 1.0, (B, H, T))
+    W0 = rng.standard_normal((H, d, d)) * 0.05
+    z, Wf = oracle.linear(q, k, v, W0, b=b, causal=causal, eta=eta)
+    for bi in range(B):
+        for h in range(H):
+            zr, Wr = _defs.dual_linear(q[bi, h], k[bi, h], v[bi, h], W0[h], eta[bi, h], b, causal)
+            np.testing.assert_allclose(z[bi, h], zr, atol=1e-11)
+            np.testing.assert_allclose(Wf[bi, h], Wr, atol=1e-11)
+
+
+def test_linear_eta_zero_is_identity():
+    B, H, T, d = 1, 2, 9, 4
+    q, k, v = _qkv(B, H, T, d)
+    W0 = rng.standard_normal((H, d, d))
+    z, Wf = oracle.linear(q, k, v, W0, b=3, eta_scalar=0.0)
+    np.testing.assert_allclose(Wf[0], W0, atol=0)
+    np.testing.assert_allclose(z[0], np.einsum("htd,hde->hte", q[0], W0), atol=1e-13)
+
+
+def test_linear_column_separable():
+    """Column j of W, E and Z only involves column j of W0 and V (plus the shared
+    Q, K, eta), so running on a column slice gives that slice of the full run."""
+    B, H, T, d = 1, 1, 30, 8
+    q, k, v = _qkv(B, H, T, d)
+    W0 = rng.standard_normal((H, d, d)) * 0.1
+    z, Wf = oracle.linear(q, k, v, W0, b=4)
+    cols = [1, 5, 6]
+    # pad the sliced problem back to d columns with zeros so shapes stay square
+    W0s = np.zeros_like(W0); W0s[..., cols] = W0[..., cols]
+    vs = np.zeros_like(v); vs[..., cols] = v[..., cols]
+    zs, Ws = oracle.linear(q, k, vs, W0s, b=4)
+    np.testing.assert_allclose(zs[..., cols], z[..., cols], atol=1e-12)
+    np.testing.assert_allclose(Ws[..., cols], Wf[..., cols], atol=1e-12)
+
+
+def test_linear_split_run_continues():
+    """Passing W_final back as W0 continues the sequence (chunked prefill) when the
+    split point is a multiple of b."""
+    B, H, T, d, b = 2, 2, 48, 8, 8
+    q, k, v = _qkv(B, H, T, d)
+    W0 = rng.standard_normal((B, H, d, d)) * 0.1
+    z, Wf = oracle.linear(q, k, v, W0, b=b)
+    z1, W1 = oracle.linear(q[:, :, :24], k[:, :, :24], v[:, :, :24], W0, b=b)
+    z2, W2 = oracle.linear(q[:, :, 24:], k[:, :, 24:], v[:, :, 24:], W1, b=b)
+    np.testing.assert_allclose(np.concatenate([z1, z2], 2), z, atol=1e-12)
+    np.testing.assert_allclose(W2, Wf, atol=1e-12)
+
+
+def test_linear_shared_vs_per_batch_w0():
+    B, H, T, d = 3, 2, 10, 4
+    q, k, v = _qkv(B, H, T, d)
+    W0 = rng.standard_normal((H, d, d))
+    z1, W1 = oracle.linear(q, k, v, W0, b=3)
+    z2, W2 = oracle.linear(q, k, v, np.broadcast_to(W0, (B, H, d, d)).copy(), b=3)
+    np.testing.assert_array_equal(z1, z2)
+    np.testing.assert_array_equal(W1, W2)
+
+
+# ------------------------------------------------------------------ TTT-MLP
+
+
+def test_mlp_gradient_matches_finite_differences():
+    """One mini-batch step: W_out = W0 - grad(sum_s eta_s l_s)(W0) with the hand
+    gradient inside the oracle; compare every parameter entry with central finite
+    differences of the plain forward loss (h = 1e-6)."""
+    B, H, T, d, m = 1, 1, 3, 4, 16
+    q, k, v = _qkv(B, H, T, d)
+    W1, c1, W2, c2 = _mlp_params(H, d, m)
+    eta = np.array([[[0.3, 0.7, 1.1]]])
+    _, W1o, c1o, W2o, c2o = oracle.mlp(q, k, v, W1, c1, W2, c2, b=T, causal=True, eta=eta)
+    sig = lambda x: 1 / (1 + np.exp(-x))
+
+    def loss(P):
+        a, ca, bm, cb = P
+        tot = 0.0
+        for s in range(T):
+            h = k[0, 0, s] @ a + ca
+            out = (h * sig(h)) @ bm + cb
+            tot += eta[0, 0, s] * 0.5 * np.sum((out - v[0, 0, s]) ** 2)
+        return tot
+
+    P = [W1[0].copy(), c1[0].copy(), W2[0].copy(), c2[0].copy()]
+    got = [W1[0] - W1o[0, 0], c1[0] - c1o[0, 0], W2[0] - W2o[0, 0], c2[0] - c2o[0, 0]]
+    hstep = 1e-6
+    for pi in range(4):
+        fd = np.zeros_like(P[pi])
+        for idx in np.ndindex(P[pi].shape):
+            Pp = [p.copy() for p in P]; Pm = [p.copy() for p in P]
+            Pp[pi][idx] += hstep; Pm[pi][idx] -= hstep
+            fd[idx] = (loss(Pp) - loss(Pm)) / (2 * hstep)
+        np.testing.assert_allclose(got[pi], fd, rtol=1e-7, atol=1e-9)
+
+
+@pytest.mark.parametrize("T,b,causal", [(7, 1, True), (7, 3, True), (8, 4, False),
+                                        (7, 7, False), (6, 10, True)])
+def test_mlp_matches_definition_autograd(T, b, causal):
+    B, H, d, m = 1, 1, 3, 8
+    q, k, v = _qkv(B, H, T, d)
+    W1, c1, W2, c2 = _mlp_params(H, d, m)
+    eta = rng.uniform(0.1, 1.0, (B, H, T))
+    z, W1o, c1o, W2o, c2o = oracle.mlp(q, k, v, W1, c1, W2, c2, b=b, causal=causal, eta=eta)
+    t = lambda a: torch.tensor(a)
+    zr, Pr = _defs.definition_autograd(_defs.f_mlp, [t(W1[0]), t(c1[0]), t(W2[0]), t(c2[0])],
+                                       t(q[0, 0]), t(k[0, 0]), t(v[0, 0]), t(eta[0, 0]), b, causal)
+    np.testing.assert_allclose(z[0, 0], zr.numpy(), atol=1e-12)
+    for got, ref in zip([W1o, c1o, W2o, c2o], Pr):
+        np.testing.assert_allclose(got[0, 0], ref.numpy(), atol=1e-12)
+
+
+@pytest.mark.parametrize("b,causal", [(1, True), (16, True), (6, True), (16, False), (40, False)])
+def test_mlp_dual_form_equals_primal(b, causal):
+    B, H, T, d, m = 1, 2, 41, 8, 32
+    q, k, v = _qkv(B, H, T, d)
+    W1, c1, W2, c2 = _mlp_params(H, d, m, scale=0.2)
+    eta = rng.uniform(0.02, 0.15, (B, H, T))   # keeps the inner dynamics bounded
+    z, W1o, c1o, W2o, c2o = oracle.mlp(q, k, v, W1, c1, W2, c2, b=b, causal=causal, eta=eta)
+    for h in range(H):
+        zr, (a, ca, bm, cb) = _defs.dual_mlp(q[0, h], k[0, h], v[0, h], W1[h], c1[h], W2[h],
+                                             c2[h], eta[0, h], b, causal)
+        np.testing.assert_allclose(z[0, h], zr, atol=1e-11)
+        for got, ref in zip([W1o, c1o, W2o, c2o], [a, ca, bm, cb]):
+            np.testing.assert_allclose(got[0, h], ref, atol=1e-11)
+
+
+def test_mlp_full_batch_is_one_gd_step():
+    B, H, T, d, m = 2, 1, 9, 4, 16
+    q, k, v = _qkv(B, H, T, d)
+    W1, c1, W2, c2 = _mlp_params(H, d, m)
+    z, W1o, c1o, W2o, c2o = oracle.mlp(q, k, v, W1, c1, W2, c2, b=T, causal=False,
+                                       eta_scalar=1.0)
+    for bi in range(B):
+        P = [torch.tensor(p[0], requires_grad=True) for p in (W1, c1, W2, c2)]
+        K, V, Q = (torch.tensor(x[bi, 0]) for x in (k, v, q))
+        L = 0.5 * ((_defs.f_mlp(K, P) - V) ** 2).sum()
+        gs = torch.autograd.grad(L, P)
+        P1 = [(p - g).detach() for p, g in zip(P, gs)]
+        for got, ref in zip([W1o, c1o, W2o, c2o], P1):
+            np.testing.assert_allclose(got[bi, 0], ref.numpy(), atol=1e-12)
+        np.testing.assert_allclose(z[bi, 0], _defs.f_mlp(Q, P1).numpy(), atol=1e-12)
+
+
+def test_mlp_eta_zero_is_identity():
+    B, H, T, d, m = 1, 1, 5, 4, 8
+    q, k, v = _qkv(B, H, T, d)
+    W1, c1, W2, c2 = _mlp_params(H, d, m)
+    z, W1o, *_ = oracle.mlp(q, k, v, W1, c1, W2, c2, b=2, eta_scalar=0.0)
+    np.testing.assert_array_equal(W1o[0], W1)
+    P = [torch.tensor(p[0]) for p in (W1, c1, W2, c2)]
+    np.testing.assert_allclose(z[0, 0], _defs.f_mlp(torch.tensor(q[0, 0]), P).numpy(), atol=1e-13)
+
+
+def test_empty_sequence():
+    q = np.zeros((1, 1, 0, 4))
+    W0 = rng.standard_normal((1, 4, 4))
+    z, Wf = oracle.linear(q, q, q, W0, b=4)
+    assert z.shape == (1, 1, 0, 4)
+    np.testing.assert_array_equal(Wf[0], W0)
