@@ -1,0 +1,359 @@
+"""Benchmark of the TTT layer forward on GB300: tokens/s (B*H*T per second).
+
+    python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one forward of the whole layer (one kernel launch) over one batch of
+synthetic inputs already resident in HBM; the L2 is flushed (a 256 MiB write,
+larger than the 129 MB L2) before every timed step.  Device time comes from CUDA
+events on the launching stream.  Rank 0 prints one JSON line.
+
+Under torchrun every rank runs the same workload on its own GPU (independent
+(batch, head) chains, no data-path collective: weak scaling); the step time is the
+maximum over ranks.
+
+--impl reference times the fp64 CPU oracle (the only reference this method has)
+on the host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "TTT layer fwd tokens/s (B·H·T) and TFLOP/s vs GB300 bf16 dense peak, 1 GPU"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------- work model
+
+
+def flops_per_token_head(inp):
+    """Algorithmic FLOPs of one token-head (masked products counted exactly:
+    (b+1)/2 visible pairs per token in a causal block of b)."""
+    d, m, b = inp.d, inp.m, inp.b
+    if inp.kind == "linear":
+        # E = K W, update K^T Et, Q W (2d^2 each); causal: masked (Q K^T) and its product
+        # with Et over (b+1)/2 visible pairs (2d each); non-causal: Z = Q W_end
+        return 6 * d * d + (2 * (b + 1) * d if inp.causal else 0)
+    # MLP: 7 products of 2dm (K W1, A W2, E W2^T, two updates, Q W1, A_q W2) + masked terms
+    if inp.causal:
+        return 14 * d * m + 2 * (b + 1) * (d + m)
+    return 14 * d * m + 2 * (d + m)
+
+
+def bytes_per_launch(inp):
+    """Algorithmic HBM bytes of one launch: q, k, v read once, z written once,
+    per-token eta read, initial weights read once per head, final weights written."""
+    es = inp.q.element_size()
+    BH, T, d = inp.B * inp.H, inp.T, inp.d
+    n = BH * T * d * es * 4
+    if inp.eta is not None:
+        n += BH * T * 4
+    nparam = sum(p.numel() for p in inp.params.values()) // inp.H  # one head's set
+    n += inp.H * nparam * 4 + BH * nparam * 4
+    return n
+
+
+# --------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.out)) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+
+
+def run_ours(args, rank, world, inp, peaks):
+    from test_sequence_layers_gb300 import abi, build
+    build.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    eta = inp.eta.to(dev) if inp.eta is not None else None
+    params = {n: p.to(dev) for n, p in inp.params.items()}
+    z = torch.empty_like(q)
+    B, H, d = inp.B, inp.H, inp.d
+    if inp.kind == "linear":
+        outs = torch.empty((B, H, d, d), device=dev)
+
+        def step(qq=q, kk=k, vv=v, ee=eta, zz=z):
+            abi.ttt_linear_fwd(qq, kk, vv, params["W0"], inp.b, inp.causal, eta=ee,
+                               eta_scalar=inp.eta_scalar, z=zz, W_out=outs)
+        out_bytes = [z, outs]
+    else:
+        m = inp.m
+        outs = (torch.empty((B, H, d, m), device=dev), torch.empty((B, H, m), device=dev),
+                torch.empty((B, H, m, d), device=dev), torch.empty((B, H, d), device=dev))
+
+        def step(qq=q, kk=k, vv=v, ee=eta, zz=z):
+            abi.ttt_mlp_fwd(qq, kk, vv, params["W1"], params["c1"], params["W2"], params["c2"],
+                            inp.b, inp.causal, eta=ee, eta_scalar=inp.eta_scalar, z=zz, outs=outs)
+        out_bytes = [z, *outs]
+
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        flush.add_(1.0)
+        step()
+    abi.ttt_sync_status()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    n0 = abi.ttt_launch_count()
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            flush.add_(1.0)  # evict the inputs from L2 (outside the timed events)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    launches = abi.ttt_launch_count() - n0
+    abi.ttt_sync_status()
+    if world > 1:
+        torch.distributed.barrier()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(times)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the same call with host buffers: pinned host -> device
+    # copies of the step's inputs, the forward, device -> host copies of z and the
+    # final weights, all inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
+        he = inp.eta.pin_memory() if inp.eta is not None else None
+        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out_bytes]
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        de = torch.empty_like(eta) if eta is not None else None
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            if de is not None:
+                de.copy_(he, non_blocking=True)
+            step(dq, dk, dv, de, z)
+            for h, t in zip(hout, out_bytes):
+                h.copy_(t, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ne = max(3, min(args.steps, 10))
+        t0 = time.perf_counter()
+        for _ in range(ne):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / ne
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in (inp.q, inp.k, inp.v))
+        h2d += inp.eta.numel() * 4 if inp.eta is not None else 0
+        d2h = sum(t.numel() * t.element_size() for t in out_bytes)
+        e2e = {"value": world * inp.token_heads / (e2e_ms / 1e3), "unit": UNIT,
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    clocks = clk.summary()
+    return ms, times, launches, e2e, clocks
+
+
+# -------------------------------------------------------------- CPU baseline
+
+
+def oracle_sample(inp, budget_s):
+    """Times the fp64 oracle on whole (batch, head) chains of the workload, adding
+    chains until about budget_s of CPU work; returns (token-heads/s, threads, desc)."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    BH = inp.B * inp.H
+    n = min(BH, threads)
+    done, elapsed = 0, 0.0
+    while elapsed < budget_s and done < BH:
+        take = min(n, BH - done)
+        sel = list(range(done, done + take))
+        flat = lambda x: x.reshape(-1, *x.shape[2:])[sel].unsqueeze(0)
+        q, k, v = flat(inp.q), flat(inp.k), flat(inp.v)
+        eta = flat(inp.eta) if inp.eta is not None else None
+        t0 = time.perf_counter()
+        if inp.kind == "linear":
+            W0 = torch.stack([inp.params["W0"][c % inp.H] for c in sel]).unsqueeze(0)
+            oracle.linear(q, k, v, W0, inp.b, inp.causal, eta=eta, eta_scalar=inp.eta_scalar,
+                          threads=threads)
+        else:
+            P = [torch.stack([inp.params[nm][c % inp.H] for c in sel]).unsqueeze(0)
+                 for nm in ("W1", "c1", "W2", "c2")]
+            oracle.mlp(q, k, v, *P, inp.b, inp.causal, eta=eta, eta_scalar=inp.eta_scalar,
+                       threads=threads)
+        elapsed += time.perf_counter() - t0
+        done += take
+        n = min(2 * n, BH)
+    th = done * inp.T
+    return th / elapsed, threads, f"{done} of {BH} (batch, head) chains, full T={inp.T}, " \
+                                  f"{elapsed:.1f} s of oracle time"
+
+
+# ---------------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="linear_125m")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group(backend)
+
+    from test_sequence_layers_gb300 import synth
+    inp = synth.workload(args.workload)
+    peaks = load_peaks()
+    flops = flops_per_token_head(inp) * inp.token_heads
+    config = {"workload": args.workload, "kind": inp.kind, "B": inp.B, "H": inp.H, "T": inp.T,
+              "d": inp.d, "m": inp.m or None, "mini_batch": inp.b, "causal": inp.causal,
+              "eta": "per-token sigmoid(g)" if inp.eta is not None else inp.eta_scalar,
+              "io_dtype": str(inp.q.dtype).replace("torch.", ""),
+              "state_dtype": "float32", "l2": "flushed before every timed step (256 MiB write)",
+              "parallelism": f"weak: every rank runs its own {inp.B}x{inp.H} chains"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = []
+        threads, desc = 0, ""
+        for _ in range(args.warmup + args.steps):
+            v, threads, desc = oracle_sample(inp, budget_s=max(0.5, args.cpu_budget / 10))
+            steps.append(v)
+        val = statistics.mean(steps[args.warmup:])
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": inp.token_heads / val * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config,
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    ms, times, launches, e2e, clocks = run_ours(args, rank, world, inp, peaks)
+    value = world * inp.token_heads / (ms / 1e3)
+    tflops = flops / (ms * 1e-3) / 1e12
+    nbytes = bytes_per_launch(inp)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    if inp.kind == "linear":
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"]}
+    else:
+        roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"]}
+    roof.update({"traffic": None, "peak_source": peaks["source"],
+                 "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+                 "kernel": "ttt_linear_bf16_kernel" if inp.kind == "linear" else "ttt_mlp_bf16_kernel",
+                 "launch_ms_mean": ms, "launch_ms_min": min(times)})
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if inp.q.dtype == torch.bfloat16 else "f32",
+            "data": "synthetic (seeded N(0,1) q,k,v with unit-norm q,k; N(0,0.02^2) weights)",
+            "config": config, "tflops": tflops,
+            "tflops_frac_of_bf16_peak": tflops / peaks["bf16_tflops"], "hbm_gbs": gbs,
+            "roofline": roof, "gpu_launches": launches, "clocks": clocks}
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        v, threads, desc = oracle_sample(inp, args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,129 @@
+/*
+ * ttt.h -- C ABI of libttt: forward pass (prefill / inference) of a
+ * Test-Time-Training (TTT) layer on one NVIDIA GB300 (sm_103a).
+ *
+ * The layer.  For every (batch, head) sequence the hidden state is the weight set W
+ * of a small inner model f(x; W).  W starts at W0 and is trained on the sequence
+ * itself by gradient descent on the reconstruction loss
+ *     l_t(W) = 1/2 || f(k_t; W) - v_t ||^2
+ * ("Fast weights 与 TTT layers", opening formula; "TTT：Test-Time Training",
+ * section TTT, MSE loss).  Tokens are taken in consecutive mini-batches of b
+ * tokens; every token of a mini-batch takes its gradient at the W that the previous
+ * mini-batch left ("Learning to (Learn at Test Time)" walkthrough, section 1.2.2,
+ * mini-batch gradient descent, formula 6).  The output is z_t = f(q_t; W_t)
+ * (same walkthrough, section 1.2, output rule), where
+ *   causal = 1:  W_t = W_start - sum_{s in t's mini-batch, s <= t} eta_s grad l_s(W_start)
+ *                (the cumulative-sum channel of section 1.2.2: W_t includes token
+ *                t's own write);
+ *   causal = 0:  every query of a mini-batch reads the W at the end of that
+ *                mini-batch (b = T gives one full-batch step, the vision variant of
+ *                the ViT3 article, observation 2).
+ * b = 1 is the delta rule ("Fast weights 与 TTT layers", section 1).
+ *
+ * Inner models (walkthrough section 2.2.1; ViT3 article, observation 4):
+ *   ttt_linear_fwd:  f(x; W) = x W,                      W in R^{d x d}
+ *   ttt_mlp_fwd:     f(x) = SiLU(x W1 + c1) W2 + c2,      W1 d x m, W2 m x d
+ * Row convention throughout: a token x is a 1 x d row vector.
+ *
+ * Conventions shared by every entry point
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no device memory; it keeps one small status word per device.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream) and runs asynchronously.  The return value reports
+ *     argument validation and launch errors synchronously.  A kernel-side wait that
+ *     timed out (never expected; every on-chip wait is bounded to about 2 s) is
+ *     reported by ttt_sync_status().
+ *   - Layouts are C-contiguous: q, k, v, z are [B, H, T, d] in io_dtype; eta is
+ *     [B, H, T] fp32; weights are fp32.
+ *   - Alignment: q, k, v, z must be 16-byte aligned (TTT_ERR_ALIGN otherwise);
+ *     eta and the fp32 weight arrays 4-byte aligned.
+ *   - T may be 0 (then only the final weights are written, equal to the initial
+ *     ones) and need not be a multiple of b: the last mini-batch is shorter.
+ *   - Final-weight outputs may be NULL (not written).  They may alias the
+ *     corresponding initial-weight inputs when those are given per (batch, head)
+ *     (in-place continuation of a sequence); they may not overlap shared
+ *     ([H, ...]) initial weights (TTT_ERR_ARG).
+ */
+#ifndef TTT_H_
+#define TTT_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TTT_OK = 0,
+    TTT_ERR_ARG = -1,          /* null / negative / inconsistent argument            */
+    TTT_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. d not in the set)   */
+    TTT_ERR_ALIGN = -3,        /* pointer misaligned for the bulk-copy engine         */
+    TTT_ERR_LAUNCH = -4,       /* CUDA reported an error at or before launch          */
+    TTT_ERR_TIMEOUT = -5       /* a kernel wait ran out (reported by ttt_sync_status) */
+} ttt_status;
+
+typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
+
+/* TTT-Linear problem description. */
+typedef struct {
+    int B, H, T, d;            /* batch, heads, tokens, head dim (d in {16,32,64,128}) */
+    int mini_batch;            /* b >= 1                                               */
+    int causal;                /* 1 causal, 0 non-causal (queries read block-end W)    */
+    ttt_dtype io_dtype;        /* dtype of q, k, v and z                               */
+    long long w0_batch_stride; /* elements between batches of W0; 0 = W0 is [H,d,d]
+                                  shared by every batch entry, H*d*d = [B,H,d,d]       */
+} ttt_linear_desc;
+
+/*
+ * TTT-Linear forward.
+ *   q, k, v : [B,H,T,d] io_dtype (queries, keys = training view, values = labels)
+ *   eta     : [B,H,T] fp32 per-token learning rate of the writing token, or NULL to
+ *             use eta_scalar for every token (walkthrough section 2.2.3)
+ *   W0      : fp32 initial weights, W0[i][j] multiplies input i into output j
+ *   z       : [B,H,T,d] io_dtype output
+ *   W_out   : [B,H,d,d] fp32 final weights, or NULL
+ * io_dtype TTT_BF16 runs the tensor-core path: bf16 operands, fp32 accumulation and
+ * fp32 weight state.  TTT_F32 runs an fp32 CUDA-core path (no reduced precision).
+ */
+ttt_status ttt_linear_fwd(const ttt_linear_desc *desc,
+                          const void *q, const void *k, const void *v,
+                          const float *eta, float eta_scalar,
+                          const float *W0, void *z, float *W_out, void *stream);
+
+/* TTT-MLP problem description. */
+typedef struct {
+    int B, H, T, d, m;         /* d in {16,32,64}; m = hidden width, multiple of 16    */
+    int mini_batch;            /* b >= 1                                               */
+    int causal;
+    ttt_dtype io_dtype;
+    int params_per_batch;      /* 0: W1,c1,W2,c2 are [H,...] shared over the batch;
+                                  1: they are [B,H,...]                                */
+} ttt_mlp_desc;
+
+/*
+ * TTT-MLP forward, f(x) = SiLU(x W1 + c1) W2 + c2 (SiLU(h) = h * sigmoid(h)).
+ *   W1 [..,d,m], c1 [..,m], W2 [..,m,d], c2 [..,d] fp32 initial inner weights;
+ *   the *_out arrays are [B,H,...] fp32 final weights (each may be NULL).
+ * Other arguments as for ttt_linear_fwd.
+ */
+ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc,
+                       const void *q, const void *k, const void *v,
+                       const float *eta, float eta_scalar,
+                       const float *W1, const float *c1, const float *W2, const float *c2,
+                       void *z, float *W1_out, float *c1_out, float *W2_out, float *c2_out,
+                       void *stream);
+
+/* Waits for `stream`, then reports (and clears) a kernel wait timeout recorded on
+ * the current device, or a CUDA error seen while waiting. */
+ttt_status ttt_sync_status(void *stream);
+
+/* Static description of a status code. */
+const char *ttt_status_str(ttt_status s);
+
+/* Number of kernel launches this library has enqueued on the calling process
+ * (all devices); used to count this library's launches inside a timed region. */
+unsigned long long ttt_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTT_H_ */

@@ -1,0 +1,173 @@
+"""ctypes binding of libttt (include/ttt.h): argument marshalling only.
+
+Every step of the layer runs in the CUDA library; this module checks shapes and
+dtypes, allocates outputs with PyTorch (device memory and streams are PyTorch's
+job here) and passes raw pointers.  There is no fallback: if the library is
+missing or a tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libttt.so")
+
+TTT_F32, TTT_BF16 = 0, 1
+STATUS = {0: "TTT_OK", -1: "TTT_ERR_ARG", -2: "TTT_ERR_UNSUPPORTED", -3: "TTT_ERR_ALIGN",
+          -4: "TTT_ERR_LAUNCH", -5: "TTT_ERR_TIMEOUT"}
+
+# every symbol include/ttt.h declares
+EXPORTS = ("ttt_linear_fwd", "ttt_mlp_fwd", "ttt_sync_status", "ttt_status_str",
+           "ttt_launch_count")
+
+
+class LinearDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
+                ("d", ctypes.c_int), ("mini_batch", ctypes.c_int), ("causal", ctypes.c_int),
+                ("io_dtype", ctypes.c_int), ("w0_batch_stride", ctypes.c_longlong)]
+
+
+class MlpDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
+                ("d", ctypes.c_int), ("m", ctypes.c_int), ("mini_batch", ctypes.c_int),
+                ("causal", ctypes.c_int), ("io_dtype", ctypes.c_int),
+                ("params_per_batch", ctypes.c_int)]
+
+
+class TTTError(RuntimeError):
+    def __init__(self, fn, rc):
+        self.code = rc
+        super().__init__(f"{fn} returned {STATUS.get(rc, rc)}: {status_str(rc)}")
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libttt.so is missing ({LIB_PATH}); run "
+                               "`python -m test_sequence_layers_gb300.build` first")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, fp, f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float
+        L.ttt_linear_fwd.argtypes = [ctypes.POINTER(LinearDesc), vp, vp, vp, fp, f, fp, vp, fp, vp]
+        L.ttt_linear_fwd.restype = ctypes.c_int
+        L.ttt_mlp_fwd.argtypes = [ctypes.POINTER(MlpDesc), vp, vp, vp, fp, f, fp, fp, fp, fp,
+                                  vp, fp, fp, fp, fp, vp]
+        L.ttt_mlp_fwd.restype = ctypes.c_int
+        L.ttt_sync_status.argtypes = [vp]
+        L.ttt_sync_status.restype = ctypes.c_int
+        L.ttt_status_str.argtypes = [ctypes.c_int]
+        L.ttt_status_str.restype = ctypes.c_char_p
+        L.ttt_launch_count.argtypes = []
+        L.ttt_launch_count.restype = ctypes.c_ulonglong
+        _lib = L
+    return _lib
+
+
+def status_str(rc: int) -> str:
+    return lib().ttt_status_str(rc).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_tokens(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (no CPU path)")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B,H,T,d] tensor")
+    if not (q.shape == k.shape == v.shape and q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share shape and dtype")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q, k, v must be bfloat16 or float32")
+    return TTT_BF16 if q.dtype == torch.bfloat16 else TTT_F32
+
+
+def _f32(t, name):
+    if t is None:
+        return None
+    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    return t
+
+
+def ttt_linear_fwd(q, k, v, W0, mini_batch, causal=True, eta=None, eta_scalar=1.0,
+                   z=None, W_out=None, want_W=True, stream=None):
+    """TTT-Linear forward.  q,k,v: [B,H,T,d] bf16 or fp32 CUDA tensors; W0: fp32
+    [H,d,d] (shared over the batch) or [B,H,d,d]; eta: fp32 [B,H,T] or None.
+    Returns (z, W_final or None)."""
+    io = _check_tokens(q, k, v)
+    B, H, T, d = q.shape
+    W0 = _f32(W0, "W0")
+    eta = _f32(eta, "eta")
+    if W0.shape == (H, d, d):
+        w0s = 0
+    elif W0.shape == (B, H, d, d):
+        w0s = H * d * d
+    else:
+        raise ValueError("W0 must be [H,d,d] or [B,H,d,d]")
+    if z is None:
+        z = torch.empty_like(q)
+    if W_out is None and want_W:
+        W_out = torch.empty((B, H, d, d), device=q.device, dtype=torch.float32)
+    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, w0s)
+    rc = lib().ttt_linear_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(eta),
+                              float(eta_scalar), _ptr(W0), _ptr(z), _ptr(W_out), _stream(stream))
+    if rc != 0:
+        raise TTTError("ttt_linear_fwd", rc)
+    return z, W_out
+
+
+def ttt_mlp_fwd(q, k, v, W1, c1, W2, c2, mini_batch, causal=True, eta=None, eta_scalar=0.1,
+                z=None, outs=None, want_W=True, stream=None):
+    """TTT-MLP forward, f(x) = SiLU(x W1 + c1) W2 + c2.  Parameters fp32, per head
+    ([H,...]) or per (batch, head) ([B,H,...]).  Returns (z, (W1,c1,W2,c2) final or None)."""
+    io = _check_tokens(q, k, v)
+    B, H, T, d = q.shape
+    W1, c1, W2, c2 = (_f32(t, n) for t, n in ((W1, "W1"), (c1, "c1"), (W2, "W2"), (c2, "c2")))
+    eta = _f32(eta, "eta")
+    m = W1.shape[-1]
+    per_batch = 1 if W1.dim() == 4 else 0
+    lead = (B, H) if per_batch else (H,)
+    if (W1.shape != lead + (d, m) or c1.shape != lead + (m,) or W2.shape != lead + (m, d)
+            or c2.shape != lead + (d,)):
+        raise ValueError("inner weights must be W1 [..,d,m], c1 [..,m], W2 [..,m,d], c2 [..,d]")
+    if z is None:
+        z = torch.empty_like(q)
+    if outs is None and want_W:
+        dev = q.device
+        outs = (torch.empty((B, H, d, m), device=dev), torch.empty((B, H, m), device=dev),
+                torch.empty((B, H, m, d), device=dev), torch.empty((B, H, d), device=dev))
+    o = outs if outs is not None else (None, None, None, None)
+    desc = MlpDesc(B, H, T, d, m, int(mini_batch), 1 if causal else 0, io, per_batch)
+    rc = lib().ttt_mlp_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(eta),
+                           float(eta_scalar), _ptr(W1), _ptr(c1), _ptr(W2), _ptr(c2), _ptr(z),
+                           *(_ptr(t) for t in o), _stream(stream))
+    if rc != 0:
+        raise TTTError("ttt_mlp_fwd", rc)
+    return z, outs
+
+
+def ttt_sync_status(stream=None):
+    """Waits for the stream; raises TTTError if a kernel wait timed out."""
+    rc = lib().ttt_sync_status(_stream(stream))
+    if rc != 0:
+        raise TTTError("ttt_sync_status", rc)
+
+
+def ttt_launch_count() -> int:
+    return int(lib().ttt_launch_count())

@@ -1,0 +1,250 @@
+// ttt_api.cu -- the C ABI declared in include/ttt.h: argument validation, TMA
+// descriptor encoding, kernel dispatch and the per-device status word.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ttt.h"
+#include "ttt_internal.h"
+
+// Status word written by kernels whose bounded on-chip wait ran out (one per
+// device: every device that loads the library has its own copy).
+__device__ int g_ttt_status;
+
+namespace {
+
+std::atomic<unsigned long long> g_launches{0};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Address of this device's status word (looked up once per device).
+int *status_word()
+{
+    static std::mutex mu;
+    static int *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ttt_status) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<int *>(p);
+    }
+    return addr[dev];
+}
+
+// q/k/v viewed as a 3-D tensor [B*H][T][d] of bf16; box = 16 tokens x min(d,64)
+// features, swizzled to the box row length so that ldmatrix is conflict-free.
+bool encode_tokens(CUtensorMap *m, const void *ptr, int BH, int T, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)(d < 64 ? d : 64), 16, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle sw = d >= 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : d == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                            : CU_TENSOR_MAP_SWIZZLE_32B;
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+ttt_status code(int rc) { return static_cast<ttt_status>(rc); }
+
+}  // namespace
+
+extern "C" {
+
+ttt_status ttt_linear_fwd(const ttt_linear_desc *desc, const void *q, const void *k, const void *v,
+                          const float *eta, float eta_scalar, const float *W0, void *z,
+                          float *W_out, void *stream)
+{
+    if (!desc) return TTT_ERR_ARG;
+    const ttt_linear_desc D = *desc;
+    if (D.B < 1 || D.H < 1 || D.T < 0 || D.mini_batch < 1 || !W0) return TTT_ERR_ARG;
+    if (D.causal != 0 && D.causal != 1) return TTT_ERR_ARG;
+    if (D.io_dtype != TTT_F32 && D.io_dtype != TTT_BF16) return TTT_ERR_ARG;
+    if (D.T > 0 && (!q || !k || !v || !z)) return TTT_ERR_ARG;
+    if (D.d != 16 && D.d != 32 && D.d != 64 && D.d != 128) return TTT_ERR_UNSUPPORTED;
+    const long long dd = (long long)D.d * D.d;
+    if (D.w0_batch_stride != 0 && D.w0_batch_stride != (long long)D.H * dd) return TTT_ERR_ARG;
+    if ((long long)D.B * D.H > 0x7fffffffLL) return TTT_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16)) return TTT_ERR_ALIGN;
+    if (!aligned(W0, 4) || !aligned(eta, 4) || !aligned(W_out, 4)) return TTT_ERR_ALIGN;
+    if (W_out && D.w0_batch_stride == 0 &&
+        overlaps(W_out, sizeof(float) * dd * D.B * D.H, W0, sizeof(float) * dd * D.H))
+        return TTT_ERR_ARG;
+
+    ttt::LinearArgs a;
+    a.B = D.B;
+    a.H = D.H;
+    a.T = D.T;
+    a.d = D.d;
+    a.b = D.T > 0 && D.mini_batch > D.T ? D.T : D.mini_batch;  // b >= T is one block
+    a.causal = D.causal;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.eta = eta;
+    a.eta_scalar = eta_scalar;
+    a.W0 = W0;
+    a.w0_bstride = D.w0_batch_stride;
+    a.z = z;
+    a.W_out = W_out;
+    a.status = status_word();
+    a.stream = static_cast<cudaStream_t>(stream);
+    if (!a.status) return TTT_ERR_LAUNCH;
+
+    int rc;
+    if (D.io_dtype == TTT_BF16) {
+        CUtensorMap maps[3];
+        std::memset(maps, 0, sizeof(maps));
+        if (D.T > 0) {
+            const int BH = D.B * D.H;
+            if (!encode_tokens(&maps[0], q, BH, D.T, D.d) || !encode_tokens(&maps[1], k, BH, D.T, D.d) ||
+                !encode_tokens(&maps[2], v, BH, D.T, D.d))
+                return TTT_ERR_LAUNCH;
+        }
+        rc = ttt::launch_linear_bf16(a, maps);
+    } else {
+        rc = ttt::launch_linear_f32(a);
+    }
+    if (rc == 0) g_launches.fetch_add(1, std::memory_order_relaxed);
+    return code(rc);
+}
+
+ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc, const void *q, const void *k, const void *v,
+                       const float *eta, float eta_scalar, const float *W1, const float *c1,
+                       const float *W2, const float *c2, void *z, float *W1_out, float *c1_out,
+                       float *W2_out, float *c2_out, void *stream)
+{
+    if (!desc) return TTT_ERR_ARG;
+    const ttt_mlp_desc D = *desc;
+    if (D.B < 1 || D.H < 1 || D.T < 0 || D.mini_batch < 1 || D.m < 1) return TTT_ERR_ARG;
+    if (!W1 || !c1 || !W2 || !c2) return TTT_ERR_ARG;
+    if (D.causal != 0 && D.causal != 1) return TTT_ERR_ARG;
+    if (D.params_per_batch != 0 && D.params_per_batch != 1) return TTT_ERR_ARG;
+    if (D.io_dtype != TTT_F32 && D.io_dtype != TTT_BF16) return TTT_ERR_ARG;
+    if (D.T > 0 && (!q || !k || !v || !z)) return TTT_ERR_ARG;
+    if (D.d != 16 && D.d != 32 && D.d != 64) return TTT_ERR_UNSUPPORTED;
+    if (D.m % 16 != 0) return TTT_ERR_UNSUPPORTED;
+    if ((long long)D.B * D.H > 0x7fffffffLL) return TTT_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16)) return TTT_ERR_ALIGN;
+    const void *f32p[] = {eta, W1, c1, W2, c2, W1_out, c1_out, W2_out, c2_out};
+    for (const void *p : f32p)
+        if (!aligned(p, 4)) return TTT_ERR_ALIGN;
+    if (!D.params_per_batch) {
+        const size_t nH = (size_t)D.H, nBH = (size_t)D.B * D.H, dm = (size_t)D.d * D.m;
+        const struct { const void *o; size_t no; const void *i; size_t ni; } pairs[] = {
+            {W1_out, nBH * dm, W1, nH * dm}, {c1_out, nBH * D.m, c1, nH * D.m},
+            {W2_out, nBH * dm, W2, nH * dm}, {c2_out, nBH * D.d, c2, nH * D.d}};
+        for (const auto &pr : pairs)
+            if (pr.o && overlaps(pr.o, 4 * pr.no, pr.i, 4 * pr.ni)) return TTT_ERR_ARG;
+    }
+
+    ttt::MlpArgs a;
+    a.B = D.B;
+    a.H = D.H;
+    a.T = D.T;
+    a.d = D.d;
+    a.m = D.m;
+    a.b = D.T > 0 && D.mini_batch > D.T ? D.T : D.mini_batch;
+    a.causal = D.causal;
+    a.per_batch = D.params_per_batch;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.eta = eta;
+    a.eta_scalar = eta_scalar;
+    a.W1 = W1;
+    a.c1 = c1;
+    a.W2 = W2;
+    a.c2 = c2;
+    a.z = z;
+    a.W1o = W1_out;
+    a.c1o = c1_out;
+    a.W2o = W2_out;
+    a.c2o = c2_out;
+    a.status = status_word();
+    a.stream = static_cast<cudaStream_t>(stream);
+    if (!a.status) return TTT_ERR_LAUNCH;
+
+    int rc;
+    if (D.io_dtype == TTT_BF16) {
+        CUtensorMap maps[3];
+        std::memset(maps, 0, sizeof(maps));
+        if (D.T > 0) {
+            const int BH = D.B * D.H;
+            if (!encode_tokens(&maps[0], q, BH, D.T, D.d) || !encode_tokens(&maps[1], k, BH, D.T, D.d) ||
+                !encode_tokens(&maps[2], v, BH, D.T, D.d))
+                return TTT_ERR_LAUNCH;
+        }
+        rc = ttt::launch_mlp_bf16(a, maps);
+    } else {
+        rc = ttt::launch_mlp_f32(a);
+    }
+    if (rc == 0) g_launches.fetch_add(1, std::memory_order_relaxed);
+    return code(rc);
+}
+
+ttt_status ttt_sync_status(void *stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTT_ERR_LAUNCH;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_ttt_status, sizeof(int)) != cudaSuccess) return TTT_ERR_LAUNCH;
+    if (v != 0) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_ttt_status, &zero, sizeof(int));
+        return TTT_ERR_TIMEOUT;
+    }
+    return TTT_OK;
+}
+
+const char *ttt_status_str(ttt_status s)
+{
+    switch (s) {
+    case TTT_OK: return "ok";
+    case TTT_ERR_ARG: return "invalid argument";
+    case TTT_ERR_UNSUPPORTED: return "unsupported configuration";
+    case TTT_ERR_ALIGN: return "pointer misaligned (q, k, v, z need 16 bytes; fp32 arrays 4)";
+    case TTT_ERR_LAUNCH: return "CUDA error at launch";
+    case TTT_ERR_TIMEOUT: return "kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+unsigned long long ttt_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+"""The C-ABI library without a GPU: it loads, exports every function include/ttt.h
+declares, and rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from test_sequence_layers_gb300 import abi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return abi.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ttt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ttt_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared() == sorted(abi.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for rc in (0, -1, -2, -3, -4, -5):
+        assert abi.status_str(rc)
+    assert abi.status_str(7) == "unknown status"
+
+
+FAKE = 1 << 20  # an aligned address that is never dereferenced (validation fails first)
+
+
+def _lin(**kw):
+    d = dict(B=1, H=1, T=32, d=64, mini_batch=16, causal=1, io_dtype=abi.TTT_BF16,
+             w0_batch_stride=0)
+    d.update(kw)
+    return abi.LinearDesc(**d)
+
+
+def _call_lin(L, desc, q=FAKE, k=FAKE, v=FAKE, eta=None, W0=FAKE, z=FAKE, Wout=None):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.ttt_linear_fwd(ctypes.byref(desc) if desc is not None else None, vp(q), vp(k), vp(v),
+                            vp(eta), 1.0, vp(W0), vp(z), vp(Wout), None)
+
+
+def test_linear_rejects_bad_arguments(L):
+    assert L.ttt_linear_fwd(None, None, None, None, None, 1.0, None, None, None, None) == -1
+    assert _call_lin(L, _lin(B=0)) == -1
+    assert _call_lin(L, _lin(T=-1)) == -1
+    assert _call_lin(L, _lin(mini_batch=0)) == -1
+    assert _call_lin(L, _lin(causal=2)) == -1
+    assert _call_lin(L, _lin(io_dtype=5)) == -1
+    assert _call_lin(L, _lin(), q=None) == -1
+    assert _call_lin(L, _lin(), W0=None) == -1
+    assert _call_lin(L, _lin(w0_batch_stride=7)) == -1
+    assert _call_lin(L, _lin(d=48)) == -2
+    assert _call_lin(L, _lin(d=256)) == -2
+    assert _call_lin(L, _lin(), q=FAKE + 8) == -3
+    assert _call_lin(L, _lin(), z=FAKE + 2) == -3
+    assert _call_lin(L, _lin(), eta=FAKE + 2) == -3
+    # final weights may not overlap weights shared over the batch
+    assert _call_lin(L, _lin(B=2), W0=FAKE, Wout=FAKE + 64) == -1
+
+
+def _mlp(**kw):
+    d = dict(B=1, H=1, T=32, d=64, m=256, mini_batch=16, causal=1, io_dtype=abi.TTT_BF16,
+             params_per_batch=0)
+    d.update(kw)
+    return abi.MlpDesc(**d)
+
+
+def _call_mlp(L, desc, q=FAKE, W1=FAKE, c1=FAKE, W2=FAKE, c2=FAKE, W1o=None):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.ttt_mlp_fwd(ctypes.byref(desc), vp(q), vp(q), vp(q), None, 0.1, vp(W1), vp(c1),
+                         vp(W2), vp(c2), vp(FAKE), vp(W1o), None, None, None, None)
+
+
+def test_mlp_rejects_bad_arguments(L):
+    assert _call_mlp(L, _mlp(m=0)) == -1
+    assert _call_mlp(L, _mlp(), c1=None) == -1
+    assert _call_mlp(L, _mlp(params_per_batch=3)) == -1
+    assert _call_mlp(L, _mlp(d=128)) == -2
+    assert _call_mlp(L, _mlp(m=40)) == -2
+    assert _call_mlp(L, _mlp(), q=FAKE + 4) == -3
+    assert _call_mlp(L, _mlp(), W2=FAKE + 1) == -3
+    assert _call_mlp(L, _mlp(B=2), W1=FAKE, W1o=FAKE) == -1
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 1, 4, 16, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        abi.ttt_linear_fwd(q, q, q, torch.zeros(1, 16, 16), 4)

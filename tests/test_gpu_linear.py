@@ -1,0 +1,121 @@
+"""TTT-Linear on the GPU against the fp64 oracle (element by element), through the
+C ABI.  Small cases span several tiles and ragged tails; the full-size workloads
+run in the launch configuration the benchmark times and are compared on sampled
+(batch, head) chains, each over its whole sequence."""
+import numpy as np
+import pytest
+import torch
+
+from tests import gpu_common as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    G.ensure_built()
+
+
+def _check(inp, chains=None, per_batch_w0=False, tol=None):
+    tol = tol or G.tol_for(inp)
+    zg, Wg = G.gpu_linear(inp, per_batch_w0=per_batch_w0)
+    zr, Wr = G.oracle_linear(inp, chains)
+    if chains is not None:
+        zg, Wg = G.pick(zg, chains), G.pick(Wg, chains)
+    ez, eW = G.rel_err(zg, zr), G.rel_err(Wg, Wr)
+    assert ez <= tol and eW <= tol, (ez, eW, tol)
+    return ez, eW
+
+
+def test_tiny_fp32_workload():
+    """B1 H2 T64 d16 b16 causal fp32, eta 0.5 (fp32 path, 1e-4)."""
+    _check(G.synth.workload("linear_tiny_f32"), tol=G.TOL_F32)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("b,causal", [(16, True), (1, True), (5, True), (40, True),
+                                      (16, False), (7, False), (40, False)])
+def test_bf16_small(d, b, causal):
+    inp = G.synth.make("linear", B=2, H=3, T=75, d=d, b=b, causal=causal, eta=1.0, seed=d + b)
+    _check(inp)
+
+
+@pytest.mark.parametrize("d", [16, 64])
+@pytest.mark.parametrize("b,causal", [(16, True), (3, True), (24, False)])
+def test_fp32_small(d, b, causal):
+    inp = G.synth.make("linear", B=2, H=2, T=50, d=d, b=b, causal=causal, dtype=torch.float32,
+                       eta="sigmoid", seed=100 + d + b)
+    _check(inp)
+
+
+@pytest.mark.parametrize("T", [0, 1, 15, 16, 17, 33])
+def test_short_and_empty_sequences(T):
+    inp = G.synth.make("linear", B=1, H=2, T=T, d=64, b=16, causal=True, seed=7 + T)
+    _check(inp)
+
+
+def test_per_token_eta_and_per_batch_w0():
+    inp = G.synth.make("linear", B=3, H=2, T=130, d=64, b=16, causal=True, eta="sigmoid", seed=11)
+    _check(inp, per_batch_w0=True)
+
+
+def test_full_batch_noncausal_single_block():
+    """b = T: one full-batch GD step, every query reads the updated weights."""
+    inp = G.synth.make("linear", B=4, H=2, T=196, d=64, b=196, causal=False, seed=12)
+    _check(inp)
+
+
+def test_split_run_continues_sequence():
+    """W_final passed back as W0 continues the sequence (chunked prefill)."""
+    inp = G.synth.make("linear", B=2, H=2, T=96, d=64, b=16, causal=True, seed=13)
+    dev = torch.device("cuda")
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    W0 = inp.params["W0"].to(dev)
+    from test_sequence_layers_gb300 import abi
+    z, W = abi.ttt_linear_fwd(q, k, v, W0, 16)
+    z1, W1 = abi.ttt_linear_fwd(q[:, :, :48].contiguous(), k[:, :, :48].contiguous(),
+                                v[:, :, :48].contiguous(), W0, 16)
+    # continue in place: the final-weight buffer is the initial-weight input
+    z2, W2 = abi.ttt_linear_fwd(q[:, :, 48:].contiguous(), k[:, :, 48:].contiguous(),
+                                v[:, :, 48:].contiguous(), W1, 16, W_out=W1)
+    abi.ttt_sync_status()
+    assert torch.equal(torch.cat([z1, z2], 2), z)
+    assert torch.equal(W2, W)
+
+
+def test_deterministic():
+    inp = G.synth.make("linear", B=2, H=4, T=300, d=64, b=16, causal=True, seed=14)
+    a = G.gpu_linear(inp)
+    b = G.gpu_linear(inp)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------------ full workloads
+
+
+def test_workload_125m_layer_full():
+    """B8 H12 T2048 d64 b16 causal bf16, eta 1: every chain against the oracle."""
+    inp = G.synth.workload("linear_125m")
+    ez, eW = _check(inp)
+    print(f"linear_125m rel err z {ez:.3e} W {eW:.3e}")
+
+
+def test_workload_125m_delta_rule_b1():
+    """The b = 1 check of the 125M-layer shape (delta rule), B1 H12 T2048."""
+    inp = G.synth.workload("linear_125m_b1")
+    ez, eW = _check(inp)
+    print(f"linear_125m_b1 rel err z {ez:.3e} W {eW:.3e}")
+
+
+def test_workload_long_context_gated_sampled():
+    """B2 H32 T32768 with per-token eta = sigmoid(g): sampled chains, full length."""
+    inp = G.synth.workload("linear_long_gated")
+    ez, eW = _check(inp, chains=[0, 17, 63])
+    print(f"linear_long_gated rel err z {ez:.3e} W {eW:.3e}")
+
+
+def test_workload_vision_full_batch_sampled():
+    """B256 N196 H6, b = N, non-causal: sampled chains."""
+    inp = G.synth.workload("vision_linear")
+    ez, eW = _check(inp, chains=[0, 5, 777, 1535])
+    print(f"vision_linear rel err z {ez:.3e} W {eW:.3e}")
