@@ -82,30 +82,30 @@ def bytes_per_launch(inp):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling; summary() keeps the samples taken
+    inside the timed region [t0, t1] (host wall clock)."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.out = ""
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        return self
 
-    def __exit__(self, *exc):
-        self.out = ""
+    def stop(self):
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.out, _ = self.proc.communicate(timeout=5)
@@ -113,19 +113,41 @@ class ClockSampler:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
 
-    def summary(self):
+    @staticmethod
+    def _ts(s):
+        import datetime
+        try:
+            return datetime.datetime.strptime(s.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def summary(self, t0, t1):
         rows = [r for r in csv.reader(io.StringIO(self.out)) if len(r) >= 9]
-        if not rows:
+        inside = [r for r in rows if (lambda t: t is not None and t0 <= t <= t1)(self._ts(r[0]))]
+        use = inside or rows
+        if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v})
+        num = lambda x: float(x) if x.strip().replace(".", "", 1).isdigit() else None
+        sm = [v for v in (num(r[1]) for r in use) if v is not None]
+        mx = [v for v in (num(r[2]) for r in use) if v is not None]
+        pw = [v for v in (num(r[3]) for r in use) if v is not None]
+        reasons = sorted({n for r in use for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
 # ------------------------------------------------------------------ our arm
+
+
+def allreduce_max(x, dev):
+    """Maximum of a host float over ranks (device tensor for NCCL, host for gloo)."""
+    on = dev if torch.distributed.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=on)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 def run_ours(args, rank, world, inp, peaks):
@@ -164,27 +186,36 @@ def run_ours(args, rank, world, inp, peaks):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clk = ClockSampler(dev.index)
+    if not args.quick:
+        clk.start()
+    # keep the GPU busy (untimed) while the sampler starts up
+    t_spin = time.perf_counter()
+    while not args.quick and time.perf_counter() - t_spin < 0.6:
+        flush.add_(1.0)
+        step()
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     n0 = abi.ttt_launch_count()
-    with ClockSampler(dev.index) as clk:
-        for i in range(args.steps):
-            flush.add_(1.0)  # evict the inputs from L2 (outside the timed events)
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize()
+    w0 = time.time()
+    for i in range(args.steps):
+        flush.add_(1.0)  # evict the inputs from L2 (outside the timed events)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
     launches = abi.ttt_launch_count() - n0
+    clk.stop()
     abi.ttt_sync_status()
     if world > 1:
         torch.distributed.barrier()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = statistics.mean(times)
     if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = allreduce_max(ms, dev)
 
     # end to end through the same call with host buffers: pinned host -> device
     # copies of the step's inputs, the forward, device -> host copies of z and the
@@ -216,16 +247,14 @@ def run_ours(args, rank, world, inp, peaks):
         torch.cuda.synchronize()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / ne
         if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+            e2e_ms = allreduce_max(e2e_ms, dev)
         h2d = sum(x.numel() * x.element_size() for x in (inp.q, inp.k, inp.v))
         h2d += inp.eta.numel() * 4 if inp.eta is not None else 0
         d2h = sum(t.numel() * t.element_size() for t in out_bytes)
         e2e = {"value": world * inp.token_heads / (e2e_ms / 1e3), "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    clocks = clk.summary()
+    clocks = clk.summary(w0, w1)
     return ms, times, launches, e2e, clocks
 
 
@@ -271,14 +300,19 @@ def oracle_sample(inp, budget_s):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="linear_125m")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="warm-up and timed steps only (no clock spin, e2e or CPU baseline); "
+                         "used for profiler captures")
     args = ap.parse_args()
+    if args.quick:
+        args.no_e2e = args.no_cpu_baseline = True
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
