@@ -3,8 +3,9 @@
     python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl ours|reference]
 
 One step = one forward of the whole layer (one kernel launch) over one batch of
-synthetic inputs already resident in HBM; the L2 is flushed (a 256 MiB write,
-larger than the 129 MB L2) before every timed step.  Device time comes from CUDA
+synthetic inputs already resident in HBM; the L2 is flushed before every timed
+step (a 256 MiB write, larger than the 129 MB L2, then a 256 MiB read so the L2
+holds clean lines).  Device time comes from CUDA
 events on the launching stream.  Rank 0 prints one JSON line.
 
 Under torchrun every rank runs the same workload on its own GPU (independent
@@ -178,9 +179,18 @@ def run_ours(args, rank, world, inp, peaks):
                             inp.b, inp.causal, eta=ee, eta_scalar=inp.eta_scalar, z=zz, outs=outs)
         out_bytes = [z, *outs]
 
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_w = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def l2_flush():
+        # write a buffer larger than L2, then read another one so the L2 holds clean
+        # lines (no write-back of the flush traffic inside the timed launch)
+        flush_w.add_(1.0)
+        flush_out.copy_(flush_r.sum())
+
     for _ in range(args.warmup):
-        flush.add_(1.0)
+        l2_flush()
         step()
     abi.ttt_sync_status()
 
@@ -192,7 +202,7 @@ def run_ours(args, rank, world, inp, peaks):
     # keep the GPU busy (untimed) while the sampler starts up
     t_spin = time.perf_counter()
     while not args.quick and time.perf_counter() - t_spin < 0.6:
-        flush.add_(1.0)
+        l2_flush()
         step()
         torch.cuda.synchronize()
     if world > 1:
@@ -201,7 +211,7 @@ def run_ours(args, rank, world, inp, peaks):
     n0 = abi.ttt_launch_count()
     w0 = time.time()
     for i in range(args.steps):
-        flush.add_(1.0)  # evict the inputs from L2 (outside the timed events)
+        l2_flush()  # evict the inputs from L2 (outside the timed events)
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -332,7 +342,7 @@ def main():
               "d": inp.d, "m": inp.m or None, "mini_batch": inp.b, "causal": inp.causal,
               "eta": "per-token sigmoid(g)" if inp.eta is not None else inp.eta_scalar,
               "io_dtype": str(inp.q.dtype).replace("torch.", ""),
-              "state_dtype": "float32", "l2": "flushed before every timed step (256 MiB write)",
+              "state_dtype": "float32", "l2": "flushed before every timed step (256 MiB write + 256 MiB read)",
               "parallelism": f"weak: every rank runs its own {inp.B}x{inp.H} chains"}
 
     if args.impl == "reference":
