@@ -1,0 +1,120 @@
+"""TTT-MLP on the GPU against the fp64 oracle (element by element, final inner
+weights included), through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from tests import gpu_common as G
+from test_sequence_layers_gb300 import abi
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    G.ensure_built()
+
+
+def _check(inp, chains=None, tol=None, per_batch=False):
+    tol = tol or G.tol_for(inp)
+    if per_batch:
+        for n in ("W1", "c1", "W2", "c2"):
+            inp.params[n] = inp.params[n].expand(inp.B, *inp.params[n].shape).contiguous()
+    zg, Wg = G.gpu_mlp(inp)
+    if per_batch:
+        zr, Wr = _oracle_per_batch(inp)
+    else:
+        zr, Wr = G.oracle_mlp(inp, chains)
+    if chains is not None:
+        zg, Wg = G.pick(zg, chains), [G.pick(x, chains) for x in Wg]
+    assert np.isfinite(zr).all() and (zr.size == 0 or np.abs(zr).max() < 1e4), \
+        "reference diverged: choose a smaller inner learning rate"
+    errs = [G.rel_err(zg, zr)]
+    for got, ref, name in zip(Wg, Wr, ("W1", "c1", "W2", "c2")):
+        if np.abs(ref).max() > 0:
+            errs.append(G.rel_err(got, ref))
+    assert max(errs) <= tol, (errs, tol)
+    return errs
+
+
+def _oracle_per_batch(inp):
+    import oracle
+    P = [inp.params[n] for n in ("W1", "c1", "W2", "c2")]
+    z, *W = oracle.mlp(inp.q, inp.k, inp.v, *P, inp.b, inp.causal, eta=inp.eta,
+                       eta_scalar=inp.eta_scalar)
+    return z, W
+
+
+def _mlp_inputs(B, H, T, d, b, causal, dtype=torch.bfloat16, eta=0.1, seed=0, bias=0.0):
+    inp = G.synth.make("mlp", B=B, H=H, T=T, d=d, m=4 * d, b=b, causal=causal, dtype=dtype,
+                       eta=eta, seed=seed)
+    if bias:
+        g = torch.Generator().manual_seed(seed + 1000)
+        inp.params["c1"] = torch.randn(inp.params["c1"].shape, generator=g) * bias
+        inp.params["c2"] = torch.randn(inp.params["c2"].shape, generator=g) * bias
+    return inp
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("b,causal", [(16, True), (1, True), (5, True), (16, False),
+                                      (7, False), (40, False)])
+def test_bf16_small(d, b, causal):
+    inp = _mlp_inputs(2, 2, 75, d, b, causal, eta=0.05, seed=d + b, bias=0.1)
+    _check(inp)
+
+
+def test_bf16_per_token_eta_and_per_batch_params():
+    inp = _mlp_inputs(3, 2, 90, 64, 16, True, eta="sigmoid", seed=21, bias=0.1)
+    inp.eta = inp.eta * 0.1  # eta_t = 0.1 sigmoid(g_t): bounded dynamics
+    _check(inp, per_batch=True)
+
+
+@pytest.mark.parametrize("T", [0, 1, 15, 17])
+def test_short_and_empty_sequences(T):
+    inp = _mlp_inputs(1, 2, T, 64, 16, True, seed=30 + T)
+    _check(inp)
+
+
+@pytest.mark.parametrize("b,causal", [(16, True), (3, True), (8, False)])
+def test_fp32_small(b, causal):
+    inp = _mlp_inputs(2, 2, 40, 16, b, causal, dtype=torch.float32, eta=0.05, seed=40 + b, bias=0.1)
+    _check(inp, tol=G.TOL_F32)
+
+
+def test_causal_multichunk_minibatch_is_reported_unsupported():
+    inp = _mlp_inputs(1, 1, 64, 64, 32, True, seed=50)
+    with pytest.raises(abi.TTTError) as ei:
+        G.gpu_mlp(inp)
+    assert ei.value.code == -2
+
+
+def test_deterministic():
+    inp = _mlp_inputs(2, 2, 100, 64, 16, True, seed=51)
+    a = G.gpu_mlp(inp)
+    b = G.gpu_mlp(inp)
+    assert np.array_equal(a[0], b[0])
+    assert all(np.array_equal(x, y) for x, y in zip(a[1], b[1]))
+
+
+def test_workload_mlp_125m_finite_prefix():
+    """B8 H12 d64 m256 b16 causal at the specified eta = 0.1.  With these inputs the
+    plain inner gradient descent overflows after about 64 tokens (in fp64 too), so
+    the exact workload is compared over its first 48 tokens, every chain."""
+    inp = G.synth.workload("mlp_125m", T=48)
+    errs = _check(inp)
+    print("mlp_125m (T=48) rel err z, W1, c1, W2, c2:", errs)
+
+
+def test_workload_mlp_125m_shape_full_length_stable_eta():
+    """B8 H12 T2048 d64 m256 b16 causal with eta = 0.01 (bounded dynamics): sampled
+    chains over the full length."""
+    inp = G.synth.workload("mlp_125m", eta=0.01)
+    errs = _check(inp, chains=[0, 37, 95])
+    print("mlp_125m (eta 0.01) rel err z, W1, c1, W2, c2:", errs)
+
+
+def test_workload_vision_mlp_sampled():
+    """B256 N196 H6 d64 m256, b = N, non-causal, eta 1: sampled chains."""
+    inp = G.synth.workload("vision_mlp")
+    errs = _check(inp, chains=[0, 9, 1000, 1535])
+    print("vision_mlp rel err z, W1, W2:", errs)
