@@ -79,6 +79,24 @@ def bytes_per_launch(inp):
     return n
 
 
+def recorded_traffic(workload):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json), or
+    None when there is no record or the kernel sources changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(workload)
+    if not rec:
+        return None
+    m = hashlib.sha256()
+    for name in rec["sources"]:
+        with open(os.path.join(ROOT, "test_sequence_layers_gb300", "csrc", name), "rb") as f:
+            m.update(f.read())
+    return rec["dram_bytes_per_launch"] if m.hexdigest() == rec["sources_sha256"] else None
+
+
 # --------------------------------------------------------------------- clocks
 
 
@@ -377,7 +395,7 @@ def main():
     else:
         roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"]}
-    roof.update({"traffic": None, "peak_source": peaks["source"],
+    roof.update({"traffic": recorded_traffic(args.workload), "peak_source": peaks["source"],
                  "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
                  "kernel": "ttt_linear_bf16_kernel" if inp.kind == "linear" else "ttt_mlp_bf16_kernel",
                  "launch_ms_mean": ms, "launch_ms_min": min(times)})
