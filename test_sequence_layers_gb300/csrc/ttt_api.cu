@@ -55,15 +55,17 @@ int *status_word()
     return addr[dev];
 }
 
-// q/k/v viewed as a 3-D tensor [B*H][T][d] of bf16; box = 16 tokens x min(d,64)
+}  // namespace
+
+// q/k/v viewed as a 3-D tensor [B*H][T][d] of bf16; box = `rows` tokens x min(d,64)
 // features, swizzled to the box row length so that ldmatrix is conflict-free.
-bool encode_tokens(CUtensorMap *m, const void *ptr, int BH, int T, int d)
+bool ttt::encode_token_map(CUtensorMap *m, const void *ptr, int BH, int T, int d, int rows)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)(d < 64 ? d : 64), 16, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)(d < 64 ? d : 64), (cuuint32_t)rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapSwizzle sw = d >= 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : d == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -72,6 +74,8 @@ bool encode_tokens(CUtensorMap *m, const void *ptr, int BH, int T, int d)
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -128,19 +132,10 @@ ttt_status ttt_linear_fwd(const ttt_linear_desc *desc, const void *q, const void
     if (!a.status) return TTT_ERR_LAUNCH;
 
     int rc;
-    if (D.io_dtype == TTT_BF16) {
-        CUtensorMap maps[3];
-        std::memset(maps, 0, sizeof(maps));
-        if (D.T > 0) {
-            const int BH = D.B * D.H;
-            if (!encode_tokens(&maps[0], q, BH, D.T, D.d) || !encode_tokens(&maps[1], k, BH, D.T, D.d) ||
-                !encode_tokens(&maps[2], v, BH, D.T, D.d))
-                return TTT_ERR_LAUNCH;
-        }
-        rc = ttt::launch_linear_bf16(a, maps);
-    } else {
+    if (D.io_dtype == TTT_BF16)
+        rc = (a.b == 16 && a.d <= 64) ? ttt::launch_linear_b16(a) : ttt::launch_linear_bf16(a);
+    else
         rc = ttt::launch_linear_f32(a);
-    }
     if (rc == 0) g_launches.fetch_add(1, std::memory_order_relaxed);
     return code(rc);
 }
@@ -202,19 +197,10 @@ ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc, const void *q, const void *k, c
     if (!a.status) return TTT_ERR_LAUNCH;
 
     int rc;
-    if (D.io_dtype == TTT_BF16) {
-        CUtensorMap maps[3];
-        std::memset(maps, 0, sizeof(maps));
-        if (D.T > 0) {
-            const int BH = D.B * D.H;
-            if (!encode_tokens(&maps[0], q, BH, D.T, D.d) || !encode_tokens(&maps[1], k, BH, D.T, D.d) ||
-                !encode_tokens(&maps[2], v, BH, D.T, D.d))
-                return TTT_ERR_LAUNCH;
-        }
-        rc = ttt::launch_mlp_bf16(a, maps);
-    } else {
+    if (D.io_dtype == TTT_BF16)
+        rc = ttt::launch_mlp_bf16(a);
+    else
         rc = ttt::launch_mlp_f32(a);
-    }
     if (rc == 0) g_launches.fetch_add(1, std::memory_order_relaxed);
     return code(rc);
 }

@@ -32,11 +32,28 @@ struct MlpArgs {
     cudaStream_t stream;
 };
 
-// Each returns 0 or a negative ttt_status code; maps = q, k, v tensor maps.
-int launch_linear_bf16(const LinearArgs &a, const CUtensorMap *maps);
+// TMA descriptor of a bf16 token tensor viewed as [BH][T][d]: boxes of `rows`
+// tokens x min(d, 64) features, swizzled to the box row length, rows past T
+// zero-filled.  Returns false if the driver entry point is unavailable or rejects it.
+bool encode_token_map(CUtensorMap *m, const void *ptr, int BH, int T, int d, int rows);
+
+// q, k, v descriptors (zeroed, unused when T == 0); false on an encoding failure.
+inline bool encode_qkv(CUtensorMap *maps, const void *q, const void *k, const void *v, int BH, int T,
+                       int d, int rows)
+{
+    for (int i = 0; i < 3; ++i)
+        for (size_t j = 0; j < sizeof(CUtensorMap); ++j) reinterpret_cast<char *>(&maps[i])[j] = 0;
+    if (T == 0) return true;
+    return encode_token_map(&maps[0], q, BH, T, d, rows) && encode_token_map(&maps[1], k, BH, T, d, rows) &&
+           encode_token_map(&maps[2], v, BH, T, d, rows);
+}
+
+// Each returns 0 or a negative ttt_status code.
+int launch_linear_bf16(const LinearArgs &a);
+int launch_linear_b16(const LinearArgs &a);  // b = 16 specialisation (d <= 64)
 int launch_linear_f32(const LinearArgs &a);
 int launch_mlp_f32(const MlpArgs &a);
-int launch_mlp_bf16(const MlpArgs &a, const CUtensorMap *maps);
+int launch_mlp_bf16(const MlpArgs &a);
 // Largest d*m the fp32 MLP path holds on chip.
 bool mlp_f32_fits(int d, int m);
 

@@ -354,8 +354,10 @@ static int launch_t(const LinearArgs &a, const CUtensorMap *maps)
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
-int launch_linear_bf16(const LinearArgs &a, const CUtensorMap *maps)
+int launch_linear_bf16(const LinearArgs &a)
 {
+    CUtensorMap maps[3];
+    if (!encode_qkv(maps, a.q, a.k, a.v, a.B * a.H, a.T, a.d, 16)) return -4;
     switch (a.d) {
     case 16: return launch_t<16>(a, maps);
     case 32: return launch_t<32>(a, maps);

@@ -90,7 +90,9 @@ __device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r
                  : "memory");
 }
 
-__device__ __forceinline__ float sigmoid_f(float h) { return 1.f / (1.f + __expf(-h)); }
+// logistic function with the fast exponential and divide intrinsics (1 + e^-h
+// overflowing to +inf gives 0, the correct limit)
+__device__ __forceinline__ float sigmoid_f(float h) { return __fdividef(1.f, 1.f + __expf(-h)); }
 
 struct MlpParams {
     int H, T, b, causal, per_batch;
@@ -581,10 +583,12 @@ static int launch_mlp_t(const MlpArgs &a, const CUtensorMap *maps)
 
 // d in {16, 32, 64} with hidden width m = 4d; causal mini-batches longer than one
 // 16-token chunk are not implemented on this path (TTT_ERR_UNSUPPORTED).
-int launch_mlp_bf16(const MlpArgs &a, const CUtensorMap *maps)
+int launch_mlp_bf16(const MlpArgs &a)
 {
     if (a.m != 4 * a.d) return -2;
     if (a.causal && a.b > 16) return -2;
+    CUtensorMap maps[3];
+    if (!encode_qkv(maps, a.q, a.k, a.v, a.B * a.H, a.T, a.d, 16)) return -4;
     switch (a.d) {
     case 16: return launch_mlp_t<16>(a, maps);
     case 32: return launch_mlp_t<32>(a, maps);
