@@ -10,10 +10,13 @@
 //  * tokens arrive in 64-token blocks (one TMA box per tensor per four chunks);
 //    the four chunks of a block are unrolled, so every fragment address is a
 //    per-lane constant plus a compile-time offset from the block's base;
-//  * the chain warps wait for and release a block once, not per chunk;
-//  * one score warp forms mask .* (Q K^T) per chunk into a 4-slot ring;
-//  * each chain warp prefetches the next chunk's fragments (K, K^T, Q, V, eta)
-//    into a second register set while the current chunk's products run;
+//  * the compute warps wait for and release a block once, not per chunk;
+//  * each warp forms the scores S = Q K^T of its chunk from fragments already in
+//    its registers (K's fragments are the B operand of E as well), masks them in
+//    registers and uses them directly as the A operand of S (-Et);
+//  * each warp prefetches the next chunk's fragments (K, K^T, Q, V, eta) into a
+//    second register set while the current chunk's products run;
+//  * full 16-token chunks take a path without per-token bounds masks;
 //  * Z is stored straight from the accumulator registers.
 #include <cuda.h>
 
@@ -27,20 +30,17 @@ namespace {
 
 template <int D>
 struct B16Cfg {
-    static constexpr int NCW = D / 16;               // chain warps, 16 output columns each
-    static constexpr int SW = NCW;                   // score warp
-    static constexpr int PW = NCW + 1;               // producer warp
-    static constexpr int THREADS = (NCW + 2) * 32;
+    static constexpr int NCW = D / 16;               // compute warps, 16 output columns each
+    static constexpr int PW = NCW;                   // producer warp
+    static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int NJ = D / 8, NK = D / 16;
     static constexpr int NB = 4;                     // 64-token blocks in flight
     static constexpr int RB = 2 * D;                 // bytes per token row
     static constexpr int BLK = 64 * RB;              // one tensor's 64-token block
     static constexpr int SLOT = ((3 * BLK + 1023) / 1024) * 1024;  // Q, K, V of one block
     static constexpr int ETA_OFF = NB * SLOT;        // 64 fp32 per block
-    static constexpr int SROW = 48;                  // bf16 16 x 16 score tile row
-    static constexpr int S_OFF = ETA_OFF + NB * 256; // 4 score tiles
-    static constexpr int BAR_OFF = S_OFF + 4 * 16 * SROW;
-    static constexpr int SMEM = BAR_OFF + (2 * NB + 8) * 8 + 1024;
+    static constexpr int BAR_OFF = ETA_OFF + NB * 256;
+    static constexpr int SMEM = BAR_OFF + 2 * NB * 8 + 1024;
     static constexpr uint32_t SWM = RB == 128 ? 7u : (RB == 64 ? 3u : 1u);
 };
 
@@ -90,18 +90,12 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
     const int nblk = (T + 63) >> 6;
     const bool has_eta = p.eta != nullptr;
 
-    const uint32_t blk_full = base + C::BAR_OFF;      // block landed (producer -> all)
-    const uint32_t blk_empty = blk_full + 8 * NB;     // block released (chain + score -> producer)
-    const uint32_t s_full = blk_empty + 8 * NB;       // score tile written (score -> chain)
-    const uint32_t s_empty = s_full + 8 * 4;          // score tile read (chain -> score)
+    const uint32_t blk_full = base + C::BAR_OFF;      // block landed (producer -> warps)
+    const uint32_t blk_empty = blk_full + 8 * NB;     // block released (warps -> producer)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NB; ++s) {
             mbar_init(blk_full + 8 * s, 1 + (has_eta ? 32 : 0));
-            mbar_init(blk_empty + 8 * s, C::NCW + 1);
-        }
-        for (int s = 0; s < 4; ++s) {
-            mbar_init(s_full + 8 * s, 1);
-            mbar_init(s_empty + 8 * s, C::NCW);
+            mbar_init(blk_empty + 8 * s, C::NCW);
         }
         fence_barrier_init();
     }
@@ -140,59 +134,7 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
         return;
     }
 
-    if (warp == C::SW) {
-        // ---------------------------------------------------------- score warp
-        uint32_t offA[NK], offB[NK];
-#pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {
-            offA[kk] = boff<D>(rowA, 16 * kk + colA);
-            offB[kk] = boff<D>(rowB, 16 * kk + colB);
-        }
-        bool vis[2][4];  // causal visibility of (query g + 8(i>>1), key 8nt + 2t4 + (i&1))
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) vis[nt][i] = !p.causal || (8 * nt + 2 * t4 + (i & 1)) <= g + 8 * (i >> 1);
-        for (int L = 0; L < nblk; ++L) {
-            const int s = L & (NB - 1);
-            if (!mbar_wait(blk_full + 8 * s, (L / NB) & 1, p.status, kSiteConsumerFull)) return;
-            const uint32_t st = base + s * C::SLOT;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int t0 = 64 * L + 16 * q;
-                if (t0 >= T) break;
-                const int c = min(16, T - t0);
-                if (L > 0 && !mbar_wait(s_empty + 8 * q, (L - 1) & 1, p.status, kSiteStage)) return;
-                float sc[2][2][4] = {};
-#pragma unroll
-                for (int kk = 0; kk < NK; ++kk) {
-                    uint32_t a0, a1, a2, a3, b00, b01, b10, b11;
-                    ldsm_x4(st + 16 * q * C::RB + offA[kk], a0, a1, a2, a3);
-                    ldsm_x4(st + C::BLK + 16 * q * C::RB + offB[kk], b00, b01, b10, b11);
-                    mma_bf16(sc[kk & 1][0], a0, a1, a2, a3, b00, b01);
-                    mma_bf16(sc[kk & 1][1], a0, a1, a2, a3, b10, b11);
-                }
-                float sm[2][4];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const bool keep = vis[nt][i] && (8 * nt + 2 * t4 + (i & 1)) < c;
-                        sm[nt][i] = keep ? sc[0][nt][i] + sc[1][nt][i] : 0.f;
-                    }
-                stsm_x4(base + C::S_OFF + q * 16 * C::SROW + rowA * C::SROW + colA * 2,
-                        pack_bf16(sm[0][0], sm[0][1]), pack_bf16(sm[0][2], sm[0][3]),
-                        pack_bf16(sm[1][0], sm[1][1]), pack_bf16(sm[1][2], sm[1][3]));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_full + 8 * q);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(blk_empty + 8 * s);
-        }
-        return;
-    }
-
-    // -------------------------------------------------------------- chain warp
+    // ------------------------------------------------------------ compute warp
     const int w = warp, col0 = 16 * w;
     float wacc[NJ][4];  // W^T[col0+g (+8)][8j+2t4 .. +1]
     {
@@ -250,14 +192,22 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
         }
     };
 
-    bool ok = true;
+    bool vis[2][4];  // causal visibility of (query g + 8(i>>1), key 8nt + 2t4 + (i&1))
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vis[nt][i] = !p.causal || (8 * nt + 2 * t4 + (i & 1)) <= g + 8 * (i >> 1);
+    __nv_bfloat16 *const zlane = p.z + (size_t)bh * T * D + (size_t)g * D + col0 + 2 * t4;
+
     // one chunk (L, Q) on fragments F; fetches chunk (L, Q+1) or (L+1, 0) into Fn.
-    // Returns false when there is no next chunk (or a wait gave up).
-    auto chunk = [&](auto qc, Frag<D> &F, Frag<D> &Fn, int L) -> bool {
+    // FULL: the chunk has 16 tokens (no bounds masks).  Returns false when there
+    // is no next chunk (or a wait gave up).
+    auto chunk = [&](auto qc, auto fullc, Frag<D> &F, Frag<D> &Fn, int L) -> bool {
         constexpr int Q = decltype(qc)::value;
+        constexpr bool FULL = decltype(fullc)::value;
         const int t0 = 64 * L + 16 * Q;
-        const int c = min(16, T - t0);
-        float e[2][2][4] = {}, zc[2][2][4] = {};
+        const int c = FULL ? 16 : T - t0;
+        float e[2][2][4] = {}, sc[2][4] = {}, zc[2][4] = {};
 #pragma unroll
         for (int kk = 0; kk < NK; ++kk) {  // E^T = W^T K^T
             mma_bf16(e[kk & 1][0], wb[4 * kk], wb[4 * kk + 1], wb[4 * kk + 2], wb[4 * kk + 3], F.kB[kk][0],
@@ -266,27 +216,23 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
                      F.kB[kk][3]);
         }
 #pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {  // Z = Q W
-            mma_bf16(zc[kk & 1][0], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk],
-                     wb[4 * kk + 2]);
-            mma_bf16(zc[kk & 1][1], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk + 1],
-                     wb[4 * kk + 3]);
+        for (int kk = 0; kk < NK; ++kk) {  // S = Q K^T (off the serial chain)
+            mma_bf16(sc[0], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], F.kB[kk][0], F.kB[kk][1]);
+            mma_bf16(sc[1], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], F.kB[kk][2], F.kB[kk][3]);
         }
-        // next chunk's fragments
+        // next chunk's fragments: inside a block the load is unconditional (reads of
+        // the ring past the sequence end stay in bounds and are never used), so the
+        // chunk body stays one basic block; crossing into the next block waits for it
         const bool more = t0 + 16 < T;
-        if (more) {
-            if constexpr (Q < 3) {
-                load(std::integral_constant<int, Q + 1>{}, Fn, L);
-            } else {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(blk_empty + 8 * (L & (NB - 1)));
-                if (!mbar_wait(blk_full + 8 * ((L + 1) & (NB - 1)), ((L + 1) / NB) & 1, p.status,
-                               kSiteConsumerFull)) {
-                    ok = false;
-                    return false;
-                }
-                load(std::integral_constant<int, 0>{}, Fn, L + 1);
-            }
+        if constexpr (Q < 3) {
+            load(std::integral_constant<int, Q + 1>{}, Fn, L);
+        } else if (more) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(blk_empty + 8 * (L & (NB - 1)));
+            if (!mbar_wait(blk_full + 8 * ((L + 1) & (NB - 1)), ((L + 1) / NB) & 1, p.status,
+                           kSiteConsumerFull))
+                return false;
+            load(std::integral_constant<int, 0>{}, Fn, L + 1);
         }
         // -Et^T as an A fragment
         float ne[2][4];
@@ -297,7 +243,7 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
                 const uint32_t vw = F.vv[nt][i >> 1];
                 const float vval = (i & 1) ? bf16_hi(vw) : bf16_lo(vw);
                 const float r = e[0][nt][i] + e[1][nt][i] - vval;
-                ne[nt][i] = (8 * nt + 2 * t4 + (i & 1)) < c ? -F.et[nt][i & 1] * r : 0.f;
+                ne[nt][i] = (FULL || (8 * nt + 2 * t4 + (i & 1)) < c) ? -F.et[nt][i & 1] * r : 0.f;
             }
         const uint32_t ea0 = pack_bf16(ne[0][0], ne[0][1]), ea1 = pack_bf16(ne[0][2], ne[0][3]);
         const uint32_t ea2 = pack_bf16(ne[1][0], ne[1][1]), ea3 = pack_bf16(ne[1][2], ne[1][3]);
@@ -306,42 +252,52 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
             mma_bf16(wacc[2 * j2], ea0, ea1, ea2, ea3, F.kT[j2][0], F.kT[j2][1]);
             mma_bf16(wacc[2 * j2 + 1], ea0, ea1, ea2, ea3, F.kT[j2][2], F.kT[j2][3]);
         }
-        // Z += (mask .* Q K^T)(-Et)
-        if (!mbar_wait(s_full + 8 * Q, L & 1, p.status, kSiteConsumerReady)) {
-            ok = false;
-            return false;
+        // Z = Q W + (mask .* S)(-Et), masked scores as an A fragment from registers
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+            mma_bf16(zc[0], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk], wb[4 * kk + 2]);
+            mma_bf16(zc[1], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk + 1],
+                     wb[4 * kk + 3]);
         }
-        uint32_t s0, s1, s2, s3;
-        ldsm_x4(base + C::S_OFF + Q * 16 * C::SROW + rowA * C::SROW + colA * 2, s0, s1, s2, s3);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_empty + 8 * Q);
-        mma_bf16(zc[1][0], s0, s1, s2, s3, ea0, ea2);
-        mma_bf16(zc[1][1], s0, s1, s2, s3, ea1, ea3);
-        __nv_bfloat16 *zb = p.z + ((size_t)bh * T + t0) * D + col0 + 2 * t4;
+        float sm[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool keep = vis[nt][i] && (FULL || (8 * nt + 2 * t4 + (i & 1)) < c);
+                sm[nt][i] = keep ? sc[nt][i] : 0.f;
+            }
+        mma_bf16(zc[0], pack_bf16(sm[0][0], sm[0][1]), pack_bf16(sm[0][2], sm[0][3]),
+                 pack_bf16(sm[1][0], sm[1][1]), pack_bf16(sm[1][2], sm[1][3]), ea0, ea2);
+        mma_bf16(zc[1], pack_bf16(sm[0][0], sm[0][1]), pack_bf16(sm[0][2], sm[0][3]),
+                 pack_bf16(sm[1][0], sm[1][1]), pack_bf16(sm[1][2], sm[1][3]), ea1, ea3);
+        convert();
+        __nv_bfloat16 *zb = zlane + (size_t)t0 * D;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            if (g < c)
-                *reinterpret_cast<uint32_t *>(zb + (size_t)g * D + 8 * hh) =
-                    pack_bf16(zc[0][hh][0] + zc[1][hh][0], zc[0][hh][1] + zc[1][hh][1]);
-            if (g + 8 < c)
-                *reinterpret_cast<uint32_t *>(zb + (size_t)(g + 8) * D + 8 * hh) =
-                    pack_bf16(zc[0][hh][2] + zc[1][hh][2], zc[0][hh][3] + zc[1][hh][3]);
+            if (FULL || g < c)
+                *reinterpret_cast<uint32_t *>(zb + 8 * hh) = pack_bf16(zc[hh][0], zc[hh][1]);
+            if (FULL || g + 8 < c)
+                *reinterpret_cast<uint32_t *>(zb + 8 * D + 8 * hh) = pack_bf16(zc[hh][2], zc[hh][3]);
         }
-        convert();
         return more;
+    };
+    auto step = [&](auto qc, Frag<D> &F, Frag<D> &Fn, int L) -> bool {
+        if (64 * L + 16 * decltype(qc)::value + 16 <= T)
+            return chunk(qc, std::true_type{}, F, Fn, L);
+        return chunk(qc, std::false_type{}, F, Fn, L);
     };
 
     if (nblk > 0 && mbar_wait(blk_full, 0, p.status, kSiteConsumerFull)) {
         Frag<D> FA, FB;
         load(std::integral_constant<int, 0>{}, FA, 0);
         for (int L = 0;; ++L) {  // two fragment sets alternate: no register copies
-            if (!chunk(std::integral_constant<int, 0>{}, FA, FB, L)) break;
-            if (!chunk(std::integral_constant<int, 1>{}, FB, FA, L)) break;
-            if (!chunk(std::integral_constant<int, 2>{}, FA, FB, L)) break;
-            if (!chunk(std::integral_constant<int, 3>{}, FB, FA, L)) break;
+            if (!step(std::integral_constant<int, 0>{}, FA, FB, L)) break;
+            if (!step(std::integral_constant<int, 1>{}, FB, FA, L)) break;
+            if (!step(std::integral_constant<int, 2>{}, FA, FB, L)) break;
+            if (!step(std::integral_constant<int, 3>{}, FB, FA, L)) break;
         }
     }
-    (void)ok;
 
     if (p.W_out) {
         float *Wo = p.W_out + (size_t)bh * D * D;
