@@ -62,7 +62,12 @@ struct MlpCfg {
     static constexpr int SP_OFF = NEB_OFF + 16 * ER;      // bf16 M .* (Q K^T + 1)
     static constexpr int S2_OFF = SP_OFF + 16 * SR;       // bf16 M .* (A_q A_k^T + 1)
     static constexpr int BAR_OFF = ((S2_OFF + 16 * SR + 15) / 16) * 16;
-    static constexpr int SMEM = BAR_OFF + NS * 8 + 1024;
+    static constexpr int SMEM = BAR_OFF + NS * 8 + 16 + 1024;
+    // causal mini-batches of several chunks: bf16 copies of the current weights
+    // (the queries' weights) next to the block-start copies the residuals read
+    static constexpr int W2C_OFF = ((BAR_OFF + NS * 8 + 16 + 127) / 128) * 128;  // bf16 W2 [M][W2R]
+    static constexpr int W1C_OFF = W2C_OFF + M * W2R;             // bf16 W1^T [M][W2R]
+    static constexpr int SMEM_MULTI = W1C_OFF + M * W2R + 1024;
     static constexpr uint32_t SWM = RB == 128 ? 7u : (RB == 64 ? 3u : 1u);
 };
 
@@ -104,7 +109,10 @@ struct MlpParams {
     int *status;
 };
 
-template <int D>
+// MULTI: causal with mini-batches longer than one 16-token chunk, so the chunk's
+// queries read weights that already include the earlier chunks' writes while its
+// residuals are taken at the mini-batch's start weights.
+template <int D, bool MULTI>
 __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
     ttt_mlp_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const MlpParams p)
@@ -129,6 +137,8 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
     const uint32_t W2B = base + C::W2B_OFF, AK = base + C::AK_OFF, AQ = base + C::AQ_OFF;
     const uint32_t EB = base + C::EB_OFF, NEB = base + C::NEB_OFF;
     const uint32_t SP = base + C::SP_OFF, S2P = base + C::S2_OFF;
+    const uint32_t W2C = base + C::W2C_OFF, W1C = base + C::W1C_OFF;  // used when MULTI
+    const uint32_t W2Q = MULTI ? W2C : W2B;  // W2 the queries read
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(bar_full + 8 * s, 1 + (has_eta ? 32 : 0));
@@ -251,6 +261,27 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
                           pack_bf16(__uint_as_float(x1.x), __uint_as_float(x1.y)),
                           pack_bf16(__uint_as_float(x1.z), __uint_as_float(x1.w)));
             }
+        }
+        if constexpr (MULTI) {
+            // current weights for this chunk's queries: W2 [hidden][d] and W1^T
+            // [hidden][d_in] as bf16 (this warp's 16 hidden rows of each)
+#pragma unroll
+            for (int mt = 0; mt < NK; ++mt) {
+                const uint4 x0 = lds128(w2f(mt, 0)), x1 = lds128(w2f(mt, 1));
+                const int blk = lane >> 3, rr = lane & 7;
+                const uint32_t addr = W2C + (uint32_t)(h0 + 8 * (blk >> 1) + rr) * C::W2R +
+                                      (uint32_t)(16 * mt + 8 * (blk & 1)) * 2;
+                stsm_x4_t(addr, pack_bf16(__uint_as_float(x0.x), __uint_as_float(x0.y)),
+                          pack_bf16(__uint_as_float(x0.z), __uint_as_float(x0.w)),
+                          pack_bf16(__uint_as_float(x1.x), __uint_as_float(x1.y)),
+                          pack_bf16(__uint_as_float(x1.z), __uint_as_float(x1.w)));
+            }
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk)
+                stsm_x4(W1C + (uint32_t)(h0 + rowA) * C::W2R + (16 * kk + colA) * 2,
+                        pack_bf16(w1[2 * kk][0], w1[2 * kk][1]), pack_bf16(w1[2 * kk][2], w1[2 * kk][3]),
+                        pack_bf16(w1[2 * kk + 1][0], w1[2 * kk + 1][1]),
+                        pack_bf16(w1[2 * kk + 1][2], w1[2 * kk + 1][3]));
         }
         if (!mbar_wait(bar_full + 8 * s, (jb / NS) & 1, p.status, kSiteConsumerFull)) *abort_flag = 1;
 
@@ -410,8 +441,15 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
             for (int kk = 0; kk < NK; ++kk) {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(tQ + mtoff<D>(rowA, 16 * kk + colA), a0, a1, a2, a3);
-                mma_bf16(hq[0], a0, a1, a2, a3, w1b[4 * kk], w1b[4 * kk + 2]);
-                mma_bf16(hq[1], a0, a1, a2, a3, w1b[4 * kk + 1], w1b[4 * kk + 3]);
+                if constexpr (MULTI) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(W1C + (uint32_t)(h0 + rowB) * C::W2R + (16 * kk + colB) * 2, b0, b1, b2, b3);
+                    mma_bf16(hq[0], a0, a1, a2, a3, b0, b1);
+                    mma_bf16(hq[1], a0, a1, a2, a3, b2, b3);
+                } else {
+                    mma_bf16(hq[0], a0, a1, a2, a3, w1b[4 * kk], w1b[4 * kk + 2]);
+                    mma_bf16(hq[1], a0, a1, a2, a3, w1b[4 * kk + 1], w1b[4 * kk + 3]);
+                }
             }
             if (both) {
                 uint32_t s0, s1, s2, s3;
@@ -452,7 +490,7 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
 #pragma unroll
                 for (int kp = 0; kp < NKM / 2; ++kp) {
                     uint32_t b0a, b1a, b0b, b1b, a0, a1, a2, a3, a4, a5, a6, a7;
-                    ldsm_x4_t(W2B + (uint32_t)(32 * kp + lane) * C::W2R + c0 * 2, b0a, b1a, b0b, b1b);
+                    ldsm_x4_t(W2Q + (uint32_t)(32 * kp + lane) * C::W2R + c0 * 2, b0a, b1a, b0b, b1b);
                     ldsm_x4(AQ + rowA * C::AR + (32 * kp + colA) * 2, a0, a1, a2, a3);
                     ldsm_x4(AQ + rowA * C::AR + (32 * kp + 16 + colA) * 2, a4, a5, a6, a7);
                     mma_bf16(pz[0], a0, a1, a2, a3, b0a, b1a);
@@ -556,8 +594,10 @@ template <int D>
 static int launch_mlp_t(const MlpArgs &a, const CUtensorMap *maps)
 {
     using C = MlpCfg<D>;
-    auto kern = ttt_mlp_bf16_kernel<D>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    const bool multi = a.causal && a.b > 16;
+    auto kern = multi ? ttt_mlp_bf16_kernel<D, true> : ttt_mlp_bf16_kernel<D, false>;
+    const int smem = multi ? C::SMEM_MULTI : C::SMEM;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return -4;
     MlpParams p;
     p.H = a.H;
@@ -577,16 +617,14 @@ static int launch_mlp_t(const MlpArgs &a, const CUtensorMap *maps)
     p.W2o = a.W2o;
     p.c2o = a.c2o;
     p.status = a.status;
-    kern<<<a.B * a.H, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
+    kern<<<a.B * a.H, C::THREADS, smem, a.stream>>>(maps[0], maps[1], maps[2], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
-// d in {16, 32, 64} with hidden width m = 4d; causal mini-batches longer than one
-// 16-token chunk are not implemented on this path (TTT_ERR_UNSUPPORTED).
+// d in {16, 32, 64} with hidden width m = 4d.
 int launch_mlp_bf16(const MlpArgs &a)
 {
     if (a.m != 4 * a.d) return -2;
-    if (a.causal && a.b > 16) return -2;
     CUtensorMap maps[3];
     if (!encode_qkv(maps, a.q, a.k, a.v, a.B * a.H, a.T, a.d, 16)) return -4;
     switch (a.d) {

@@ -81,8 +81,17 @@ def test_fp32_small(b, causal):
     _check(inp, tol=G.TOL_F32)
 
 
-def test_causal_multichunk_minibatch_is_reported_unsupported():
-    inp = _mlp_inputs(1, 1, 64, 64, 32, True, seed=50)
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("b", [24, 32, 40])
+def test_bf16_causal_multichunk_minibatch(d, b):
+    """Causal mini-batches longer than one 16-token chunk: residuals at the block's
+    start weights, queries at the weights after the earlier chunks' writes."""
+    inp = _mlp_inputs(2, 2, 90, d, b, True, eta=0.02, seed=60 + d + b, bias=0.1)
+    _check(inp)
+
+
+def test_unsupported_width_is_reported():
+    inp = G.synth.make("mlp", B=1, H=1, T=32, d=64, m=128, b=16, causal=True, eta=0.1, seed=50)
     with pytest.raises(abi.TTTError) as ei:
         G.gpu_mlp(inp)
     assert ei.value.code == -2
