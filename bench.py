@@ -79,6 +79,15 @@ def bytes_per_launch(inp):
     return n
 
 
+def kernel_name(inp):
+    """The kernel the library dispatches this workload to (mirrors the C ABI's choice)."""
+    if inp.q.element_size() == 4:
+        return "ttt_linear_f32_kernel" if inp.kind == "linear" else "ttt_mlp_f32_kernel"
+    if inp.kind == "linear":
+        return "ttt_linear_b16_kernel" if min(inp.b, inp.T) == 16 and inp.d <= 64 else "ttt_linear_bf16_kernel"
+    return "ttt_mlp_bf16_kernel"
+
+
 def recorded_traffic(workload):
     """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json), or
     None when there is no record or the kernel sources changed since it was taken."""
@@ -397,7 +406,7 @@ def main():
                 "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"]}
     roof.update({"traffic": recorded_traffic(args.workload), "peak_source": peaks["source"],
                  "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
-                 "kernel": "ttt_linear_bf16_kernel" if inp.kind == "linear" else "ttt_mlp_bf16_kernel",
+                 "kernel": kernel_name(inp),
                  "launch_ms_mean": ms, "launch_ms_min": min(times)})
     if rank != 0:
         return
