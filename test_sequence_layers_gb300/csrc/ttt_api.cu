@@ -59,17 +59,19 @@ int *status_word()
 
 // q/k/v viewed as a 3-D tensor [B*H][T][d] of bf16; box = `rows` tokens x min(d,64)
 // features, swizzled to the box row length so that ldmatrix is conflict-free.
-bool ttt::encode_token_map(CUtensorMap *m, const void *ptr, int BH, int T, int d, int rows)
+bool ttt::encode_token_map(CUtensorMap *m, const void *ptr, int BH, int T, int d, int rows, int cols)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    if (cols <= 0) cols = d < 64 ? d : 64;
     const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)(d < 64 ? d : 64), (cuuint32_t)rows, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapSwizzle sw = d >= 64   ? CU_TENSOR_MAP_SWIZZLE_128B
-                                  : d == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                            : CU_TENSOR_MAP_SWIZZLE_32B;
+    // swizzle span = the box row length (128, 64 or 32 bytes)
+    const CUtensorMapSwizzle sw = cols >= 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

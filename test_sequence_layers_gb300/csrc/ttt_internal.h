@@ -33,9 +33,10 @@ struct MlpArgs {
 };
 
 // TMA descriptor of a bf16 token tensor viewed as [BH][T][d]: boxes of `rows`
-// tokens x min(d, 64) features, swizzled to the box row length, rows past T
-// zero-filled.  Returns false if the driver entry point is unavailable or rejects it.
-bool encode_token_map(CUtensorMap *m, const void *ptr, int BH, int T, int d, int rows);
+// tokens x `cols` features (0: min(d, 64)), swizzled to the box row length, rows
+// past T zero-filled on loads and dropped on stores.  Returns false if the driver
+// entry point is unavailable or rejects it.
+bool encode_token_map(CUtensorMap *m, const void *ptr, int BH, int T, int d, int rows, int cols = 0);
 
 // q, k, v descriptors (zeroed, unused when T == 0); false on an encoding failure.
 inline bool encode_qkv(CUtensorMap *maps, const void *q, const void *k, const void *v, int BH, int T,

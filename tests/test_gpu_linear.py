@@ -54,6 +54,23 @@ def test_short_and_empty_sequences(T):
     _check(inp)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("T", [48, 64, 128, 130, 191, 250])
+def test_b16_d64_block_boundaries(T, causal):
+    """b = 16, d = 64 (outputs formed per 64-token block on the tensor cores):
+    whole blocks, partial last blocks and a partial last mini-batch, per-token eta."""
+    inp = G.synth.make("linear", B=2, H=2, T=T, d=64, b=16, causal=causal, eta="sigmoid", seed=200 + T)
+    _check(inp)
+
+
+@pytest.mark.parametrize("B,H", [(1, 1), (1, 3), (3, 3)])
+def test_b16_d64_odd_chain_counts(B, H):
+    """b = 16, d = 64 with an odd number of (batch, head) chains (the chains are
+    served in pairs)."""
+    inp = G.synth.make("linear", B=B, H=H, T=200, d=64, b=16, causal=True, seed=300 + 3 * B + H)
+    _check(inp)
+
+
 def test_per_token_eta_and_per_batch_w0():
     inp = G.synth.make("linear", B=3, H=2, T=130, d=64, b=16, causal=True, eta="sigmoid", seed=11)
     _check(inp, per_batch_w0=True)
@@ -65,22 +82,33 @@ def test_full_batch_noncausal_single_block():
     _check(inp)
 
 
-def test_split_run_continues_sequence():
-    """W_final passed back as W0 continues the sequence (chunked prefill)."""
-    inp = G.synth.make("linear", B=2, H=2, T=96, d=64, b=16, causal=True, seed=13)
+@pytest.mark.parametrize("split", [64, 48])
+def test_split_run_continues_sequence(split):
+    """W_final passed back as W0 continues the sequence (chunked prefill).  The
+    state chain is per mini-batch, so the final weights are bit-identical for any
+    split at a mini-batch boundary.  Outputs may be formed from the start weights
+    of 64-token blocks (a valid dual-form grouping), so z is required bit-identical
+    when the split falls on a 64-token boundary and otherwise equal up to the bf16
+    rounding of those start weights."""
+    inp = G.synth.make("linear", B=2, H=2, T=160, d=64, b=16, causal=True, seed=13)
     dev = torch.device("cuda")
     q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
     W0 = inp.params["W0"].to(dev)
     from test_sequence_layers_gb300 import abi
     z, W = abi.ttt_linear_fwd(q, k, v, W0, 16)
-    z1, W1 = abi.ttt_linear_fwd(q[:, :, :48].contiguous(), k[:, :, :48].contiguous(),
-                                v[:, :, :48].contiguous(), W0, 16)
+    z1, W1 = abi.ttt_linear_fwd(q[:, :, :split].contiguous(), k[:, :, :split].contiguous(),
+                                v[:, :, :split].contiguous(), W0, 16)
     # continue in place: the final-weight buffer is the initial-weight input
-    z2, W2 = abi.ttt_linear_fwd(q[:, :, 48:].contiguous(), k[:, :, 48:].contiguous(),
-                                v[:, :, 48:].contiguous(), W1, 16, W_out=W1)
+    z2, W2 = abi.ttt_linear_fwd(q[:, :, split:].contiguous(), k[:, :, split:].contiguous(),
+                                v[:, :, split:].contiguous(), W1, 16, W_out=W1)
     abi.ttt_sync_status()
-    assert torch.equal(torch.cat([z1, z2], 2), z)
     assert torch.equal(W2, W)
+    zc = torch.cat([z1, z2], 2)
+    if split % 64 == 0:
+        assert torch.equal(zc, z)
+    else:
+        err = ((zc.float() - z.float()).abs().max() / z.float().abs().max()).item()
+        assert err <= 1e-2, err
 
 
 def test_deterministic():
