@@ -21,6 +21,7 @@ struct Job {
     int kind;        // JobKind
     int first;       // first chunk of its pass over the mini-batch
     int last_of_mb;  // last job of the mini-batch
+    int last_upd;    // last job of the mini-batch that updates the weights
 };
 
 struct JobIter {
@@ -50,6 +51,7 @@ struct JobIter {
         o.kind = !split ? kBoth : (j < nch ? kUpd : kOut);
         o.first = (ch == 0);
         o.last_of_mb = (j == njobs - 1);
+        o.last_upd = split ? (j == nch - 1) : o.last_of_mb;
         return o;
     }
     __device__ __forceinline__ void next()

@@ -68,6 +68,9 @@ struct MlpCfg {
     static constexpr int W2C_OFF = ((BAR_OFF + NS * 8 + 16 + 127) / 128) * 128;  // bf16 W2 [M][W2R]
     static constexpr int W1C_OFF = W2C_OFF + M * W2R;             // bf16 W1^T [M][W2R]
     static constexpr int SMEM_MULTI = W1C_OFF + M * W2R + 1024;
+    // otherwise: the W2C region is the second of two bf16 W2 buffers (the copy of the
+    // next mini-batch's start weights is written while the current one is read)
+    static constexpr int SMEM_DBL = W2C_OFF + M * W2R + 1024;
     static constexpr uint32_t SWM = RB == 128 ? 7u : (RB == 64 ? 3u : 1u);
 };
 
@@ -134,11 +137,11 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
     const bool has_eta = p.eta != nullptr;
     const uint32_t bar_full = base + C::BAR_OFF;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::BAR_OFF + NS * 8);
-    const uint32_t W2B = base + C::W2B_OFF, AK = base + C::AK_OFF, AQ = base + C::AQ_OFF;
+    const uint32_t AK = base + C::AK_OFF, AQ = base + C::AQ_OFF;
+    int w2cur = 0;  // which bf16 W2 buffer holds the current mini-batch's start weights
     const uint32_t EB = base + C::EB_OFF, NEB = base + C::NEB_OFF;
     const uint32_t SP = base + C::SP_OFF, S2P = base + C::S2_OFF;
     const uint32_t W2C = base + C::W2C_OFF, W1C = base + C::W1C_OFF;  // used when MULTI
-    const uint32_t W2Q = MULTI ? W2C : W2B;  // W2 the queries read
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(bar_full + 8 * s, 1 + (has_eta ? 32 : 0));
@@ -232,6 +235,11 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
         const float *eta_s = reinterpret_cast<const float *>(gbase + s * C::STAGE + 3 * C::TILE_A);
         const bool upd = J.kind != kOut, out = J.kind != kUpd, both = J.kind == kBoth;
         auto eta_of = [&](int tok) -> float { return has_eta ? eta_s[tok] : p.eta_scalar; };
+        // bf16 W2 [hidden][d] at the start of this mini-batch (the residuals read it;
+        // so do the queries unless MULTI), and the buffer for the next one
+        const uint32_t W2B = base + (w2cur ? C::W2C_OFF : C::W2B_OFF);
+        const uint32_t W2N = base + (w2cur ? C::W2B_OFF : C::W2C_OFF);
+        const uint32_t W2Q = MULTI ? W2C : W2B;  // W2 the queries read
 
         // phase 0: bf16 copies of the weights this pass reads (start of a
         // mini-batch for the residuals; block-end weights for a query pass)
@@ -249,7 +257,11 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
             }
             c2s[0] = c2r[0];
             c2s[1] = c2r[1];
-            // W2 as bf16 [hidden][d] (transposed stores of the W2^T fragments)
+        }
+        // W2 as bf16 [hidden][d] (transposed stores of the W2^T fragments).  Without
+        // MULTI only the first chunk converts: each mini-batch's last update writes
+        // the next start weights straight from its registers.
+        if (MULTI ? J.first : jb == 0) {
 #pragma unroll
             for (int mt = 0; mt < NK; ++mt) {
                 const uint4 x0 = lds128(w2f(mt, 0)), x1 = lds128(w2f(mt, 1));
@@ -411,9 +423,11 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
                 mma_bf16(w1[2 * j2], d00, d01, d10, d11, k0, k1);
                 mma_bf16(w1[2 * j2 + 1], d00, d01, d10, d11, k2, k3);
             }
-            // W2^T += (-Et^T) A_k
+            // W2^T += (-Et^T) A_k (fp32 slices in shared memory); the last update of a
+            // mini-batch also writes the bf16 copy of the next start weights
             const uint32_t bt00 = movmatrix_t(akp[0]), bt01 = movmatrix_t(akp[1]);
             const uint32_t bt10 = movmatrix_t(akp[2]), bt11 = movmatrix_t(akp[3]);
+            const bool put_next = !MULTI && J.last_upd;
 #pragma unroll
             for (int mt = 0; mt < NK; ++mt) {
                 uint32_t a0, a1, a2, a3;
@@ -432,6 +446,13 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
                 asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(w2f(mt, 1)), "f"(x1[0]),
                              "f"(x1[1]), "f"(x1[2]), "f"(x1[3])
                              : "memory");
+                if (put_next) {
+                    const int blk = lane >> 3, rr = lane & 7;
+                    const uint32_t addr = W2N + (uint32_t)(h0 + 8 * (blk >> 1) + rr) * C::W2R +
+                                          (uint32_t)(16 * mt + 8 * (blk & 1)) * 2;
+                    stsm_x4_t(addr, pack_bf16(x0[0], x0[1]), pack_bf16(x0[2], x0[3]), pack_bf16(x1[0], x1[1]),
+                              pack_bf16(x1[2], x1[3]));
+                }
             }
         }
         if (out) {
@@ -546,6 +567,7 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
             c2r[0] += cs2[0];
             c2r[1] += cs2[1];
         }
+        if (!MULTI && J.last_upd) w2cur ^= 1;
     }
 
     // ------------------------------------------------------------ final state
@@ -596,7 +618,7 @@ static int launch_mlp_t(const MlpArgs &a, const CUtensorMap *maps)
     using C = MlpCfg<D>;
     const bool multi = a.causal && a.b > 16;
     auto kern = multi ? ttt_mlp_bf16_kernel<D, true> : ttt_mlp_bf16_kernel<D, false>;
-    const int smem = multi ? C::SMEM_MULTI : C::SMEM;
+    const int smem = multi ? C::SMEM_MULTI : C::SMEM_DBL;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return -4;
     MlpParams p;
@@ -621,6 +643,505 @@ static int launch_mlp_t(const MlpArgs &a, const CUtensorMap *maps)
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
+// ---------------------------------------------------------------------------
+// Eight-warp kernel for d = 64 (m = 256) and mini-batches of at most 16 tokens
+// (one chunk per mini-batch).  Same algebra as above; the work split differs:
+//  * warp w owns hidden units [32w, 32w + 32) as two groups of 16 and keeps the
+//    rows of W1^T and W2 for them in registers as fp32 mma accumulators (no
+//    shared-memory read-modify-write of W2), updating both with mma.sync;
+//  * every warp is also the column warp of output columns [8w, 8w + 8) for the
+//    products that contract over all hidden units (E = A_k W2, P = A_q W2);
+//  * A_q A_k^T is formed as eight per-warp partial sums over each warp's own
+//    hidden units, straight from registers;
+//  * warp 0 also issues the TMA loads a few chunks ahead into a four-stage ring
+//    (eight warps: two per SM sub-partition, so each may hold up to 255 registers);
+//  * the bf16 copy of W2 that the contractions read is double-buffered: each
+//    update writes the next mini-batch's copy from registers while the current
+//    copy is still read.
+struct W8Cfg {
+    static constexpr int D = 64, M = 256, NW = 8, THREADS = NW * 32;
+    static constexpr int NK = D / 16, NKM = M / 16, NJ = D / 8, NS = 4;
+    static constexpr int TILE = 16 * D * 2;                     // one 16-token tile
+    static constexpr int STAGE = ((3 * TILE + 64 + 1023) / 1024) * 1024;  // Q, K, V, eta
+    static constexpr int W2R = 2 * D + 16, AR = 2 * M + 16, ER = 2 * D + 16;
+    static constexpr int W2B_OFF = NS * STAGE;                  // two bf16 W2 [M][W2R]
+    static constexpr int AK_OFF = W2B_OFF + 2 * M * W2R;        // bf16 A_k [16][AR]
+    static constexpr int AQ_OFF = AK_OFF + 16 * AR;             // bf16 A_q [16][AR]
+    static constexpr int EB_OFF = AQ_OFF + 16 * AR;             // bf16 E [16][ER]
+    static constexpr int NEB_OFF = EB_OFF + 16 * ER;            // bf16 -Et [16][ER]
+    static constexpr int S2R = 20;                              // fp32 row stride of a partial (bank spread)
+    static constexpr int SP_OFF = NEB_OFF + 16 * ER;            // bf16 S' = M .* (Q K^T + 1) [16][48 B]
+    static constexpr int S2P_OFF = SP_OFF + 16 * 48;            // bf16 S2' = M .* (A_q A_k^T + 1) [16][48 B]
+    static constexpr int S2F_OFF = S2P_OFF + 16 * 48;           // fp32 [NW][16][S2R] partial A_q A_k^T
+    static constexpr int BAR_OFF = S2F_OFF + NW * 16 * S2R * 4; // full[NS], abort flag
+    static constexpr int SMEM = BAR_OFF + NS * 8 + 16 + 1024;
+};
+static_assert(MlpCfg<64>::RB == 128, "tile rows of 128 bytes");
+static_assert(W8Cfg::SMEM <= 227 * 1024, "shared memory");
+
+__global__ void __launch_bounds__(W8Cfg::THREADS, 1)
+    ttt_mlp_w8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, const MlpParams p)
+{
+    using C = W8Cfg;
+    constexpr int D = C::D, M = C::M, NK = C::NK, NKM = C::NKM, NJ = C::NJ, NS = C::NS, NW = C::NW;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x, T = p.T;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int rowA = (lane & 7) + 8 * ((lane >> 3) & 1), colA = 8 * (lane >> 4);
+    const int rowB = (lane & 7) + 8 * (lane >> 4), colB = 8 * ((lane >> 3) & 1);
+    const bool has_eta = p.eta != nullptr;
+    const uint32_t bar_full = base + C::BAR_OFF;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::BAR_OFF + NS * 8);
+    const uint32_t AK = base + C::AK_OFF, AQ = base + C::AQ_OFF, EB = base + C::EB_OFF;
+    const uint32_t NEB = base + C::NEB_OFF;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(bar_full + 8 * s, 1 + (has_eta ? 32 : 0));
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------- initial state
+    const int w = warp, c0 = 8 * w;
+    const size_t ps = p.per_batch ? (size_t)bh : (size_t)(bh % p.H);
+    const float *W1g = p.W1 + ps * D * M, *c1g = p.c1 + ps * M;
+    const float *W2g = p.W2 + ps * M * D, *c2g = p.c2 + ps * D;
+    // group hg (hidden 32w + 16hg ..): w1[hg][j] = W1^T rows (+g, +g+8) x columns 8j + 2t4 .. +1
+    float w1[2][NJ][4];
+    // w2[hg][mt][nt] = W2[h + 2t4 .. +1][16mt + g (+8)], h = 32w + 16hg + 8nt
+    float w2[2][NK][2][4];
+    float c1r[2][2][2];  // c1 of hidden 32w + 16hg + 8nt + 2t4 + i
+#pragma unroll
+    for (int hg = 0; hg < 2; ++hg) {
+        const int h0 = 32 * w + 16 * hg;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int r = 8 * j + 2 * t4;
+            w1[hg][j][0] = W1g[(size_t)r * M + h0 + g];
+            w1[hg][j][1] = W1g[(size_t)(r + 1) * M + h0 + g];
+            w1[hg][j][2] = W1g[(size_t)r * M + h0 + g + 8];
+            w1[hg][j][3] = W1g[(size_t)(r + 1) * M + h0 + g + 8];
+        }
+#pragma unroll
+        for (int mt = 0; mt < NK; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int hr = h0 + 8 * nt + 2 * t4, dc = 16 * mt + g;
+                w2[hg][mt][nt][0] = W2g[(size_t)hr * D + dc];
+                w2[hg][mt][nt][1] = W2g[(size_t)(hr + 1) * D + dc];
+                w2[hg][mt][nt][2] = W2g[(size_t)hr * D + dc + 8];
+                w2[hg][mt][nt][3] = W2g[(size_t)(hr + 1) * D + dc + 8];
+            }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) c1r[hg][nt][i] = c1g[h0 + 8 * nt + 2 * t4 + i];
+    }
+    float c2r[2] = {c2g[c0 + 2 * t4], c2g[c0 + 2 * t4 + 1]};  // c2 of columns c0 + 2t4 + i
+    // bf16 copy of this warp's W2 rows into buffer `buf` ([hidden][d], transposed
+    // stores of the accumulator tiles)
+    auto put_w2 = [&](uint32_t buf) {
+        const int blk = lane >> 3, rr = lane & 7;
+#pragma unroll
+        for (int hg = 0; hg < 2; ++hg)
+#pragma unroll
+            for (int mt = 0; mt < NK; ++mt)
+                stsm_x4_t(buf + (uint32_t)(32 * w + 16 * hg + 8 * (blk >> 1) + rr) * C::W2R +
+                              (uint32_t)(16 * mt + 8 * (blk & 1)) * 2,
+                          pack_bf16(w2[hg][mt][0][0], w2[hg][mt][0][1]),
+                          pack_bf16(w2[hg][mt][0][2], w2[hg][mt][0][3]),
+                          pack_bf16(w2[hg][mt][1][0], w2[hg][mt][1][1]),
+                          pack_bf16(w2[hg][mt][1][2], w2[hg][mt][1][3]));
+    };
+    // bf16 W1 of group hg as the B operand of a product with it (k-tile kk):
+    // n-tile 0 (hidden +0..7) uses (b[0], b[1]), n-tile 1 (hidden +8..15) (b[2], b[3])
+    auto w1_b = [&](int hg, int kk, uint32_t (&b)[4]) {
+        b[0] = pack_bf16(w1[hg][2 * kk][0], w1[hg][2 * kk][1]);
+        b[1] = pack_bf16(w1[hg][2 * kk + 1][0], w1[hg][2 * kk + 1][1]);
+        b[2] = pack_bf16(w1[hg][2 * kk][2], w1[hg][2 * kk][3]);
+        b[3] = pack_bf16(w1[hg][2 * kk + 1][2], w1[hg][2 * kk + 1][3]);
+    };
+    int w2cur = 0;
+    put_w2(base + C::W2B_OFF);
+
+    // ------------------------------------------------ token tiles (warp 0 issues)
+    JobIter itp(T, p.b, p.causal);
+    int issued = 0;
+    auto issue_next = [&]() {  // into the stage the chunk NS - 1 back released (after its barrier B3)
+        if (!itp.valid()) return;
+        const Job J = itp.get();
+        const int s = issued % NS;
+        const uint32_t st = base + s * C::STAGE, full = bar_full + 8 * s;
+        if (has_eta) {
+            if (lane < J.c) cp_async_4(st + 3 * C::TILE + 4 * lane, p.eta + (size_t)bh * T + J.t0 + lane);
+            cp_async_arrive_noinc(full);
+        }
+        if (lane == 0) {
+            mbar_arrive_expect_tx(full, 3 * C::TILE);
+            tma_load_3d(st, &tq, full, 0, J.t0, bh);
+            tma_load_3d(st + C::TILE, &tk, full, 0, J.t0, bh);
+            tma_load_3d(st + 2 * C::TILE, &tv, full, 0, J.t0, bh);
+        }
+        __syncwarp();
+        itp.next();
+        ++issued;
+    };
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tq)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
+        }
+        for (int i = 0; i < NS - 1; ++i) issue_next();
+    }
+    __syncthreads();
+
+    // acc += X W2[:, c0 .. c0+7] over all hidden units, X = A_k or A_q ([16][AR] bf16);
+    // the fragments of the next 32 hidden units load while the current ones multiply
+    auto col_product = [&](uint32_t W, uint32_t X, float (&acc)[2][4]) {
+        uint32_t fb[2][4], fa[2][8];
+        auto ld = [&](int kp, int sl) {
+            ldsm_x4_t(W + (uint32_t)(32 * kp + lane) * C::W2R + c0 * 2, fb[sl][0], fb[sl][1], fb[sl][2], fb[sl][3]);
+            ldsm_x4(X + rowA * C::AR + (32 * kp + colA) * 2, fa[sl][0], fa[sl][1], fa[sl][2], fa[sl][3]);
+            ldsm_x4(X + rowA * C::AR + (32 * kp + 16 + colA) * 2, fa[sl][4], fa[sl][5], fa[sl][6], fa[sl][7]);
+        };
+        ld(0, 0);
+#pragma unroll
+        for (int kp = 0; kp < NKM / 2; ++kp) {
+            if (kp + 1 < NKM / 2) ld(kp + 1, (kp + 1) & 1);
+            const int sl = kp & 1;
+            mma_bf16(acc[0], fa[sl][0], fa[sl][1], fa[sl][2], fa[sl][3], fb[sl][0], fb[sl][1]);
+            mma_bf16(acc[1], fa[sl][4], fa[sl][5], fa[sl][6], fa[sl][7], fb[sl][2], fb[sl][3]);
+        }
+    };
+
+    // ---------------------------------------------------------------- chunks
+    JobIter it(T, p.b, p.causal);
+    for (int jb = 0; it.valid(); it.next(), ++jb) {
+        const Job J = it.get();
+        if (warp == 0) issue_next();
+        const int s = jb % NS;
+        const uint32_t tQ = base + s * C::STAGE, tK = tQ + C::TILE, tV = tQ + 2 * C::TILE;
+        const float *eta_s = reinterpret_cast<const float *>(gbase + s * C::STAGE + 3 * C::TILE);
+        auto eta_of = [&](int tok) -> float { return has_eta ? eta_s[tok] : p.eta_scalar; };
+        // bf16 W2 at this mini-batch's start, and the buffer of the next one
+        const uint32_t W2B = base + C::W2B_OFF + (uint32_t)(w2cur * M * C::W2R);
+        const uint32_t W2N = base + C::W2B_OFF + (uint32_t)((w2cur ^ 1) * M * C::W2R);
+        if (!mbar_wait(bar_full + 8 * s, (jb / NS) & 1, p.status, kSiteConsumerFull)) *abort_flag = 1;
+
+        // phase 1: H_k = K W1 + c1, A_k = SiLU(H_k), SiLU'(H_k); scores for the queries
+        uint32_t kf[NK][4];
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) ldsm_x4(tK + mtoff<D>(rowA, 16 * kk + colA), kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3]);
+        float sp[2][2][4];
+        uint32_t akp[2][4];
+#pragma unroll
+        for (int hg = 0; hg < 2; ++hg) {
+            float hk[2][4] = {};
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                uint32_t b[4];
+                w1_b(hg, kk, b);
+                mma_bf16(hk[0], kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3], b[0], b[1]);
+                mma_bf16(hk[1], kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3], b[2], b[3]);
+            }
+            float ak[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float h = hk[nt][i] + c1r[hg][nt][i & 1];
+                    const float sg = sigmoid_f(h);
+                    ak[nt][i] = h * sg;
+                    sp[hg][nt][i] = sg * (1.f + h * (1.f - sg));
+                }
+            akp[hg][0] = pack_bf16(ak[0][0], ak[0][1]);  // (tok 0-7, hidden 0-7 of the group)
+            akp[hg][1] = pack_bf16(ak[0][2], ak[0][3]);  // (tok 8-15, hidden 0-7)
+            akp[hg][2] = pack_bf16(ak[1][0], ak[1][1]);  // (tok 0-7, hidden 8-15)
+            akp[hg][3] = pack_bf16(ak[1][2], ak[1][3]);  // (tok 8-15, hidden 8-15)
+            stsm_x4(AK + rowA * C::AR + (32 * w + 16 * hg + colA) * 2, akp[hg][0], akp[hg][1], akp[hg][2],
+                    akp[hg][3]);
+        }
+        if (w >= NW - 2) {
+            // S' = M .* (Q K^T + 1): warp NW-2 forms keys 0-7, warp NW-1 keys 8-15
+            const int nt = w - (NW - 2);
+            float sc[4] = {};
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                uint32_t a0, a1, a2, a3, b00, b01, b10, b11;
+                ldsm_x4(tQ + mtoff<D>(rowA, 16 * kk + colA), a0, a1, a2, a3);
+                ldsm_x4(tK + mtoff<D>(rowB, 16 * kk + colB), b00, b01, b10, b11);
+                mma_bf16(sc, a0, a1, a2, a3, nt ? b10 : b00, nt ? b11 : b01);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int tq_ = g + 8 * (i >> 1), ss = 8 * nt + 2 * t4 + (i & 1);
+                const bool keep = ss < J.c && (!p.causal || ss <= tq_);
+                sc[i] = keep ? sc[i] + 1.f : 0.f;
+            }
+            const uint32_t addr = base + C::SP_OFF + (uint32_t)((lane & 7) + 8 * ((lane >> 3) & 1)) * 48 + 16 * nt;
+            asm volatile("stmatrix.sync.aligned.m8n8.x2.shared.b16 [%0], {%1,%2};" ::"r"(addr),
+                         "r"(pack_bf16(sc[0], sc[1])), "r"(pack_bf16(sc[2], sc[3]))
+                         : "memory");
+        }
+        __syncthreads();  // B1: A_k visible
+        if (*abort_flag) break;
+
+        // phase 2: E = A_k W2 + c2 - V on columns c0 .. c0+7; -Et
+        float cs2[2] = {0.f, 0.f};  // column sums of -Et (the c2 write of this mini-batch)
+        {
+            float e[2][4] = {};
+            col_product(W2B, AK, e);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {  // token rows g, g + 8
+                const int tok = g + 8 * r;
+                const uint32_t vw =
+                    *reinterpret_cast<const uint32_t *>(gbase + (tV - base) + mtoff<D>(tok, c0 + 2 * t4));
+                const float ex = e[0][2 * r] + e[1][2 * r] + c2r[0] - bf16_lo(vw);
+                const float ey = e[0][2 * r + 1] + e[1][2 * r + 1] + c2r[1] - bf16_hi(vw);
+                const bool ok = tok < J.c;
+                const float et = -eta_of(tok);
+                const float nx = ok ? et * ex : 0.f, ny = ok ? et * ey : 0.f;
+                cs2[0] += nx;
+                cs2[1] += ny;
+                *reinterpret_cast<uint32_t *>(gbase + C::EB_OFF + tok * C::ER + (c0 + 2 * t4) * 2) = pack_bf16(ex, ey);
+                *reinterpret_cast<uint32_t *>(gbase + C::NEB_OFF + tok * C::ER + (c0 + 2 * t4) * 2) =
+                    pack_bf16(nx, ny);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                cs2[i] += __shfl_xor_sync(0xffffffffu, cs2[i], 4);
+                cs2[i] += __shfl_xor_sync(0xffffffffu, cs2[i], 8);
+                cs2[i] += __shfl_xor_sync(0xffffffffu, cs2[i], 16);
+            }
+        }
+        __syncthreads();  // B2: E, -Et visible
+
+        // phase 3: delta; query pre-activations (W1, c1 of the mini-batch start);
+        // then the weight updates and the next bf16 W2 copy
+        uint32_t ef[NK][4];
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) ldsm_x4(EB + rowA * C::ER + (16 * kk + colA) * 2, ef[kk][0], ef[kk][1], ef[kk][2], ef[kk][3]);
+        uint32_t dfr[2][4];  // -Dt^T blocks per group: (h 0-7, tok 0-7), (h 8-15, tok 0-7), (h 0-7, tok 8-15), (h 8-15, tok 8-15)
+        float cs1[2][2][2] = {};  // column sums of -Dt (the c1 write)
+#pragma unroll
+        for (int hg = 0; hg < 2; ++hg) {
+            float dl[2][4] = {};
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(W2B + (uint32_t)(32 * w + 16 * hg + rowB) * C::W2R + (16 * kk + colB) * 2, b0, b1, b2, b3);
+                mma_bf16(dl[0], ef[kk][0], ef[kk][1], ef[kk][2], ef[kk][3], b0, b1);
+                mma_bf16(dl[1], ef[kk][0], ef[kk][1], ef[kk][2], ef[kk][3], b2, b3);
+            }
+            float nd[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = g + 8 * (i >> 1);
+                    nd[nt][i] = tok < J.c ? -eta_of(tok) * dl[nt][i] * sp[hg][nt][i] : 0.f;
+                    cs1[hg][nt][i & 1] += nd[nt][i];
+                }
+            dfr[hg][0] = movmatrix_t(pack_bf16(nd[0][0], nd[0][1]));
+            dfr[hg][1] = movmatrix_t(pack_bf16(nd[1][0], nd[1][1]));
+            dfr[hg][2] = movmatrix_t(pack_bf16(nd[0][2], nd[0][3]));
+            dfr[hg][3] = movmatrix_t(pack_bf16(nd[1][2], nd[1][3]));
+        }
+        float aq[2][2][4];
+        {
+            uint32_t qf[NK][4], spf[4];
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) ldsm_x4(tQ + mtoff<D>(rowA, 16 * kk + colA), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+            ldsm_x4(base + C::SP_OFF + rowA * 48 + colA * 2, spf[0], spf[1], spf[2], spf[3]);
+#pragma unroll
+            for (int hg = 0; hg < 2; ++hg) {
+                // H_q = Q W1 + c1 + S' (-Dt); A_q = SiLU(H_q) -> shared
+                float hq[2][4] = {};
+#pragma unroll
+                for (int kk = 0; kk < NK; ++kk) {
+                    uint32_t b[4];
+                    w1_b(hg, kk, b);
+                    mma_bf16(hq[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b[0], b[1]);
+                    mma_bf16(hq[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b[2], b[3]);
+                }
+                mma_bf16(hq[0], spf[0], spf[1], spf[2], spf[3], dfr[hg][0], dfr[hg][2]);
+                mma_bf16(hq[1], spf[0], spf[1], spf[2], spf[3], dfr[hg][1], dfr[hg][3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float h = hq[nt][i] + c1r[hg][nt][i & 1];
+                        aq[hg][nt][i] = h * sigmoid_f(h);
+                    }
+                stsm_x4(AQ + rowA * C::AR + (32 * w + 16 * hg + colA) * 2, pack_bf16(aq[hg][0][0], aq[hg][0][1]),
+                        pack_bf16(aq[hg][0][2], aq[hg][0][3]), pack_bf16(aq[hg][1][0], aq[hg][1][1]),
+                        pack_bf16(aq[hg][1][2], aq[hg][1][3]));
+            }
+        }
+        {
+            // W1^T += (-Dt^T) K,  W2 += A_k^T (-Et) (as W2^T += (-Et^T) A_k tiles)
+            uint32_t ktf[NK][4], nef[NK][4];
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                ldsm_x4_t(tK + mtoff<D>(rowA, 16 * kk + colA), ktf[kk][0], ktf[kk][1], ktf[kk][2], ktf[kk][3]);
+                ldsm_x4_t(NEB + rowB * C::ER + (16 * kk + colB) * 2, nef[kk][0], nef[kk][1], nef[kk][2], nef[kk][3]);
+            }
+#pragma unroll
+            for (int hg = 0; hg < 2; ++hg) {
+#pragma unroll
+                for (int j2 = 0; j2 < NK; ++j2) {
+                    mma_bf16(w1[hg][2 * j2], dfr[hg][0], dfr[hg][1], dfr[hg][2], dfr[hg][3], ktf[j2][0], ktf[j2][1]);
+                    mma_bf16(w1[hg][2 * j2 + 1], dfr[hg][0], dfr[hg][1], dfr[hg][2], dfr[hg][3], ktf[j2][2], ktf[j2][3]);
+                }
+                const uint32_t bt00 = movmatrix_t(akp[hg][0]), bt01 = movmatrix_t(akp[hg][1]);
+                const uint32_t bt10 = movmatrix_t(akp[hg][2]), bt11 = movmatrix_t(akp[hg][3]);
+#pragma unroll
+                for (int mt = 0; mt < NK; ++mt) {
+                    mma_bf16(w2[hg][mt][0], nef[mt][0], nef[mt][1], nef[mt][2], nef[mt][3], bt00, bt01);
+                    mma_bf16(w2[hg][mt][1], nef[mt][0], nef[mt][1], nef[mt][2], nef[mt][3], bt10, bt11);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        float v = cs1[hg][nt][i];
+                        v += __shfl_xor_sync(0xffffffffu, v, 4);
+                        v += __shfl_xor_sync(0xffffffffu, v, 8);
+                        v += __shfl_xor_sync(0xffffffffu, v, 16);
+                        c1r[hg][nt][i] += v;
+                    }
+            }
+            put_w2(W2N);
+        }
+        __syncthreads();  // B3: A_q visible; the stage's tiles are no longer read
+
+        // phase 4: P = A_q W2 (mini-batch start copy) on columns c0 ..; partial
+        // A_q A_k^T over this warp's hidden units
+        float pz[2][4] = {};
+        col_product(W2B, AQ, pz);
+        {
+            float s2[2][4] = {};
+#pragma unroll
+            for (int hg = 0; hg < 2; ++hg) {
+                const uint32_t a0 = pack_bf16(aq[hg][0][0], aq[hg][0][1]), a1 = pack_bf16(aq[hg][0][2], aq[hg][0][3]);
+                const uint32_t a2 = pack_bf16(aq[hg][1][0], aq[hg][1][1]), a3 = pack_bf16(aq[hg][1][2], aq[hg][1][3]);
+                mma_bf16(s2[0], a0, a1, a2, a3, akp[hg][0], akp[hg][2]);  // key tokens 0-7
+                mma_bf16(s2[1], a0, a1, a2, a3, akp[hg][1], akp[hg][3]);  // key tokens 8-15
+            }
+            float *sf = reinterpret_cast<float *>(gbase + C::S2F_OFF) + w * 16 * C::S2R;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                *reinterpret_cast<float2 *>(sf + g * C::S2R + 8 * nt + 2 * t4) = make_float2(s2[nt][0], s2[nt][1]);
+                *reinterpret_cast<float2 *>(sf + (g + 8) * C::S2R + 8 * nt + 2 * t4) = make_float2(s2[nt][2], s2[nt][3]);
+            }
+        }
+        __syncthreads();  // B4: partial A_q A_k^T visible
+        {
+            // S2' = M .* (sum of the partials + 1), one element per thread, as bf16
+            const int e = 32 * w + lane, r = e >> 4, kc = e & 15;
+            const float *sf = reinterpret_cast<const float *>(gbase + C::S2F_OFF);
+            float sum = 0.f;
+#pragma unroll
+            for (int u = 0; u < NW; ++u) sum += sf[(u * 16 + r) * C::S2R + kc];
+            const bool keep = kc < J.c && (!p.causal || kc <= r);
+            reinterpret_cast<__nv_bfloat16 *>(gbase + C::S2P_OFF + r * 48)[kc] = __float2bfloat16_rn(keep ? sum + 1.f : 0.f);
+        }
+        __syncthreads();  // B5: S2' visible
+        {
+            uint32_t sa[4];
+            ldsm_x4(base + C::S2P_OFF + rowA * 48 + colA * 2, sa[0], sa[1], sa[2], sa[3]);
+            float zz[4] = {pz[0][0] + pz[1][0], pz[0][1] + pz[1][1], pz[0][2] + pz[1][2], pz[0][3] + pz[1][3]};
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(NEB + (uint32_t)(lane & 15) * C::ER + c0 * 2, b0, b1, b2, b3);
+            mma_bf16(zz, sa[0], sa[1], sa[2], sa[3], b0, b1);
+            __nv_bfloat16 *zb = p.z + ((size_t)bh * T + J.t0) * D + c0 + 2 * t4;
+            if (g < J.c) *reinterpret_cast<uint32_t *>(zb + (size_t)g * D) = pack_bf16(zz[0] + c2r[0], zz[1] + c2r[1]);
+            if (g + 8 < J.c)
+                *reinterpret_cast<uint32_t *>(zb + (size_t)(g + 8) * D) = pack_bf16(zz[2] + c2r[0], zz[3] + c2r[1]);
+        }
+        c2r[0] += cs2[0];
+        c2r[1] += cs2[1];
+        w2cur ^= 1;
+    }
+
+    // ------------------------------------------------------------ final state
+#pragma unroll
+    for (int hg = 0; hg < 2; ++hg) {
+        const int h0 = 32 * w + 16 * hg;
+        if (p.W1o) {
+            float *o = p.W1o + (size_t)bh * D * M;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int r = 8 * j + 2 * t4;
+                o[(size_t)r * M + h0 + g] = w1[hg][j][0];
+                o[(size_t)(r + 1) * M + h0 + g] = w1[hg][j][1];
+                o[(size_t)r * M + h0 + g + 8] = w1[hg][j][2];
+                o[(size_t)(r + 1) * M + h0 + g + 8] = w1[hg][j][3];
+            }
+        }
+        if (p.c1o && g == 0) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) p.c1o[(size_t)bh * M + h0 + 8 * nt + 2 * t4 + i] = c1r[hg][nt][i];
+        }
+        if (p.W2o) {
+            float *o = p.W2o + (size_t)bh * M * D;
+#pragma unroll
+            for (int mt = 0; mt < NK; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int hr = h0 + 8 * nt + 2 * t4, dc = 16 * mt + g;
+                    o[(size_t)hr * D + dc] = w2[hg][mt][nt][0];
+                    o[(size_t)(hr + 1) * D + dc] = w2[hg][mt][nt][1];
+                    o[(size_t)hr * D + dc + 8] = w2[hg][mt][nt][2];
+                    o[(size_t)(hr + 1) * D + dc + 8] = w2[hg][mt][nt][3];
+                }
+        }
+    }
+    if (p.c2o && g == 0) {
+        p.c2o[(size_t)bh * D + c0 + 2 * t4] = c2r[0];
+        p.c2o[(size_t)bh * D + c0 + 2 * t4 + 1] = c2r[1];
+    }
+    // make sure no copy is still landing in shared memory when the CTA ends
+    if (warp == 0)
+        for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
+            if (!mbar_wait(bar_full + 8 * (j % NS), (j / NS) & 1, p.status, kSiteDrain)) break;
+}
+
+static int launch_mlp_w8(const MlpArgs &a, const CUtensorMap *maps)
+{
+    using C = W8Cfg;
+    if (cudaFuncSetAttribute(ttt_mlp_w8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+        return -4;
+    MlpParams p;
+    p.H = a.H;
+    p.T = a.T;
+    p.b = a.b;
+    p.causal = a.causal;
+    p.per_batch = a.per_batch;
+    p.eta = a.eta;
+    p.eta_scalar = a.eta_scalar;
+    p.W1 = a.W1;
+    p.c1 = a.c1;
+    p.W2 = a.W2;
+    p.c2 = a.c2;
+    p.z = static_cast<__nv_bfloat16 *>(a.z);
+    p.W1o = a.W1o;
+    p.c1o = a.c1o;
+    p.W2o = a.W2o;
+    p.c2o = a.c2o;
+    p.status = a.status;
+    ttt_mlp_w8_kernel<<<a.B * a.H, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
 // d in {16, 32, 64} with hidden width m = 4d.
 int launch_mlp_bf16(const MlpArgs &a)
 {
@@ -630,7 +1151,7 @@ int launch_mlp_bf16(const MlpArgs &a)
     switch (a.d) {
     case 16: return launch_mlp_t<16>(a, maps);
     case 32: return launch_mlp_t<32>(a, maps);
-    case 64: return launch_mlp_t<64>(a, maps);
+    case 64: return a.b <= 16 ? launch_mlp_w8(a, maps) : launch_mlp_t<64>(a, maps);
     default: return -2;
     }
 }
