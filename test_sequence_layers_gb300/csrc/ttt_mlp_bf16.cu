@@ -667,13 +667,14 @@ struct W8Cfg {
     static constexpr int W2B_OFF = NS * STAGE;                  // two bf16 W2 [M][W2R]
     static constexpr int AK_OFF = W2B_OFF + 2 * M * W2R;        // bf16 A_k [16][AR]
     static constexpr int AQ_OFF = AK_OFF + 16 * AR;             // bf16 A_q [16][AR]
-    static constexpr int EB_OFF = AQ_OFF + 16 * AR;             // bf16 E [16][ER]
-    static constexpr int NEB_OFF = EB_OFF + 16 * ER;            // bf16 -Et [16][ER]
+    static constexpr int EB_OFF = AQ_OFF + 16 * AR;             // bf16 E [2][16][ER] (by chunk parity)
+    static constexpr int NEB_OFF = EB_OFF + 2 * 16 * ER;        // bf16 -Et [2][16][ER]
     static constexpr int S2R = 20;                              // fp32 row stride of a partial (bank spread)
-    static constexpr int SP_OFF = NEB_OFF + 16 * ER;            // bf16 S' = M .* (Q K^T + 1) [16][48 B]
+    static constexpr int SP_OFF = NEB_OFF + 2 * 16 * ER;        // bf16 S' = M .* (Q K^T + 1) [16][48 B]
     static constexpr int S2P_OFF = SP_OFF + 16 * 48;            // bf16 S2' = M .* (A_q A_k^T + 1) [16][48 B]
     static constexpr int S2F_OFF = S2P_OFF + 16 * 48;           // fp32 [NW][16][S2R] partial A_q A_k^T
-    static constexpr int BAR_OFF = S2F_OFF + NW * 16 * S2R * 4; // full[NS], abort flag
+    static constexpr int C2S_OFF = S2F_OFF + NW * 16 * S2R * 4; // fp32 [2][D] c2 at a chunk's start
+    static constexpr int BAR_OFF = C2S_OFF + 2 * D * 4;         // full[NS], abort flag
     static constexpr int SMEM = BAR_OFF + NS * 8 + 16 + 1024;
 };
 static_assert(MlpCfg<64>::RB == 128, "tile rows of 128 bytes");
@@ -697,8 +698,7 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
     const bool has_eta = p.eta != nullptr;
     const uint32_t bar_full = base + C::BAR_OFF;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::BAR_OFF + NS * 8);
-    const uint32_t AK = base + C::AK_OFF, AQ = base + C::AQ_OFF, EB = base + C::EB_OFF;
-    const uint32_t NEB = base + C::NEB_OFF;
+    const uint32_t AK = base + C::AK_OFF, AQ = base + C::AQ_OFF;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(bar_full + 8 * s, 1 + (has_eta ? 32 : 0));
         *abort_flag = 0;
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
     __syncthreads();
 
     // ---------------------------------------------------------- initial state
-    const int w = warp, c0 = 8 * w;
+    const int w = warp;
     const size_t ps = p.per_batch ? (size_t)bh : (size_t)(bh % p.H);
     const float *W1g = p.W1 + ps * D * M, *c1g = p.c1 + ps * M;
     const float *W2g = p.W2 + ps * M * D, *c2g = p.c2 + ps * D;
@@ -742,7 +742,12 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 2; ++i) c1r[hg][nt][i] = c1g[h0 + 8 * nt + 2 * t4 + i];
     }
-    float c2r[2] = {c2g[c0 + 2 * t4], c2g[c0 + 2 * t4 + 1]};  // c2 of columns c0 + 2t4 + i
+    // c2 of columns 16w + 8nt + 2t4 + i (kept by warps 0-3, which form E)
+    float c2r[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) c2r[nt][i] = w < 4 ? c2g[16 * w + 8 * nt + 2 * t4 + i] : 0.f;
     // bf16 copy of this warp's W2 rows into buffer `buf` ([hidden][d], transposed
     // stores of the accumulator tiles)
     auto put_w2 = [&](uint32_t buf) {
@@ -801,12 +806,17 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
     }
     __syncthreads();
 
-    // acc += X W2[:, c0 .. c0+7] over all hidden units, X = A_k or A_q ([16][AR] bf16);
-    // the fragments of the next 32 hidden units load while the current ones multiply
-    auto col_product = [&](uint32_t W, uint32_t X, float (&acc)[2][4]) {
-        uint32_t fb[2][4], fa[2][8];
+    // acc[nt] += X W[:, cc + 8nt .. +7] over all hidden units (X = A_k or A_q,
+    // [16][AR] bf16; cc = 16 (w mod 4)); the fragments of the next 32 hidden units
+    // load while the current ones multiply
+    const int cc = 16 * (w & 3);
+    auto col_product16 = [&](uint32_t W, uint32_t X, float (&acc)[2][2][4]) {
+        uint32_t fb[2][2][4], fa[2][8];
         auto ld = [&](int kp, int sl) {
-            ldsm_x4_t(W + (uint32_t)(32 * kp + lane) * C::W2R + c0 * 2, fb[sl][0], fb[sl][1], fb[sl][2], fb[sl][3]);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+                ldsm_x4_t(W + (uint32_t)(32 * kp + lane) * C::W2R + (cc + 8 * nt) * 2, fb[sl][nt][0], fb[sl][nt][1],
+                          fb[sl][nt][2], fb[sl][nt][3]);
             ldsm_x4(X + rowA * C::AR + (32 * kp + colA) * 2, fa[sl][0], fa[sl][1], fa[sl][2], fa[sl][3]);
             ldsm_x4(X + rowA * C::AR + (32 * kp + 16 + colA) * 2, fa[sl][4], fa[sl][5], fa[sl][6], fa[sl][7]);
         };
@@ -815,23 +825,61 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
         for (int kp = 0; kp < NKM / 2; ++kp) {
             if (kp + 1 < NKM / 2) ld(kp + 1, (kp + 1) & 1);
             const int sl = kp & 1;
-            mma_bf16(acc[0], fa[sl][0], fa[sl][1], fa[sl][2], fa[sl][3], fb[sl][0], fb[sl][1]);
-            mma_bf16(acc[1], fa[sl][4], fa[sl][5], fa[sl][6], fa[sl][7], fb[sl][2], fb[sl][3]);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                mma_bf16(acc[nt][0], fa[sl][0], fa[sl][1], fa[sl][2], fa[sl][3], fb[sl][nt][0], fb[sl][nt][1]);
+                mma_bf16(acc[nt][1], fa[sl][4], fa[sl][5], fa[sl][6], fa[sl][7], fb[sl][nt][2], fb[sl][nt][3]);
+            }
         }
     };
+    // A_q A_k^T partial sums of all warps -> S2' = M .* (A_q A_k^T + 1) as bf16, one
+    // element per thread (c: tokens of that chunk)
+    auto reduce_s2 = [&](int c) {
+        const int e = 32 * w + lane, r = e >> 4, kc = e & 15;
+        const float *sf = reinterpret_cast<const float *>(gbase + C::S2F_OFF);
+        float sum = 0.f;
+#pragma unroll
+        for (int u = 0; u < NW; ++u) sum += sf[(u * 16 + r) * C::S2R + kc];
+        const bool keep = kc < c && (!p.causal || kc <= r);
+        reinterpret_cast<__nv_bfloat16 *>(gbase + C::S2P_OFF + r * 48)[kc] = __float2bfloat16_rn(keep ? sum + 1.f : 0.f);
+    };
+    // z of a chunk on columns cc .. cc+15: P (its A_q times its W2 copy) + c2 + S2' (-Et),
+    // tokens t0 .. t0+c-1; c2 at the chunk's start from the snapshot `c2s`
+    auto store_z = [&](const float (&pz)[2][2][4], uint32_t NEBc, int t0, int c, const float *c2s) {
+        uint32_t sa[4], b0, b1, b2, b3;
+        ldsm_x4(base + C::S2P_OFF + rowA * 48 + colA * 2, sa[0], sa[1], sa[2], sa[3]);
+        ldsm_x4_t(NEBc + (uint32_t)(lane & 15) * C::ER + (cc + 8 * (lane >> 4)) * 2, b0, b1, b2, b3);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float zz[4] = {pz[nt][0][0] + pz[nt][1][0], pz[nt][0][1] + pz[nt][1][1], pz[nt][0][2] + pz[nt][1][2],
+                           pz[nt][0][3] + pz[nt][1][3]};
+            mma_bf16(zz, sa[0], sa[1], sa[2], sa[3], nt ? b2 : b0, nt ? b3 : b1);
+            const int col = cc + 8 * nt + 2 * t4;
+            const float x = c2s[col], y = c2s[col + 1];
+            __nv_bfloat16 *zb = p.z + ((size_t)bh * T + t0) * D + col;
+            if (g < c) *reinterpret_cast<uint32_t *>(zb + (size_t)g * D) = pack_bf16(zz[0] + x, zz[1] + y);
+            if (g + 8 < c) *reinterpret_cast<uint32_t *>(zb + (size_t)(g + 8) * D) = pack_bf16(zz[2] + x, zz[3] + y);
+        }
+    };
+    int prev_t0 = 0, prev_c = 0;   // the previous chunk, whose outputs are finished one chunk later
 
     // ---------------------------------------------------------------- chunks
     JobIter it(T, p.b, p.causal);
-    for (int jb = 0; it.valid(); it.next(), ++jb) {
+    int jb = 0;
+    for (; it.valid(); it.next(), ++jb) {
         const Job J = it.get();
         if (warp == 0) issue_next();
         const int s = jb % NS;
         const uint32_t tQ = base + s * C::STAGE, tK = tQ + C::TILE, tV = tQ + 2 * C::TILE;
         const float *eta_s = reinterpret_cast<const float *>(gbase + s * C::STAGE + 3 * C::TILE);
         auto eta_of = [&](int tok) -> float { return has_eta ? eta_s[tok] : p.eta_scalar; };
-        // bf16 W2 at this mini-batch's start, and the buffer of the next one
+        // bf16 W2 at this mini-batch's start; the other buffer holds the previous
+        // chunk's copy (its queries are finished in phase 2) and then receives the next
         const uint32_t W2B = base + C::W2B_OFF + (uint32_t)(w2cur * M * C::W2R);
         const uint32_t W2N = base + C::W2B_OFF + (uint32_t)((w2cur ^ 1) * M * C::W2R);
+        const uint32_t EB = base + C::EB_OFF + (uint32_t)((jb & 1) * 16 * C::ER);
+        const uint32_t NEB = base + C::NEB_OFF + (uint32_t)((jb & 1) * 16 * C::ER);
+        const uint32_t NEBp = base + C::NEB_OFF + (uint32_t)(((jb & 1) ^ 1) * 16 * C::ER);
         if (!mbar_wait(bar_full + 8 * s, (jb / NS) & 1, p.status, kSiteConsumerFull)) *abort_flag = 1;
 
         // phase 1: H_k = K W1 + c1, A_k = SiLU(H_k), SiLU'(H_k); scores for the queries
@@ -870,14 +918,14 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
         if (w >= NW - 2) {
             // S' = M .* (Q K^T + 1): warp NW-2 forms keys 0-7, warp NW-1 keys 8-15
             const int nt = w - (NW - 2);
+            uint32_t qa[NK][4];
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) ldsm_x4(tQ + mtoff<D>(rowA, 16 * kk + colA), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+            // K's A fragments are the B operand: keys 8nt + g take registers nt, nt + 2
             float sc[4] = {};
 #pragma unroll
-            for (int kk = 0; kk < NK; ++kk) {
-                uint32_t a0, a1, a2, a3, b00, b01, b10, b11;
-                ldsm_x4(tQ + mtoff<D>(rowA, 16 * kk + colA), a0, a1, a2, a3);
-                ldsm_x4(tK + mtoff<D>(rowB, 16 * kk + colB), b00, b01, b10, b11);
-                mma_bf16(sc, a0, a1, a2, a3, nt ? b10 : b00, nt ? b11 : b01);
-            }
+            for (int kk = 0; kk < NK; ++kk)
+                mma_bf16(sc, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], nt ? kf[kk][1] : kf[kk][0], nt ? kf[kk][3] : kf[kk][2]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int tq_ = g + 8 * (i >> 1), ss = 8 * nt + 2 * t4 + (i & 1);
@@ -889,38 +937,51 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
                          "r"(pack_bf16(sc[0], sc[1])), "r"(pack_bf16(sc[2], sc[3]))
                          : "memory");
         }
-        __syncthreads();  // B1: A_k visible
+        if (jb > 0) reduce_s2(prev_c);  // the previous chunk's partials (written before its B3)
+        __syncthreads();  // B1: A_k, S', previous S2' visible
         if (*abort_flag) break;
 
-        // phase 2: E = A_k W2 + c2 - V on columns c0 .. c0+7; -Et
-        float cs2[2] = {0.f, 0.f};  // column sums of -Et (the c2 write of this mini-batch)
-        {
-            float e[2][4] = {};
-            col_product(W2B, AK, e);
+        // phase 2: warps 0-3: E = A_k W2 + c2 - V and -Et on columns 16w .. 16w+15;
+        // warps 4-7: the previous chunk's P = A_q W2 and z on columns 16(w-4) ..
+        float cs2[2][2] = {};  // column sums of -Et (the c2 write of this mini-batch)
+        if (w < 4) {
+            float e[2][2][4] = {};
+            col_product16(W2B, AK, e);
+            float *c2snap = reinterpret_cast<float *>(gbase + C::C2S_OFF) + (jb & 1) * D;
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {  // token rows g, g + 8
-                const int tok = g + 8 * r;
-                const uint32_t vw =
-                    *reinterpret_cast<const uint32_t *>(gbase + (tV - base) + mtoff<D>(tok, c0 + 2 * t4));
-                const float ex = e[0][2 * r] + e[1][2 * r] + c2r[0] - bf16_lo(vw);
-                const float ey = e[0][2 * r + 1] + e[1][2 * r + 1] + c2r[1] - bf16_hi(vw);
-                const bool ok = tok < J.c;
-                const float et = -eta_of(tok);
-                const float nx = ok ? et * ex : 0.f, ny = ok ? et * ey : 0.f;
-                cs2[0] += nx;
-                cs2[1] += ny;
-                *reinterpret_cast<uint32_t *>(gbase + C::EB_OFF + tok * C::ER + (c0 + 2 * t4) * 2) = pack_bf16(ex, ey);
-                *reinterpret_cast<uint32_t *>(gbase + C::NEB_OFF + tok * C::ER + (c0 + 2 * t4) * 2) =
-                    pack_bf16(nx, ny);
-            }
+            for (int nt = 0; nt < 2; ++nt) {
+                const int col = cc + 8 * nt + 2 * t4;
+                if (g == 0) {
+                    c2snap[col] = c2r[nt][0];
+                    c2snap[col + 1] = c2r[nt][1];
+                }
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                cs2[i] += __shfl_xor_sync(0xffffffffu, cs2[i], 4);
-                cs2[i] += __shfl_xor_sync(0xffffffffu, cs2[i], 8);
-                cs2[i] += __shfl_xor_sync(0xffffffffu, cs2[i], 16);
+                for (int r = 0; r < 2; ++r) {  // token rows g, g + 8
+                    const int tok = g + 8 * r;
+                    const uint32_t vw = *reinterpret_cast<const uint32_t *>(gbase + (tV - base) + mtoff<D>(tok, col));
+                    const float ex = e[nt][0][2 * r] + e[nt][1][2 * r] + c2r[nt][0] - bf16_lo(vw);
+                    const float ey = e[nt][0][2 * r + 1] + e[nt][1][2 * r + 1] + c2r[nt][1] - bf16_hi(vw);
+                    const bool ok = tok < J.c;
+                    const float et = -eta_of(tok);
+                    const float nx = ok ? et * ex : 0.f, ny = ok ? et * ey : 0.f;
+                    cs2[nt][0] += nx;
+                    cs2[nt][1] += ny;
+                    *reinterpret_cast<uint32_t *>(gbase + (EB - base) + tok * C::ER + col * 2) = pack_bf16(ex, ey);
+                    *reinterpret_cast<uint32_t *>(gbase + (NEB - base) + tok * C::ER + col * 2) = pack_bf16(nx, ny);
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    cs2[nt][i] += __shfl_xor_sync(0xffffffffu, cs2[nt][i], 4);
+                    cs2[nt][i] += __shfl_xor_sync(0xffffffffu, cs2[nt][i], 8);
+                    cs2[nt][i] += __shfl_xor_sync(0xffffffffu, cs2[nt][i], 16);
+                }
             }
+        } else if (jb > 0) {
+            float pz[2][2][4] = {};
+            col_product16(W2N, AQ, pz);
+            store_z(pz, NEBp, prev_t0, prev_c, reinterpret_cast<const float *>(gbase + C::C2S_OFF) + ((jb - 1) & 1) * D);
         }
-        __syncthreads();  // B2: E, -Et visible
+        __syncthreads();  // B2: E, -Et visible; the previous chunk's A_q and W2 copy no longer read
 
         // phase 3: delta; query pre-activations (W1, c1 of the mini-batch start);
         // then the weight updates and the next bf16 W2 copy
@@ -1019,13 +1080,8 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
             }
             put_w2(W2N);
         }
-        __syncthreads();  // B3: A_q visible; the stage's tiles are no longer read
-
-        // phase 4: P = A_q W2 (mini-batch start copy) on columns c0 ..; partial
-        // A_q A_k^T over this warp's hidden units
-        float pz[2][4] = {};
-        col_product(W2B, AQ, pz);
         {
+            // partial A_q A_k^T over this warp's hidden units, straight from registers
             float s2[2][4] = {};
 #pragma unroll
             for (int hg = 0; hg < 2; ++hg) {
@@ -1041,33 +1097,26 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
                 *reinterpret_cast<float2 *>(sf + (g + 8) * C::S2R + 8 * nt + 2 * t4) = make_float2(s2[nt][2], s2[nt][3]);
             }
         }
-        __syncthreads();  // B4: partial A_q A_k^T visible
-        {
-            // S2' = M .* (sum of the partials + 1), one element per thread, as bf16
-            const int e = 32 * w + lane, r = e >> 4, kc = e & 15;
-            const float *sf = reinterpret_cast<const float *>(gbase + C::S2F_OFF);
-            float sum = 0.f;
+        __syncthreads();  // B3: A_q, partials visible; the stage's tiles are no longer read
+        prev_t0 = J.t0;
+        prev_c = J.c;
 #pragma unroll
-            for (int u = 0; u < NW; ++u) sum += sf[(u * 16 + r) * C::S2R + kc];
-            const bool keep = kc < J.c && (!p.causal || kc <= r);
-            reinterpret_cast<__nv_bfloat16 *>(gbase + C::S2P_OFF + r * 48)[kc] = __float2bfloat16_rn(keep ? sum + 1.f : 0.f);
+        for (int nt = 0; nt < 2; ++nt) {
+            c2r[nt][0] += cs2[nt][0];
+            c2r[nt][1] += cs2[nt][1];
         }
-        __syncthreads();  // B5: S2' visible
-        {
-            uint32_t sa[4];
-            ldsm_x4(base + C::S2P_OFF + rowA * 48 + colA * 2, sa[0], sa[1], sa[2], sa[3]);
-            float zz[4] = {pz[0][0] + pz[1][0], pz[0][1] + pz[1][1], pz[0][2] + pz[1][2], pz[0][3] + pz[1][3]};
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(NEB + (uint32_t)(lane & 15) * C::ER + c0 * 2, b0, b1, b2, b3);
-            mma_bf16(zz, sa[0], sa[1], sa[2], sa[3], b0, b1);
-            __nv_bfloat16 *zb = p.z + ((size_t)bh * T + J.t0) * D + c0 + 2 * t4;
-            if (g < J.c) *reinterpret_cast<uint32_t *>(zb + (size_t)g * D) = pack_bf16(zz[0] + c2r[0], zz[1] + c2r[1]);
-            if (g + 8 < J.c)
-                *reinterpret_cast<uint32_t *>(zb + (size_t)(g + 8) * D) = pack_bf16(zz[2] + c2r[0], zz[3] + c2r[1]);
-        }
-        c2r[0] += cs2[0];
-        c2r[1] += cs2[1];
         w2cur ^= 1;
+    }
+
+    if (prev_c > 0 && !*abort_flag) {  // the last chunk's outputs
+        reduce_s2(prev_c);
+        __syncthreads();
+        if (w >= 4) {
+            float pz[2][2][4] = {};
+            col_product16(base + C::W2B_OFF + (uint32_t)((w2cur ^ 1) * M * C::W2R), AQ, pz);
+            store_z(pz, base + C::NEB_OFF + (uint32_t)(((jb - 1) & 1) * 16 * C::ER), prev_t0, prev_c,
+                    reinterpret_cast<const float *>(gbase + C::C2S_OFF) + ((jb - 1) & 1) * D);
+        }
     }
 
     // ------------------------------------------------------------ final state
@@ -1105,9 +1154,12 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
                 }
         }
     }
-    if (p.c2o && g == 0) {
-        p.c2o[(size_t)bh * D + c0 + 2 * t4] = c2r[0];
-        p.c2o[(size_t)bh * D + c0 + 2 * t4 + 1] = c2r[1];
+    if (p.c2o && g == 0 && w < 4) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            p.c2o[(size_t)bh * D + cc + 8 * nt + 2 * t4] = c2r[nt][0];
+            p.c2o[(size_t)bh * D + cc + 8 * nt + 2 * t4 + 1] = c2r[nt][1];
+        }
     }
     // make sure no copy is still landing in shared memory when the CTA ends
     if (warp == 0)
