@@ -85,7 +85,7 @@ def kernel_name(inp):
         return "ttt_linear_f32_kernel" if inp.kind == "linear" else "ttt_mlp_f32_kernel"
     if inp.kind == "linear":
         return "ttt_linear_b16_kernel" if min(inp.b, inp.T) == 16 and inp.d <= 64 else "ttt_linear_bf16_kernel"
-    return "ttt_mlp_bf16_kernel"
+    return "ttt_mlp_w8_kernel" if inp.d == 64 and min(inp.b, inp.T) <= 16 else "ttt_mlp_bf16_kernel"
 
 
 def recorded_traffic(workload):
