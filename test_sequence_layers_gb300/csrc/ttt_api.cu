@@ -134,9 +134,11 @@ ttt_status ttt_linear_fwd(const ttt_linear_desc *desc, const void *q, const void
     if (!a.status) return TTT_ERR_LAUNCH;
 
     int rc;
-    if (D.io_dtype == TTT_BF16)
-        rc = (a.b == 16 && a.d <= 64) ? ttt::launch_linear_b16(a) : ttt::launch_linear_bf16(a);
-    else
+    if (D.io_dtype == TTT_BF16) {
+        rc = ttt::launch_linear_fb(a);  // full-batch mini-batch: no serial chain
+        if (rc == TTT_ERR_UNSUPPORTED)
+            rc = (a.b == 16 && a.d <= 64) ? ttt::launch_linear_b16(a) : ttt::launch_linear_bf16(a);
+    } else
         rc = ttt::launch_linear_f32(a);
     if (rc == 0) g_launches.fetch_add(1, std::memory_order_relaxed);
     return code(rc);

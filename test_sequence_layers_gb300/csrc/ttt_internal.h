@@ -52,6 +52,7 @@ inline bool encode_qkv(CUtensorMap *maps, const void *q, const void *k, const vo
 // Each returns 0 or a negative ttt_status code.
 int launch_linear_bf16(const LinearArgs &a);
 int launch_linear_b16(const LinearArgs &a);  // b = 16 specialisation (d <= 64)
+int launch_linear_fb(const LinearArgs &a);   // one full-batch mini-batch (b = T <= 256, non-causal, d = 64); -2 otherwise
 int launch_linear_f32(const LinearArgs &a);
 int launch_mlp_f32(const MlpArgs &a);
 int launch_mlp_bf16(const MlpArgs &a);

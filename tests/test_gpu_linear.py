@@ -82,6 +82,15 @@ def test_full_batch_noncausal_single_block():
     _check(inp)
 
 
+@pytest.mark.parametrize("T", [1, 17, 64, 100, 196, 256, 300])
+def test_full_batch_lengths(T):
+    """b >= T, non-causal (one inner GD step over the whole sequence, every query
+    reads the updated weights): short, ragged, box-aligned and longest on-chip
+    lengths, one beyond them, per-token eta, per-batch W0."""
+    inp = G.synth.make("linear", B=2, H=2, T=T, d=64, b=T + 5, causal=False, eta="sigmoid", seed=400 + T)
+    _check(inp, per_batch_w0=True)
+
+
 @pytest.mark.parametrize("split", [64, 48])
 def test_split_run_continues_sequence(split):
     """W_final passed back as W0 continues the sequence (chunked prefill).  The
