@@ -63,6 +63,16 @@ def test_bf16_small(d, b, causal):
     _check(inp)
 
 
+@pytest.mark.parametrize("T", [1, 16, 17, 75, 196])
+def test_bf16_full_batch(T):
+    """b >= T, non-causal: one inner GD step over the whole sequence, every query
+    reads the updated weights (short, chunk-aligned and ragged lengths, biases,
+    per-token eta)."""
+    inp = _mlp_inputs(2, 2, T, 64, T + 3, False, eta="sigmoid", seed=70 + T, bias=0.1)
+    inp.eta = inp.eta * 0.2
+    _check(inp)
+
+
 def test_bf16_per_token_eta_and_per_batch_params():
     inp = _mlp_inputs(3, 2, 90, 64, 16, True, eta="sigmoid", seed=21, bias=0.1)
     inp.eta = inp.eta * 0.1  # eta_t = 0.1 sigmoid(g_t): bounded dynamics
