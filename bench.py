@@ -195,10 +195,19 @@ def run_ours(args, rank, world, inp, peaks):
     B, H, d = inp.B, inp.H, inp.d
     if inp.kind == "linear":
         outs = torch.empty((B, H, d, d), device=dev)
+        # fewer chains than SMs: the sequence-parallel entry point (affine maps of
+        # segments, scan, segment outputs), with its workspace allocated once
+        need = 0 if args.no_seqpar else abi.ttt_linear_seqpar_workspace(
+            B, H, inp.T, d, inp.b, inp.causal, dtype=inp.q.dtype)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
 
         def step(qq=q, kk=k, vv=v, ee=eta, zz=z):
-            abi.ttt_linear_fwd(qq, kk, vv, params["W0"], inp.b, inp.causal, eta=ee,
-                               eta_scalar=inp.eta_scalar, z=zz, W_out=outs)
+            if ws is not None:
+                abi.ttt_linear_fwd_seqpar(qq, kk, vv, params["W0"], inp.b, inp.causal, eta=ee,
+                                          eta_scalar=inp.eta_scalar, z=zz, W_out=outs, workspace=ws)
+            else:
+                abi.ttt_linear_fwd(qq, kk, vv, params["W0"], inp.b, inp.causal, eta=ee,
+                                   eta_scalar=inp.eta_scalar, z=zz, W_out=outs)
         out_bytes = [z, outs]
     else:
         m = inp.m
@@ -348,6 +357,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-seqpar", action="store_true",
+                    help="TTT-Linear: always one CTA per chain (no sequence-parallel split)")
     ap.add_argument("--quick", action="store_true",
                     help="warm-up and timed steps only (no clock spin, e2e or CPU baseline); "
                          "used for profiler captures")

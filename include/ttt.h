@@ -47,6 +47,8 @@
 #ifndef TTT_H_
 #define TTT_H_
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -87,6 +89,40 @@ ttt_status ttt_linear_fwd(const ttt_linear_desc *desc,
                           const void *q, const void *k, const void *v,
                           const float *eta, float eta_scalar,
                           const float *W0, void *z, float *W_out, void *stream);
+
+/*
+ * Sequence-parallel TTT-Linear forward: the same results as ttt_linear_fwd (up to the
+ * order of floating-point rounding), for problems with fewer (batch, head) chains
+ * than the GPU has SMs and long sequences.
+ *
+ * One mini-batch step is affine in the weights, W' = (I - K^T diag(eta) K) W +
+ * K^T diag(eta) V ("Learning to (Learn at Test Time)" walkthrough, section 1.2.2,
+ * formula 6, for the linear inner model of section 2.2.1), so each chain is cut
+ * into segments of whole 64-token blocks: the affine maps W -> A W + B of the
+ * segments are computed in parallel, a scan turns them into every segment's start
+ * weights, and the segments' outputs are computed in parallel from those.  The
+ * first segment runs from W0 while the maps are formed.
+ *
+ * Applies to io_dtype TTT_BF16 with mini_batch 16 and d in {16, 32, 64} when the
+ * GPU has at least two SMs per chain; otherwise the call runs ttt_linear_fwd
+ * (workspace unused, may be NULL).
+ *   workspace       : device scratch owned by the caller, 256-byte aligned, at least
+ *                     ttt_linear_seqpar_workspace(desc) bytes; it holds the maps and
+ *                     start weights and must not be touched until the work queued
+ *                     on `stream` has finished.
+ * The work is queued on `stream`; internally it forks to a second stream of the
+ * library's own (one per device, created on the first split call) and joins back
+ * with events, so later work on `stream` sees the outputs.  W_out must not overlap
+ * W0 here (TTT_ERR_ARG): the first segment may still read W0 while the last one
+ * writes W_out.  TTT_ERR_ARG also for a missing, misaligned or too small workspace.
+ */
+size_t ttt_linear_seqpar_workspace(const ttt_linear_desc *desc);
+
+ttt_status ttt_linear_fwd_seqpar(const ttt_linear_desc *desc,
+                                 const void *q, const void *k, const void *v,
+                                 const float *eta, float eta_scalar,
+                                 const float *W0, void *z, float *W_out,
+                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /* TTT-MLP problem description. */
 typedef struct {

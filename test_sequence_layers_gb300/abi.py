@@ -20,8 +20,8 @@ STATUS = {0: "TTT_OK", -1: "TTT_ERR_ARG", -2: "TTT_ERR_UNSUPPORTED", -3: "TTT_ER
           -4: "TTT_ERR_LAUNCH", -5: "TTT_ERR_TIMEOUT"}
 
 # every symbol include/ttt.h declares
-EXPORTS = ("ttt_linear_fwd", "ttt_mlp_fwd", "ttt_sync_status", "ttt_status_str",
-           "ttt_launch_count")
+EXPORTS = ("ttt_linear_fwd", "ttt_linear_seqpar_workspace", "ttt_linear_fwd_seqpar",
+           "ttt_mlp_fwd", "ttt_sync_status", "ttt_status_str", "ttt_launch_count")
 
 
 class LinearDesc(ctypes.Structure):
@@ -57,6 +57,11 @@ def lib():
         vp, fp, f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float
         L.ttt_linear_fwd.argtypes = [ctypes.POINTER(LinearDesc), vp, vp, vp, fp, f, fp, vp, fp, vp]
         L.ttt_linear_fwd.restype = ctypes.c_int
+        L.ttt_linear_seqpar_workspace.argtypes = [ctypes.POINTER(LinearDesc)]
+        L.ttt_linear_seqpar_workspace.restype = ctypes.c_size_t
+        L.ttt_linear_fwd_seqpar.argtypes = [ctypes.POINTER(LinearDesc), vp, vp, vp, fp, f, fp, vp, fp,
+                                            vp, ctypes.c_size_t, vp]
+        L.ttt_linear_fwd_seqpar.restype = ctypes.c_int
         L.ttt_mlp_fwd.argtypes = [ctypes.POINTER(MlpDesc), vp, vp, vp, fp, f, fp, fp, fp, fp,
                                   vp, fp, fp, fp, fp, vp]
         L.ttt_mlp_fwd.restype = ctypes.c_int
@@ -129,6 +134,46 @@ def ttt_linear_fwd(q, k, v, W0, mini_batch, causal=True, eta=None, eta_scalar=1.
                               float(eta_scalar), _ptr(W0), _ptr(z), _ptr(W_out), _stream(stream))
     if rc != 0:
         raise TTTError("ttt_linear_fwd", rc)
+    return z, W_out
+
+
+def ttt_linear_seqpar_workspace(B, H, T, d, mini_batch, causal=True, dtype=torch.bfloat16) -> int:
+    """Workspace bytes ttt_linear_fwd_seqpar needs on the current device (0: the
+    problem is not split)."""
+    io = TTT_BF16 if dtype == torch.bfloat16 else TTT_F32
+    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, 0)
+    return int(lib().ttt_linear_seqpar_workspace(ctypes.byref(desc)))
+
+
+def ttt_linear_fwd_seqpar(q, k, v, W0, mini_batch, causal=True, eta=None, eta_scalar=1.0,
+                          z=None, W_out=None, want_W=True, workspace=None, stream=None):
+    """Sequence-parallel TTT-Linear forward (same arguments as ttt_linear_fwd).
+    workspace: a CUDA uint8 tensor of at least ttt_linear_seqpar_workspace(...) bytes,
+    allocated here when None.  Returns (z, W_final or None)."""
+    io = _check_tokens(q, k, v)
+    B, H, T, d = q.shape
+    W0 = _f32(W0, "W0")
+    eta = _f32(eta, "eta")
+    if W0.shape == (H, d, d):
+        w0s = 0
+    elif W0.shape == (B, H, d, d):
+        w0s = H * d * d
+    else:
+        raise ValueError("W0 must be [H,d,d] or [B,H,d,d]")
+    if z is None:
+        z = torch.empty_like(q)
+    if W_out is None and want_W:
+        W_out = torch.empty((B, H, d, d), device=q.device, dtype=torch.float32)
+    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, w0s)
+    need = int(lib().ttt_linear_seqpar_workspace(ctypes.byref(desc)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().ttt_linear_fwd_seqpar(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(eta),
+                                     float(eta_scalar), _ptr(W0), _ptr(z), _ptr(W_out),
+                                     _ptr(workspace), nbytes, _stream(stream))
+    if rc != 0:
+        raise TTTError("ttt_linear_fwd_seqpar", rc)
     return z, W_out
 
 

@@ -91,11 +91,13 @@ ttt_status code(int rc) { return static_cast<ttt_status>(rc); }
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-ttt_status ttt_linear_fwd(const ttt_linear_desc *desc, const void *q, const void *k, const void *v,
-                          const float *eta, float eta_scalar, const float *W0, void *z,
-                          float *W_out, void *stream)
+// Validates a TTT-Linear call and fills the launch arguments (status TTT_OK or the
+// error to return).
+ttt_status linear_args(const ttt_linear_desc *desc, const void *q, const void *k, const void *v,
+                       const float *eta, float eta_scalar, const float *W0, void *z, float *W_out,
+                       void *stream, ttt::LinearArgs &a)
 {
     if (!desc) return TTT_ERR_ARG;
     const ttt_linear_desc D = *desc;
@@ -113,7 +115,6 @@ ttt_status ttt_linear_fwd(const ttt_linear_desc *desc, const void *q, const void
         overlaps(W_out, sizeof(float) * dd * D.B * D.H, W0, sizeof(float) * dd * D.H))
         return TTT_ERR_ARG;
 
-    ttt::LinearArgs a;
     a.B = D.B;
     a.H = D.H;
     a.T = D.T;
@@ -132,15 +133,80 @@ ttt_status ttt_linear_fwd(const ttt_linear_desc *desc, const void *q, const void
     a.status = status_word();
     a.stream = static_cast<cudaStream_t>(stream);
     if (!a.status) return TTT_ERR_LAUNCH;
+    return TTT_OK;
+}
 
+int launch_linear(const ttt::LinearArgs &a, ttt_dtype io)
+{
     int rc;
-    if (D.io_dtype == TTT_BF16) {
+    if (io == TTT_BF16) {
         rc = ttt::launch_linear_fb(a);  // full-batch mini-batch: no serial chain
         if (rc == TTT_ERR_UNSUPPORTED)
             rc = (a.b == 16 && a.d <= 64) ? ttt::launch_linear_b16(a) : ttt::launch_linear_bf16(a);
     } else
         rc = ttt::launch_linear_f32(a);
+    return rc;
+}
+
+// The split plan of a validated bf16 call (nsplit 0: not split).
+ttt::SeqparPlan seqpar_plan_for(const ttt_linear_desc *desc, const ttt::LinearArgs &a)
+{
+    ttt::SeqparPlan pl;
+    if (desc->io_dtype != TTT_BF16 || !ttt::seqpar_plan(a, pl)) pl = ttt::SeqparPlan{};
+    return pl;
+}
+
+}  // namespace
+
+extern "C" {
+
+ttt_status ttt_linear_fwd(const ttt_linear_desc *desc, const void *q, const void *k, const void *v,
+                          const float *eta, float eta_scalar, const float *W0, void *z,
+                          float *W_out, void *stream)
+{
+    ttt::LinearArgs a;
+    const ttt_status st = linear_args(desc, q, k, v, eta, eta_scalar, W0, z, W_out, stream, a);
+    if (st != TTT_OK) return st;
+    const int rc = launch_linear(a, desc->io_dtype);
     if (rc == 0) g_launches.fetch_add(1, std::memory_order_relaxed);
+    return code(rc);
+}
+
+size_t ttt_linear_seqpar_workspace(const ttt_linear_desc *desc)
+{
+    if (!desc || desc->B < 1 || desc->H < 1 || desc->T < 1 || desc->mini_batch < 1) return 0;
+    ttt::LinearArgs a{};
+    a.B = desc->B;
+    a.H = desc->H;
+    a.T = desc->T;
+    a.d = desc->d;
+    a.b = desc->mini_batch > desc->T ? desc->T : desc->mini_batch;
+    return ttt::seqpar_workspace_bytes(seqpar_plan_for(desc, a));
+}
+
+ttt_status ttt_linear_fwd_seqpar(const ttt_linear_desc *desc, const void *q, const void *k, const void *v,
+                                 const float *eta, float eta_scalar, const float *W0, void *z,
+                                 float *W_out, void *workspace, size_t workspace_bytes, void *stream)
+{
+    ttt::LinearArgs a;
+    const ttt_status st = linear_args(desc, q, k, v, eta, eta_scalar, W0, z, W_out, stream, a);
+    if (st != TTT_OK) return st;
+    const ttt::SeqparPlan pl = seqpar_plan_for(desc, a);
+    int rc, n = 1;
+    if (pl.nsplit < 2) {
+        rc = launch_linear(a, desc->io_dtype);
+    } else {
+        const size_t need = ttt::seqpar_workspace_bytes(pl);
+        if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return TTT_ERR_ARG;
+        // the first segment reads W0 while the last one writes W_out on another stream
+        const size_t dd = sizeof(float) * desc->d * desc->d;
+        const size_t nW0 = desc->w0_batch_stride ? dd * desc->B * desc->H : dd * desc->H;
+        if (W_out && overlaps(W_out, dd * desc->B * desc->H, W0, nW0)) return TTT_ERR_ARG;
+        if (overlaps(workspace, need, z, (size_t)desc->B * desc->H * desc->T * desc->d * 2)) return TTT_ERR_ARG;
+        rc = ttt::launch_linear_seqpar(a, pl, workspace);
+        n = pl.nsplit > 2 ? 4 : 3;  // segment 0, chain (+ maps), scan, later segments
+    }
+    if (rc == 0) g_launches.fetch_add(n, std::memory_order_relaxed);
     return code(rc);
 }
 

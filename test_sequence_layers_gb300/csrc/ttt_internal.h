@@ -52,10 +52,30 @@ inline bool encode_qkv(CUtensorMap *maps, const void *q, const void *k, const vo
 // Each returns 0 or a negative ttt_status code.
 int launch_linear_bf16(const LinearArgs &a);
 int launch_linear_b16(const LinearArgs &a);  // b = 16 specialisation (d <= 64)
+// b = 16, d <= 64 kernel over segments of each chain (segment 0 = tokens [0, len0),
+// segment s >= 1 = [len0 + (s-1) seg_len, len0 + s seg_len)).  prep = false: output
+// units for segments seg0 .. seg0+nseg-1 of every chain, from start weights W0
+// (segment 0) or Wst (segment s: Wst[bh][s-1]).  prep = true: the state chain of
+// segment 0 (its end weights to Wst[bh][0]) and the affine maps of segments
+// 1 .. nsplit-2 (to mapbuf).  maps: the q, k, v descriptors (64-token boxes).
+int launch_linear_b16_segments(const LinearArgs &a, int nsplit, int len0, int seg_len, int seg0, int nseg,
+                               bool prep, float *Wst, float *mapbuf, const CUtensorMap *maps);
 int launch_linear_fb(const LinearArgs &a);   // one full-batch mini-batch (b = T <= 256, non-causal, d = 64); -2 otherwise
 int launch_linear_f32(const LinearArgs &a);
 int launch_mlp_f32(const MlpArgs &a);
 int launch_mlp_bf16(const MlpArgs &a);
+// Sequence-parallel TTT-Linear (ttt_linear_seqpar.cu): the segment plan for a
+// problem (false: the problem is not split, run the one-unit-per-chain path).
+struct SeqparPlan {
+    int nsplit = 0, len0 = 0, seg_len = 0;   // segments per chain, segment lengths
+    size_t map_bytes = 0, wst_bytes = 0;     // scratch: affine maps, start weights
+};
+bool seqpar_plan(const LinearArgs &a, SeqparPlan &pl);
+size_t seqpar_workspace_bytes(const SeqparPlan &pl);
+// Enqueues the split forward on a.stream (forks a side stream and joins it back);
+// ws: at least seqpar_workspace_bytes(pl) bytes of device memory, 256-byte aligned.
+int launch_linear_seqpar(const LinearArgs &a, const SeqparPlan &pl, void *ws);
+
 // Largest d*m the fp32 MLP path holds on chip.
 bool mlp_f32_fits(int d, int m);
 

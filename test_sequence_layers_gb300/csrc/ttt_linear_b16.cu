@@ -18,6 +18,20 @@
 //    second register set while the current chunk's products run;
 //  * full 16-token chunks take a path without per-token bounds masks;
 //  * Z is stored straight from the accumulator registers.
+//
+// Every CTA serves one unit: a token range of one (batch, head) chain, in one of
+// three roles.  Unsplit launches have one output unit per chain (the whole
+// sequence).  The sequence-parallel path (ttt_linear_seqpar.cu) cuts a chain into
+// segments of whole 64-token blocks:
+//  * output role: the layer's outputs of a segment from its start weights;
+//  * chain role: the state chain of the first segment alone (no query side), whose
+//    end weights are the second segment's start;
+//  * map role: a later segment's affine map.  One mini-batch step is affine in W,
+//        W' = W - K^T diag(eta) (K W - V) = (I - K^T diag(eta) K) W + K^T diag(eta) V,
+//    so a segment maps its start weights to its end weights as W -> A W + B.  The
+//    map role runs the chain on the d x 2d state X = [A | B] from [I | 0], the
+//    columns of A seeing labels V = 0: each column of X is updated as a column of
+//    W is, so the per-warp code is the state chain with twice as many warps.
 #include <cuda.h>
 
 #include <type_traits>
@@ -28,9 +42,9 @@
 namespace ttt {
 namespace {
 
-template <int D>
+template <int D, bool MAP = false>
 struct B16Cfg {
-    static constexpr int NCW = D / 16;               // compute warps, 16 output columns each
+    static constexpr int NCW = (MAP ? 2 : 1) * D / 16;  // compute warps, 16 state columns each
     static constexpr int PW = NCW;                   // producer warp
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int NJ = D / 8, NK = D / 16;
@@ -63,8 +77,10 @@ struct Frag {
     float et[2][2];          // eta of tokens 8nt + 2t4 + i of the chunk
 };
 
+enum { kRoleOut = 0, kRoleChain = 1, kRoleMap = 2 };
+
 struct B16Params {
-    int H, T, causal;
+    int BH, H, T, causal;
     const float *eta;
     float eta_scalar;
     const float *W0;
@@ -72,21 +88,30 @@ struct B16Params {
     __nv_bfloat16 *z;
     float *W_out;
     int *status;
+    // units: CTA u serves chain u / nseg, segment s = seg0 + u % nseg; segment 0 is
+    // tokens [0, len0), segment s >= 1 is [len0 + (s-1) seg_len, len0 + s seg_len)
+    // cut at T (len0 and seg_len multiples of 64)
+    int len0, seg_len, nseg, seg0, nsplit;  // nsplit: segments per chain in the whole pass
+    float *Wst;   // [BH][nsplit-1][d][d] start weights of segments 1 .. nsplit-1
+    float *maps;  // [BH][nsplit-2][2][d][d] affine maps A, B of segments 1 .. nsplit-2
 };
 
-template <int D>
-__global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
-    ttt_linear_b16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                          const __grid_constant__ CUtensorMap tv, const B16Params p)
+// One unit (chain bh, segment seg) in role ROLE; the CTA has at least the role's
+// warps (extra warps leave after the barrier set-up).
+template <int D, int ROLE>
+__device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
+                                         const B16Params &p, const int bh, const int seg)
 {
-    using C = B16Cfg<D>;
+    constexpr bool MAP = ROLE == kRoleMap, QSIDE = ROLE == kRoleOut;
+    using C = B16Cfg<D, MAP>;
     constexpr int NJ = C::NJ, NK = C::NK, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x, T = p.T;
+    const int tb = seg == 0 ? 0 : p.len0 + (seg - 1) * p.seg_len;               // first token of the unit
+    const int T = max(0, min(p.T, seg == 0 ? p.len0 : tb + p.seg_len) - tb);   // tokens of the unit
     const int nblk = (T + 63) >> 6;
     const bool has_eta = p.eta != nullptr;
 
@@ -100,6 +125,7 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
         fence_barrier_init();
     }
     __syncthreads();
+    if (warp > C::PW) return;
 
     //  A pattern: blocks (rows 0-7, c), (rows 8-15, c), (rows 0-7, c+8), (rows 8-15, c+8)
     //  B pattern: blocks (rows 0-7, c), (rows 0-7, c+8), (rows 8-15, c), (rows 8-15, c+8)
@@ -118,14 +144,14 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
                 const uint32_t ed = base + C::ETA_OFF + s * 256;
 #pragma unroll
                 for (int i = lane; i < 64; i += 32)
-                    if (64 * L + i < T) cp_async_4(ed + 4 * i, p.eta + (size_t)bh * T + 64 * L + i);
+                    if (64 * L + i < T) cp_async_4(ed + 4 * i, p.eta + (size_t)bh * p.T + tb + 64 * L + i);
                 cp_async_arrive_noinc(full);
             }
             if (lane == 0) {
-                mbar_arrive_expect_tx(full, 3 * C::BLK);
-                tma_load_3d(st, &tq, full, 0, 64 * L, bh);
-                tma_load_3d(st + C::BLK, &tk, full, 0, 64 * L, bh);
-                tma_load_3d(st + 2 * C::BLK, &tv, full, 0, 64 * L, bh);
+                mbar_arrive_expect_tx(full, (QSIDE ? 3 : 2) * C::BLK);
+                if (QSIDE) tma_load_3d(st, tq, full, 0, tb + 64 * L, bh);
+                tma_load_3d(st + C::BLK, tk, full, 0, tb + 64 * L, bh);
+                tma_load_3d(st + 2 * C::BLK, tv, full, 0, tb + 64 * L, bh);
             }
             __syncwarp();
         }
@@ -135,10 +161,20 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
     }
 
     // ------------------------------------------------------------ compute warp
-    const int w = warp, col0 = 16 * w;
+    // MAP: warps 0 .. D/16-1 hold columns of A, the others columns of B
+    const int part = MAP ? warp / (D / 16) : 0;
+    const int w = MAP ? warp % (D / 16) : warp, col0 = 16 * w;
+    const bool zero_v = MAP && part == 0;  // the columns of A see labels V = 0
     float wacc[NJ][4];  // W^T[col0+g (+8)][8j+2t4 .. +1]
-    {
-        const float *W0 = p.W0 + (size_t)(bh / p.H) * p.w0_bstride + (size_t)(bh % p.H) * D * D;
+    if constexpr (MAP) {
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                wacc[j][i] = (part == 0 && 8 * j + 2 * t4 + (i & 1) == col0 + g + 8 * (i >> 1)) ? 1.f : 0.f;
+    } else {
+        const float *W0 = seg == 0 ? p.W0 + (size_t)(bh / p.H) * p.w0_bstride + (size_t)(bh % p.H) * D * D
+                                   : p.Wst + ((size_t)bh * (p.nsplit - 1) + seg - 1) * D * D;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
             const int r = 8 * j + 2 * t4;
@@ -177,9 +213,12 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
         for (int kk = 0; kk < NK; ++kk) {
             ldsm_x4(st + C::BLK + offB[kk], F.kB[kk][0], F.kB[kk][1], F.kB[kk][2], F.kB[kk][3]);
             ldsm_x4_t(st + C::BLK + offA[kk], F.kT[kk][0], F.kT[kk][1], F.kT[kk][2], F.kT[kk][3]);
-            ldsm_x4(st + offA[kk], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3]);
+            if (QSIDE) ldsm_x4(st + offA[kk], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3]);
         }
-        ldsm_x4_t(st + 2 * C::BLK + offV, F.vv[0][0], F.vv[0][1], F.vv[1][0], F.vv[1][1]);
+        if (zero_v)
+            F.vv[0][0] = F.vv[0][1] = F.vv[1][0] = F.vv[1][1] = 0u;
+        else
+            ldsm_x4_t(st + 2 * C::BLK + offV, F.vv[0][0], F.vv[0][1], F.vv[1][0], F.vv[1][1]);
         if (has_eta) {
             const float *e = reinterpret_cast<const float *>(gbase + C::ETA_OFF + (L & (NB - 1)) * 256) +
                              16 * Q + 2 * t4;
@@ -197,7 +236,10 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) vis[nt][i] = !p.causal || (8 * nt + 2 * t4 + (i & 1)) <= g + 8 * (i >> 1);
-    __nv_bfloat16 *const zlane = p.z + (size_t)bh * T * D + (size_t)g * D + col0 + 2 * t4;
+    __nv_bfloat16 *const zlane =
+        QSIDE ? p.z + ((size_t)bh * p.T + tb) * D + (size_t)g * D + col0 + 2 * t4 : nullptr;
+
+    bool next_ready = false;  // the next block has landed (tested in chunk 2 of a block)
 
     // one chunk (L, Q) on fragments F; fetches chunk (L, Q+1) or (L+1, 0) into Fn.
     // FULL: the chunk has 16 tokens (no bounds masks).  Returns false when there
@@ -207,16 +249,31 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
         constexpr bool FULL = decltype(fullc)::value;
         const int t0 = 64 * L + 16 * Q;
         const int c = FULL ? 16 : T - t0;
-        float e[2][2][4] = {}, sc[2][4] = {}, zc[2][4] = {};
+        // E^T = W^T K^T - V^T.  ONE: a single accumulator per n-tile that starts at
+        // -V^T (fewer instructions, a deeper product chain: the map role has a second
+        // warp on each SM sub-partition to hide it); otherwise two interleaved
+        // accumulators with V subtracted afterwards (shorter chain for the lone warp)
+        constexpr bool ONE = true;
+        float e[2][2][4] = {};
+        [[maybe_unused]] float sc[2][4] = {}, zc[2][4] = {};
+        if constexpr (ONE) {
 #pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {  // E^T = W^T K^T
-            mma_bf16(e[kk & 1][0], wb[4 * kk], wb[4 * kk + 1], wb[4 * kk + 2], wb[4 * kk + 3], F.kB[kk][0],
-                     F.kB[kk][1]);
-            mma_bf16(e[kk & 1][1], wb[4 * kk], wb[4 * kk + 1], wb[4 * kk + 2], wb[4 * kk + 3], F.kB[kk][2],
-                     F.kB[kk][3]);
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t vw = F.vv[nt][i >> 1];
+                    e[0][nt][i] = -((i & 1) ? bf16_hi(vw) : bf16_lo(vw));
+                }
         }
 #pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {  // S = Q K^T (off the serial chain)
+        for (int kk = 0; kk < NK; ++kk) {
+            mma_bf16(e[ONE ? 0 : kk & 1][0], wb[4 * kk], wb[4 * kk + 1], wb[4 * kk + 2], wb[4 * kk + 3],
+                     F.kB[kk][0], F.kB[kk][1]);
+            mma_bf16(e[ONE ? 0 : kk & 1][1], wb[4 * kk], wb[4 * kk + 1], wb[4 * kk + 2], wb[4 * kk + 3],
+                     F.kB[kk][2], F.kB[kk][3]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < NK && QSIDE; ++kk) {  // S = Q K^T (off the serial chain)
             mma_bf16(sc[0], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], F.kB[kk][0], F.kB[kk][1]);
             mma_bf16(sc[1], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], F.kB[kk][2], F.kB[kk][3]);
         }
@@ -226,11 +283,15 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
         const bool more = t0 + 16 < T;
         if constexpr (Q < 3) {
             load(std::integral_constant<int, Q + 1>{}, Fn, L);
+            // test for the next block a chunk ahead (non-blocking): the result is
+            // read in the block's last chunk, so the test's latency is hidden
+            if constexpr (Q == 2)
+                next_ready = mbar_test_wait(blk_full + 8 * ((L + 1) & (NB - 1)), ((L + 1) / NB) & 1);
         } else if (more) {
             __syncwarp();
             if (lane == 0) mbar_arrive(blk_empty + 8 * (L & (NB - 1)));
-            if (!mbar_wait(blk_full + 8 * ((L + 1) & (NB - 1)), ((L + 1) / NB) & 1, p.status,
-                           kSiteConsumerFull))
+            if (!next_ready && !mbar_wait(blk_full + 8 * ((L + 1) & (NB - 1)), ((L + 1) / NB) & 1, p.status,
+                                          kSiteConsumerFull))
                 return false;
             load(std::integral_constant<int, 0>{}, Fn, L + 1);
         }
@@ -240,9 +301,11 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint32_t vw = F.vv[nt][i >> 1];
-                const float vval = (i & 1) ? bf16_hi(vw) : bf16_lo(vw);
-                const float r = e[0][nt][i] + e[1][nt][i] - vval;
+                float r = e[0][nt][i];
+                if constexpr (!ONE) {
+                    const uint32_t vw = F.vv[nt][i >> 1];
+                    r += e[1][nt][i] - ((i & 1) ? bf16_hi(vw) : bf16_lo(vw));
+                }
                 ne[nt][i] = (FULL || (8 * nt + 2 * t4 + (i & 1)) < c) ? -F.et[nt][i & 1] * r : 0.f;
             }
         const uint32_t ea0 = pack_bf16(ne[0][0], ne[0][1]), ea1 = pack_bf16(ne[0][2], ne[0][3]);
@@ -252,55 +315,67 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
             mma_bf16(wacc[2 * j2], ea0, ea1, ea2, ea3, F.kT[j2][0], F.kT[j2][1]);
             mma_bf16(wacc[2 * j2 + 1], ea0, ea1, ea2, ea3, F.kT[j2][2], F.kT[j2][3]);
         }
-        // Z = Q W + (mask .* S)(-Et), masked scores as an A fragment from registers
-#pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {
-            mma_bf16(zc[0], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk], wb[4 * kk + 2]);
-            mma_bf16(zc[1], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk + 1],
-                     wb[4 * kk + 3]);
-        }
-        float sm[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool keep = vis[nt][i] && (FULL || (8 * nt + 2 * t4 + (i & 1)) < c);
-                sm[nt][i] = keep ? sc[nt][i] : 0.f;
+        if constexpr (QSIDE) {
+            // Z = Q W + (mask .* S)(-Et), masked scores as an A fragment from registers
+    #pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                mma_bf16(zc[0], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk], wb[4 * kk + 2]);
+                mma_bf16(zc[1], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk + 1],
+                         wb[4 * kk + 3]);
             }
-        mma_bf16(zc[0], pack_bf16(sm[0][0], sm[0][1]), pack_bf16(sm[0][2], sm[0][3]),
-                 pack_bf16(sm[1][0], sm[1][1]), pack_bf16(sm[1][2], sm[1][3]), ea0, ea2);
-        mma_bf16(zc[1], pack_bf16(sm[0][0], sm[0][1]), pack_bf16(sm[0][2], sm[0][3]),
-                 pack_bf16(sm[1][0], sm[1][1]), pack_bf16(sm[1][2], sm[1][3]), ea1, ea3);
+            float sm[2][4];
+    #pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const bool keep = vis[nt][i] && (FULL || (8 * nt + 2 * t4 + (i & 1)) < c);
+                    sm[nt][i] = keep ? sc[nt][i] : 0.f;
+                }
+            mma_bf16(zc[0], pack_bf16(sm[0][0], sm[0][1]), pack_bf16(sm[0][2], sm[0][3]),
+                     pack_bf16(sm[1][0], sm[1][1]), pack_bf16(sm[1][2], sm[1][3]), ea0, ea2);
+            mma_bf16(zc[1], pack_bf16(sm[0][0], sm[0][1]), pack_bf16(sm[0][2], sm[0][3]),
+                     pack_bf16(sm[1][0], sm[1][1]), pack_bf16(sm[1][2], sm[1][3]), ea1, ea3);
+        }
         convert();
-        __nv_bfloat16 *zb = zlane + (size_t)t0 * D;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            if (FULL || g < c)
-                *reinterpret_cast<uint32_t *>(zb + 8 * hh) = pack_bf16(zc[hh][0], zc[hh][1]);
-            if (FULL || g + 8 < c)
-                *reinterpret_cast<uint32_t *>(zb + 8 * D + 8 * hh) = pack_bf16(zc[hh][2], zc[hh][3]);
+        if constexpr (QSIDE) {
+            __nv_bfloat16 *zb = zlane + (size_t)t0 * D;
+    #pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                if (FULL || g < c)
+                    *reinterpret_cast<uint32_t *>(zb + 8 * hh) = pack_bf16(zc[hh][0], zc[hh][1]);
+                if (FULL || g + 8 < c)
+                    *reinterpret_cast<uint32_t *>(zb + 8 * D + 8 * hh) = pack_bf16(zc[hh][2], zc[hh][3]);
+            }
         }
         return more;
     };
-    auto step = [&](auto qc, Frag<D> &F, Frag<D> &Fn, int L) -> bool {
-        if (64 * L + 16 * decltype(qc)::value + 16 <= T)
-            return chunk(qc, std::true_type{}, F, Fn, L);
-        return chunk(qc, std::false_type{}, F, Fn, L);
+    // the four chunks of block L; FULL: the block holds 64 tokens (no bounds masks)
+    auto block = [&](auto fullc, Frag<D> &FA, Frag<D> &FB, int L) -> bool {
+        using I0 = std::integral_constant<int, 0>;
+        using I1 = std::integral_constant<int, 1>;
+        using I2 = std::integral_constant<int, 2>;
+        using I3 = std::integral_constant<int, 3>;
+        return chunk(I0{}, fullc, FA, FB, L) && chunk(I1{}, fullc, FB, FA, L) && chunk(I2{}, fullc, FA, FB, L) &&
+               chunk(I3{}, fullc, FB, FA, L);
     };
 
     if (nblk > 0 && mbar_wait(blk_full, 0, p.status, kSiteConsumerFull)) {
         Frag<D> FA, FB;
         load(std::integral_constant<int, 0>{}, FA, 0);
         for (int L = 0;; ++L) {  // two fragment sets alternate: no register copies
-            if (!step(std::integral_constant<int, 0>{}, FA, FB, L)) break;
-            if (!step(std::integral_constant<int, 1>{}, FB, FA, L)) break;
-            if (!step(std::integral_constant<int, 2>{}, FA, FB, L)) break;
-            if (!step(std::integral_constant<int, 3>{}, FB, FA, L)) break;
+            const bool ok = 64 * L + 64 <= T ? block(std::true_type{}, FA, FB, L) : block(std::false_type{}, FA, FB, L);
+            if (!ok) break;
         }
     }
 
-    if (p.W_out) {
-        float *Wo = p.W_out + (size_t)bh * D * D;
+    float *Wo = nullptr;
+    if (ROLE == kRoleMap)  // map of segment seg (1 .. nsplit-2)
+        Wo = p.maps + (((size_t)bh * (p.nsplit - 2) + seg - 1) * 2 + part) * D * D;
+    else if (ROLE == kRoleChain)  // end of segment seg = start of segment seg + 1
+        Wo = p.Wst + ((size_t)bh * (p.nsplit - 1) + seg) * D * D;
+    else if (p.W_out && seg == p.nsplit - 1)
+        Wo = p.W_out + (size_t)bh * D * D;
+    if (Wo) {
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
             const int r = 8 * j + 2 * t4;
@@ -312,16 +387,45 @@ __global__ void __launch_bounds__(B16Cfg<D>::THREADS, 1)
     }
 }
 
+// Output units: CTA u serves chain u / nseg, segment seg0 + u % nseg.
 template <int D>
-int launch_b16_t(const LinearArgs &a)
+__global__ void __launch_bounds__(B16Cfg<D, false>::THREADS, 1)
+    ttt_linear_b16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                          const __grid_constant__ CUtensorMap tv, const B16Params p)
 {
-    using C = B16Cfg<D>;
-    CUtensorMap maps[3];
-    if (!encode_qkv(maps, a.q, a.k, a.v, a.B * a.H, a.T, a.d, 64)) return -4;
-    auto kern = ttt_linear_b16_kernel<D>;
+    b16_unit<D, kRoleOut>(&tq, &tk, &tv, p, blockIdx.x / p.nseg, p.seg0 + blockIdx.x % p.nseg);
+}
+
+// The work before a split run's later segments: CTAs 0 .. BH-1 run the state chain
+// of each chain's first segment, the others the affine maps of segments
+// 1 .. nsplit-2 (chain (u - BH) / (nsplit - 2)).
+template <int D>
+__global__ void __launch_bounds__(B16Cfg<D, true>::THREADS, 1)
+    ttt_linear_b16_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                               const __grid_constant__ CUtensorMap tv, const B16Params p)
+{
+    const int u = blockIdx.x;
+    if (u < p.BH)
+        b16_unit<D, kRoleChain>(&tq, &tk, &tv, p, u, 0);
+    else
+        b16_unit<D, kRoleMap>(&tq, &tk, &tv, p, (u - p.BH) / (p.nsplit - 2), 1 + (u - p.BH) % (p.nsplit - 2));
+}
+
+template <int D, bool PREP>
+int launch_b16_t(const LinearArgs &a, const B16Params &p, int units, const CUtensorMap *maps)
+{
+    using C = B16Cfg<D, PREP>;
+    auto kern = PREP ? ttt_linear_b16_prep_kernel<D> : ttt_linear_b16_kernel<D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return -4;
+    kern<<<units, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+B16Params b16_params(const LinearArgs &a)
+{
     B16Params p;
+    p.BH = a.B * a.H;
     p.H = a.H;
     p.T = a.T;
     p.causal = a.causal;
@@ -332,20 +436,49 @@ int launch_b16_t(const LinearArgs &a)
     p.z = static_cast<__nv_bfloat16 *>(a.z);
     p.W_out = a.W_out;
     p.status = a.status;
-    kern<<<a.B * a.H, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+    p.len0 = p.seg_len = ((a.T + 63) / 64) * 64;  // one unit per chain: the whole sequence
+    p.nseg = 1;
+    p.seg0 = 0;
+    p.nsplit = 1;
+    p.Wst = nullptr;
+    p.maps = nullptr;
+    return p;
+}
+
+template <bool PREP>
+int launch_b16_d(const LinearArgs &a, const B16Params &p, int units, const CUtensorMap *maps)
+{
+    switch (a.d) {
+    case 16: return launch_b16_t<16, PREP>(a, p, units, maps);
+    case 32: return launch_b16_t<32, PREP>(a, p, units, maps);
+    case 64: return launch_b16_t<64, PREP>(a, p, units, maps);
+    default: return -2;
+    }
 }
 
 }  // namespace
 
 int launch_linear_b16(const LinearArgs &a)
 {
-    switch (a.d) {
-    case 16: return launch_b16_t<16>(a);
-    case 32: return launch_b16_t<32>(a);
-    case 64: return launch_b16_t<64>(a);
-    default: return launch_linear_bf16(a);
-    }
+    if (a.d > 64) return launch_linear_bf16(a);
+    CUtensorMap maps[3];
+    if (!encode_qkv(maps, a.q, a.k, a.v, a.B * a.H, a.T, a.d, 64)) return -4;
+    return launch_b16_d<false>(a, b16_params(a), a.B * a.H, maps);
+}
+
+int launch_linear_b16_segments(const LinearArgs &a, int nsplit, int len0, int seg_len, int seg0, int nseg,
+                               bool prep, float *Wst, float *mapbuf, const CUtensorMap *maps)
+{
+    B16Params p = b16_params(a);
+    p.len0 = len0;
+    p.seg_len = seg_len;
+    p.nseg = nseg;
+    p.seg0 = seg0;
+    p.nsplit = nsplit;
+    p.Wst = Wst;
+    p.maps = mapbuf;
+    if (prep) return launch_b16_d<true>(a, p, a.B * a.H * (nsplit - 1), maps);
+    return launch_b16_d<false>(a, p, a.B * a.H * nseg, maps);
 }
 
 }  // namespace ttt

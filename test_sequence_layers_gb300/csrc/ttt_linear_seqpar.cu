@@ -1,0 +1,196 @@
+// ttt_linear_seqpar.cu -- sequence-parallel TTT-Linear forward (mini-batch b = 16,
+// bf16 operands, fp32 state, d in {16, 32, 64}) for workloads with fewer
+// (batch, head) chains than SMs, where one CTA per chain leaves most of the GPU
+// idle and the serial mini-batch chain of a long sequence sets the time.
+//
+// One mini-batch step is affine in the weights:
+//     W' = W - K^T diag(eta) (K W - V) = (I - K^T diag(eta) K) W + K^T diag(eta) V
+// ("Learning to (Learn at Test Time)" walkthrough, section 1.2.2, mini-batch
+// gradient descent, formula 6, written out for the linear inner model of section
+// 2.2.1).  A run of steps is therefore one affine map W -> A W + B, and maps
+// compose, so a chain can be cut into segments whose maps are found in parallel
+// and chained by a short scan (the block-parallel remark of "Fast weights 与 TTT
+// layers", on mini-batch versus exact sequential updates, made exact here: the
+// maps reproduce the sequential mini-batch rule, not an approximation of it).
+//
+// Schedule, for nsplit segments per chain (segment 0 longer than the others):
+//   caller's stream : outputs of segment 0 from W0 (ttt_linear_b16_kernel)
+//   side stream     : the state chain of segment 0 alone (no query side: its end
+//                     weights are segment 1's start) and, in the same launch, the
+//                     affine maps of segments 1 .. nsplit-2
+//                     -> scan: start weights of segments 2 .. nsplit-1 (fp32)
+//                     -> outputs of segments 1 .. nsplit-1 from their start weights
+// The side stream forks from and joins back into the caller's stream with events.
+// Segment 0's output pass runs beside the side stream's first launch, so the
+// segment lengths balance segment 0's output pass against that launch plus one
+// output pass of a later segment.
+//
+// Scratch (caller-provided workspace): maps [BH][nsplit-2][2][d][d] fp32, then
+// start weights [BH][nsplit-1][d][d] fp32.
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ttt_device.cuh"
+#include "ttt_internal.h"
+
+namespace ttt {
+namespace {
+
+// Start weights of segments 2 .. nsplit-1 of one chain: W_{s+1} = A_s W_s + B_s
+// in fp32, from W_1 (written by the state chain of segment 0).  One CTA of 256
+// threads per chain.
+template <int D>
+__global__ void __launch_bounds__(256) ttt_linear_scan_kernel(const float *__restrict__ maps,
+                                                              float *__restrict__ Wst, int nsplit)
+{
+    constexpr int TPR = 256 / D;      // threads per output row
+    constexpr int PER = D / TPR;      // outputs per thread
+    __shared__ float sW[D * D], sA[D * D];
+    const int bh = blockIdx.x, t = threadIdx.x;
+    const int r = t / TPR, c0 = t % TPR;
+    float *W = Wst + (size_t)bh * (nsplit - 1) * D * D;
+    for (int i = t; i < D * D; i += 256) sW[i] = W[i];
+    for (int s = 1; s + 1 < nsplit; ++s) {
+        const float *A = maps + ((size_t)bh * (nsplit - 2) + s - 1) * 2 * D * D;
+        const float *B = A + D * D;
+        for (int i = t; i < D * D; i += 256) sA[i] = A[i];
+        __syncthreads();
+        float acc[PER];
+#pragma unroll
+        for (int m = 0; m < PER; ++m) acc[m] = B[(size_t)r * D + c0 + TPR * m];
+#pragma unroll 8
+        for (int k = 0; k < D; ++k) {
+            const float a = sA[r * D + k];
+#pragma unroll
+            for (int m = 0; m < PER; ++m) acc[m] = fmaf(a, sW[k * D + c0 + TPR * m], acc[m]);
+        }
+        __syncthreads();  // every read of sW and sA is done
+        float *out = W + (size_t)s * D * D;
+#pragma unroll
+        for (int m = 0; m < PER; ++m) {
+            sW[r * D + c0 + TPR * m] = acc[m];
+            out[(size_t)r * D + c0 + TPR * m] = acc[m];
+        }
+    }
+}
+
+int launch_scan(const LinearArgs &a, int nsplit, const float *maps, float *Wst, cudaStream_t st)
+{
+    const int BH = a.B * a.H;
+    switch (a.d) {
+    case 16: ttt_linear_scan_kernel<16><<<BH, 256, 0, st>>>(maps, Wst, nsplit); break;
+    case 32: ttt_linear_scan_kernel<32><<<BH, 256, 0, st>>>(maps, Wst, nsplit); break;
+    case 64: ttt_linear_scan_kernel<64><<<BH, 256, 0, st>>>(maps, Wst, nsplit); break;
+    default: return -2;
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+// Per device: the side stream and the fork / join events (created on first use).
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+// Per-chunk times of the two preparing roles relative to the output role (b = 16,
+// d = 64, one CTA per SM), used to balance segment lengths: the state chain alone
+// and a map (the chain on twice the columns).
+constexpr double kChainToOutput = 0.55;
+constexpr double kMapToOutput = 0.95;
+
+// Modelled time (in output-chunk units) of a split with segment 0 of len0 tokens and
+// nsplit - 1 later segments of len1 tokens.
+double split_time(int len0, int len1, int nsplit)
+{
+    const double c0 = len0 / 16.0, c1 = len1 / 16.0;
+    double prep = c0 * kChainToOutput;
+    if (nsplit > 2 && c1 * kMapToOutput > prep) prep = c1 * kMapToOutput;
+    const double later = prep + c1;
+    return c0 > later ? c0 : later;
+}
+
+}  // namespace
+
+bool seqpar_plan(const LinearArgs &a, SeqparPlan &pl)
+{
+    pl = SeqparPlan{};
+    if (a.b != 16 || (a.d != 16 && a.d != 32 && a.d != 64)) return false;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    const long long BH = (long long)a.B * a.H;
+    const int T = a.T;
+    // segment 0's output CTAs and the side stream's first launch (BH chain CTAs and
+    // BH (nsplit - 2) map CTAs) share the GPU: nsplit BH <= SMs
+    int pmax = (int)(nsm / (BH > 0 ? BH : 1));
+    if (pmax > 8) pmax = 8;
+    double best = T / 16.0 * 0.9;  // a split must save at least a tenth
+    for (int P = 2; P <= pmax; ++P) {
+        for (int len0 = 64; len0 < T; len0 += 64) {
+            const int rest = T - len0;
+            const int len1 = ((rest + (P - 1) - 1) / (P - 1) + 63) / 64 * 64;
+            if (len1 < 256) continue;  // segments shorter than four blocks do not pay
+            const int nseg = 1 + (rest + len1 - 1) / len1;
+            const double t = split_time(len0, len1, nseg);
+            if (t < best) {
+                best = t;
+                pl.nsplit = nseg;
+                pl.len0 = len0;
+                pl.seg_len = len1;
+            }
+        }
+    }
+    if (pl.nsplit < 2) return false;
+    const size_t dd = (size_t)a.d * a.d * sizeof(float);
+    pl.map_bytes = (size_t)BH * (pl.nsplit - 2) * 2 * dd;
+    pl.wst_bytes = (size_t)BH * (pl.nsplit - 1) * dd;
+    return true;
+}
+
+size_t seqpar_workspace_bytes(const SeqparPlan &pl)
+{
+    return pl.nsplit < 2 ? 0 : ((pl.map_bytes + 255) / 256) * 256 + pl.wst_bytes;
+}
+
+int launch_linear_seqpar(const LinearArgs &a, const SeqparPlan &pl, void *ws)
+{
+    float *maps = static_cast<float *>(ws);
+    float *Wst = reinterpret_cast<float *>(static_cast<char *>(ws) + ((pl.map_bytes + 255) / 256) * 256);
+    CUtensorMap tm[3];
+    if (!encode_qkv(tm, a.q, a.k, a.v, a.B * a.H, a.T, a.d, 64)) return -4;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -4;
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream &S = g_side[dev];
+    if (!S.s) {
+        if (cudaStreamCreateWithFlags(&S.s, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&S.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&S.join, cudaEventDisableTiming) != cudaSuccess)
+            return -4;
+    }
+    if (cudaEventRecord(S.fork, a.stream) != cudaSuccess || cudaStreamWaitEvent(S.s, S.fork, 0) != cudaSuccess)
+        return -4;
+    // caller's stream: segment 0 from W0
+    int rc = launch_linear_b16_segments(a, pl.nsplit, pl.len0, pl.seg_len, 0, 1, false, Wst, maps, tm);
+    // side stream: segment 0's state chain (+ maps of segments 1 .. nsplit-2) -> scan -> segments 1 ..
+    LinearArgs b = a;
+    b.stream = S.s;
+    if (rc == 0) rc = launch_linear_b16_segments(b, pl.nsplit, pl.len0, pl.seg_len, 0, 1, true, Wst, maps, tm);
+    if (rc == 0 && pl.nsplit > 2) rc = launch_scan(b, pl.nsplit, maps, Wst, S.s);
+    if (rc == 0)
+        rc = launch_linear_b16_segments(b, pl.nsplit, pl.len0, pl.seg_len, 1, pl.nsplit - 1, false, Wst, maps, tm);
+    // join (also after a failed launch, so the caller's stream never runs ahead of
+    // work already queued on the side stream)
+    if (cudaEventRecord(S.join, S.s) != cudaSuccess || cudaStreamWaitEvent(a.stream, S.join, 0) != cudaSuccess)
+        return -4;
+    return rc;
+}
+
+}  // namespace ttt

@@ -102,3 +102,17 @@ def test_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 1, 4, 16, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         abi.ttt_linear_fwd(q, q, q, torch.zeros(1, 16, 16), 4)
+
+
+def test_seqpar_rejects_bad_arguments_and_reports_no_workspace_without_gpu(L):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    assert L.ttt_linear_fwd_seqpar(None, None, None, None, None, 1.0, None, None, None, None, 0,
+                                   None) == -1
+    for bad in (_lin(B=0), _lin(T=-1), _lin(mini_batch=0), _lin(causal=2)):
+        assert L.ttt_linear_fwd_seqpar(ctypes.byref(bad), vp(FAKE), vp(FAKE), vp(FAKE), None, 1.0,
+                                       vp(FAKE), vp(FAKE), None, None, 0, None) == -1
+    assert L.ttt_linear_fwd_seqpar(ctypes.byref(_lin(d=48)), vp(FAKE), vp(FAKE), vp(FAKE), None,
+                                   1.0, vp(FAKE), vp(FAKE), None, None, 0, None) == -2
+    assert L.ttt_linear_seqpar_workspace(None) == 0
+    # no device visible: the call would not split, so no workspace is needed
+    assert L.ttt_linear_seqpar_workspace(ctypes.byref(_lin(T=4096))) == 0
