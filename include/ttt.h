@@ -59,7 +59,8 @@ typedef enum {
     TTT_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. d not in the set)   */
     TTT_ERR_ALIGN = -3,        /* pointer misaligned for the bulk-copy engine         */
     TTT_ERR_LAUNCH = -4,       /* CUDA reported an error at or before launch          */
-    TTT_ERR_TIMEOUT = -5       /* a kernel wait ran out (reported by ttt_sync_status) */
+    TTT_ERR_TIMEOUT = -5,      /* a kernel wait ran out (reported by ttt_sync_status) */
+    TTT_ERR_SCRATCH = -6       /* ttt_linear_fwd_seqpar_noalloc: more than its fixed scratch */
 } ttt_status;
 
 typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
@@ -123,6 +124,38 @@ ttt_status ttt_linear_fwd_seqpar(const ttt_linear_desc *desc,
                                  const float *eta, float eta_scalar,
                                  const float *W0, void *z, float *W_out,
                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * ttt_linear_fwd_seqpar_noalloc: the sequence-parallel forward without a caller
+ * workspace and without any device allocation.  (The pages have no counterpart:
+ * this is a deployment variant of ttt_linear_fwd_seqpar.)
+ *
+ * For callers that cannot allocate device memory while they run: a serving
+ * process that has handed the free device memory to its own pool or cache has none
+ * left for cudaMalloc, cudaFree may synchronise the device in the middle of its
+ * pipeline, and a plugin inside another framework may have no access to that
+ * framework's allocator.  The scratch is instead a fixed array of 4 MiB inside the
+ * library, held on every device that loads it until the process exits.
+ *
+ * Same arguments and results as ttt_linear_fwd_seqpar (up to floating-point
+ * rounding), all work on `stream` alone: one launch for the first segment's state
+ * chain and the later segments' affine maps, the scan, then every segment's
+ * outputs in one launch (segments of equal length).  Problems that do not split
+ * run ttt_linear_fwd.  A split needs 4 (BH (P-1) + 2 BH (P-2)) d^2 bytes for P
+ * segments of BH = B*H chains (e.g. d = 64, two segments: up to 256 chains);
+ * larger problems return TTT_ERR_SCRATCH before any work is queued.  W_out must
+ * not overlap W0 (TTT_ERR_ARG).
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call uses the same array: calls whose work overlaps on the GPU
+ * (other streams, other host threads) race on it and must be ordered by the
+ * caller.  Nothing in the array needs clearing between calls.
+ */
+ttt_status ttt_linear_fwd_seqpar_noalloc(const ttt_linear_desc *desc,
+                                         const void *q, const void *k, const void *v,
+                                         const float *eta, float eta_scalar,
+                                         const float *W0, void *z, float *W_out, void *stream);
 
 /* TTT-MLP problem description. */
 typedef struct {

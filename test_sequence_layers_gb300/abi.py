@@ -17,10 +17,11 @@ LIB_PATH = os.path.join(_HERE, "libttt.so")
 
 TTT_F32, TTT_BF16 = 0, 1
 STATUS = {0: "TTT_OK", -1: "TTT_ERR_ARG", -2: "TTT_ERR_UNSUPPORTED", -3: "TTT_ERR_ALIGN",
-          -4: "TTT_ERR_LAUNCH", -5: "TTT_ERR_TIMEOUT"}
+          -4: "TTT_ERR_LAUNCH", -5: "TTT_ERR_TIMEOUT", -6: "TTT_ERR_SCRATCH"}
 
 # every symbol include/ttt.h declares
 EXPORTS = ("ttt_linear_fwd", "ttt_linear_seqpar_workspace", "ttt_linear_fwd_seqpar",
+           "ttt_linear_fwd_seqpar_noalloc",
            "ttt_mlp_fwd", "ttt_sync_status", "ttt_status_str", "ttt_launch_count")
 
 
@@ -62,6 +63,9 @@ def lib():
         L.ttt_linear_fwd_seqpar.argtypes = [ctypes.POINTER(LinearDesc), vp, vp, vp, fp, f, fp, vp, fp,
                                             vp, ctypes.c_size_t, vp]
         L.ttt_linear_fwd_seqpar.restype = ctypes.c_int
+        L.ttt_linear_fwd_seqpar_noalloc.argtypes = [ctypes.POINTER(LinearDesc), vp, vp, vp, fp, f, fp, vp,
+                                                    fp, vp]
+        L.ttt_linear_fwd_seqpar_noalloc.restype = ctypes.c_int
         L.ttt_mlp_fwd.argtypes = [ctypes.POINTER(MlpDesc), vp, vp, vp, fp, f, fp, fp, fp, fp,
                                   vp, fp, fp, fp, fp, vp]
         L.ttt_mlp_fwd.restype = ctypes.c_int
@@ -174,6 +178,32 @@ def ttt_linear_fwd_seqpar(q, k, v, W0, mini_batch, causal=True, eta=None, eta_sc
                                      _ptr(workspace), nbytes, _stream(stream))
     if rc != 0:
         raise TTTError("ttt_linear_fwd_seqpar", rc)
+    return z, W_out
+
+
+def ttt_linear_fwd_seqpar_noalloc(q, k, v, W0, z, W_out, mini_batch, causal=True, eta=None,
+                                  eta_scalar=1.0, stream=None):
+    """The sequence-parallel forward on the library's fixed scratch (no workspace,
+    no allocation inside the call): z and W_out are the caller's output tensors."""
+    io = _check_tokens(q, k, v)
+    B, H, T, d = q.shape
+    W0 = _f32(W0, "W0")
+    eta = _f32(eta, "eta")
+    W_out = _f32(W_out, "W_out")
+    if W0.shape == (H, d, d):
+        w0s = 0
+    elif W0.shape == (B, H, d, d):
+        w0s = H * d * d
+    else:
+        raise ValueError("W0 must be [H,d,d] or [B,H,d,d]")
+    if z.shape != q.shape or z.dtype != q.dtype or not z.is_contiguous():
+        raise ValueError("z must be a contiguous tensor shaped and typed like q")
+    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, w0s)
+    rc = lib().ttt_linear_fwd_seqpar_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(eta),
+                                             float(eta_scalar), _ptr(W0), _ptr(z), _ptr(W_out),
+                                             _stream(stream))
+    if rc != 0:
+        raise TTTError("ttt_linear_fwd_seqpar_noalloc", rc)
     return z, W_out
 
 

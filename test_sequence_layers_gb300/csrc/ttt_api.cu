@@ -15,6 +15,13 @@
 // device: every device that loads the library has its own copy).
 __device__ int g_ttt_status;
 
+// Fixed scratch of ttt_linear_fwd_seqpar_noalloc (affine maps and segment start
+// weights of a split run).  Every device that loads the library holds it until the
+// process exits.  Every byte a call reads from it is written earlier by the same
+// call, so it never needs clearing.
+constexpr size_t kNoAllocScratchBytes = 4u << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 std::atomic<unsigned long long> g_launches{0};
@@ -51,6 +58,24 @@ int *status_word()
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_ttt_status) != cudaSuccess) return nullptr;
         addr[dev] = static_cast<int *>(p);
+    }
+    return addr[dev];
+}
+
+// Device address of this device's fixed scratch array.  The array's name in host
+// code only stands for the symbol: the address comes from cudaGetSymbolAddress,
+// looked up once per device with that device current (nullptr on failure).
+void *noalloc_scratch()
+{
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
     }
     return addr[dev];
 }
@@ -275,6 +300,30 @@ ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc, const void *q, const void *k, c
     return code(rc);
 }
 
+ttt_status ttt_linear_fwd_seqpar_noalloc(const ttt_linear_desc *desc, const void *q, const void *k,
+                                         const void *v, const float *eta, float eta_scalar, const float *W0,
+                                         void *z, float *W_out, void *stream)
+{
+    ttt::LinearArgs a;
+    const ttt_status st = linear_args(desc, q, k, v, eta, eta_scalar, W0, z, W_out, stream, a);
+    if (st != TTT_OK) return st;
+    ttt::SeqparPlan pl;
+    if (desc->io_dtype != TTT_BF16 || !ttt::seqpar_plan_serial(a, pl)) {
+        const int rc = launch_linear(a, desc->io_dtype);  // not split: needs no scratch
+        if (rc == 0) g_launches.fetch_add(1, std::memory_order_relaxed);
+        return code(rc);
+    }
+    if (ttt::seqpar_workspace_bytes(pl) > kNoAllocScratchBytes) return TTT_ERR_SCRATCH;
+    const size_t dd = sizeof(float) * desc->d * desc->d;
+    const size_t nW0 = desc->w0_batch_stride ? dd * desc->B * desc->H : dd * desc->H;
+    if (W_out && overlaps(W_out, dd * desc->B * desc->H, W0, nW0)) return TTT_ERR_ARG;
+    void *ws = noalloc_scratch();
+    if (!ws) return TTT_ERR_LAUNCH;
+    const int rc = ttt::launch_linear_seqpar_serial(a, pl, ws);
+    if (rc == 0) g_launches.fetch_add(pl.nsplit > 2 ? 3 : 2, std::memory_order_relaxed);
+    return code(rc);
+}
+
 ttt_status ttt_sync_status(void *stream)
 {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTT_ERR_LAUNCH;
@@ -297,6 +346,7 @@ const char *ttt_status_str(ttt_status s)
     case TTT_ERR_ALIGN: return "pointer misaligned (q, k, v, z need 16 bytes; fp32 arrays 4)";
     case TTT_ERR_LAUNCH: return "CUDA error at launch";
     case TTT_ERR_TIMEOUT: return "kernel wait timed out";
+    case TTT_ERR_SCRATCH: return "the split run needs more than the library's fixed 4 MiB scratch";
     }
     return "unknown status";
 }

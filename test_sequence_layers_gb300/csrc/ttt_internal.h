@@ -75,6 +75,10 @@ size_t seqpar_workspace_bytes(const SeqparPlan &pl);
 // Enqueues the split forward on a.stream (forks a side stream and joins it back);
 // ws: at least seqpar_workspace_bytes(pl) bytes of device memory, 256-byte aligned.
 int launch_linear_seqpar(const LinearArgs &a, const SeqparPlan &pl, void *ws);
+// The same split enqueued on a.stream alone: the preparing launch, the scan, then
+// every segment's outputs in one launch (equal segments; seqpar_plan_serial).
+bool seqpar_plan_serial(const LinearArgs &a, SeqparPlan &pl);
+int launch_linear_seqpar_serial(const LinearArgs &a, const SeqparPlan &pl, void *ws);
 
 // Largest d*m the fp32 MLP path holds on chip.
 bool mlp_f32_fits(int d, int m);

@@ -193,4 +193,53 @@ int launch_linear_seqpar(const LinearArgs &a, const SeqparPlan &pl, void *ws)
     return rc;
 }
 
+// Plan for a split run on one stream (no side stream): the preparing launch first,
+// then the scan, then the outputs of all segments in one launch.  Segments of
+// equal length; time = preparing pass + one segment's output pass.
+bool seqpar_plan_serial(const LinearArgs &a, SeqparPlan &pl)
+{
+    pl = SeqparPlan{};
+    if (a.b != 16 || (a.d != 16 && a.d != 32 && a.d != 64)) return false;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    const long long BH = (long long)a.B * a.H;
+    const int T = a.T;
+    int pmax = (int)(nsm / (BH > 0 ? BH : 1));  // the output launch: nsplit BH CTAs
+    if (pmax > 8) pmax = 8;
+    double best = T / 16.0 * 0.9;  // a split must save at least a tenth
+    for (int P = 2; P <= pmax; ++P) {
+        const int len = ((T + P - 1) / P + 63) / 64 * 64;
+        if (len < 256) break;
+        const int nseg = (T + len - 1) / len;
+        if (nseg < 2) continue;
+        const double c = len / 16.0;
+        const double t = c * (nseg > 2 ? kMapToOutput : kChainToOutput) + c;
+        if (t < best) {
+            best = t;
+            pl.nsplit = nseg;
+            pl.len0 = pl.seg_len = len;
+        }
+    }
+    if (pl.nsplit < 2) return false;
+    const size_t dd = (size_t)a.d * a.d * sizeof(float);
+    pl.map_bytes = (size_t)BH * (pl.nsplit - 2) * 2 * dd;
+    pl.wst_bytes = (size_t)BH * (pl.nsplit - 1) * dd;
+    return true;
+}
+
+int launch_linear_seqpar_serial(const LinearArgs &a, const SeqparPlan &pl, void *ws)
+{
+    float *maps = static_cast<float *>(ws);
+    float *Wst = reinterpret_cast<float *>(static_cast<char *>(ws) + ((pl.map_bytes + 255) / 256) * 256);
+    CUtensorMap tm[3];
+    if (!encode_qkv(tm, a.q, a.k, a.v, a.B * a.H, a.T, a.d, 64)) return -4;
+    int rc = launch_linear_b16_segments(a, pl.nsplit, pl.len0, pl.seg_len, 0, 1, true, Wst, maps, tm);
+    if (rc == 0 && pl.nsplit > 2) rc = launch_scan(a, pl.nsplit, maps, Wst, a.stream);
+    if (rc == 0)
+        rc = launch_linear_b16_segments(a, pl.nsplit, pl.len0, pl.seg_len, 0, pl.nsplit, false, Wst, maps, tm);
+    return rc;
+}
+
 }  // namespace ttt
