@@ -24,6 +24,11 @@
  *   causal = 0: every query of a block reads the W at the end of that block
  *   (b = T gives the single full-batch step of the vision variant, ViT3 article,
  *   observation 2).
+ *   epochs (linear, causal = 0 with one block b >= T only): the block's gradient
+ *   step is taken `epochs` times, each pass with its gradients at the W the
+ *   previous pass left, before the queries read W (the ViT3 article, observation
+ *   2: one epoch of full-batch inner training is one update over all N tokens,
+ *   further epochs repeat it).
  *
  * Inner models (walkthrough section 2.2.1; ViT3 article observation 4):
  *   linear: f(x; W) = x W, W in R^{d x d} (row convention, x is a 1 x d row).
@@ -54,7 +59,7 @@
 /* ------------------------------------------------------------------ linear */
 
 typedef struct {
-    int B, H, T, d, b, causal, loss;
+    int B, H, T, d, b, causal, loss, epochs;
     const double *q, *k, *v, *eta;
     double eta_scalar;
     const double *W0;
@@ -82,6 +87,7 @@ static void linear_chain(const linear_job *J, int bh)
 
     for (int n0 = 0; n0 < T; n0 += b) {
         const int n1 = (n0 + b < T) ? n0 + b : T;
+        for (int ep = 0; ep < J->epochs; ++ep) {
         memcpy(Ws, W, sizeof(double) * d * d);
         for (int t = n0; t < n1; ++t) {
             const double *kt = k + (size_t)t * d, *vt = v + (size_t)t * d;
@@ -109,6 +115,7 @@ static void linear_chain(const linear_job *J, int bh)
                 }
             }
         }
+        }  /* epochs */
         if (!J->causal) {
             for (int t = n0; t < n1; ++t) {
                 const double *qt = q + (size_t)t * d;
@@ -137,7 +144,7 @@ static void *linear_worker(void *arg)
     return NULL;
 }
 
-int ttt_oracle_linear(int B, int H, int T, int d, int b, int causal, int loss,
+int ttt_oracle_linear(int B, int H, int T, int d, int b, int causal, int loss, int epochs,
                       const double *q, const double *k, const double *v,
                       const double *eta, double eta_scalar,
                       const double *W0, long long w0_bstride,
@@ -146,7 +153,8 @@ int ttt_oracle_linear(int B, int H, int T, int d, int b, int causal, int loss,
     if (B < 0 || H < 0 || T < 0 || d <= 0 || b <= 0 || !W0 || (T > 0 && (!q || !k || !v || !z)))
         return -1;
     if (loss != 0 && loss != 1) return -1;
-    linear_job J = {B, H, T, d, b, causal ? 1 : 0, loss, q, k, v, eta, eta_scalar,
+    if (epochs < 1 || (epochs > 1 && (causal || b < T))) return -1;
+    linear_job J = {B, H, T, d, b, causal ? 1 : 0, loss, epochs, q, k, v, eta, eta_scalar,
                     W0, w0_bstride, z, W_out, 0};
     pthread_mutex_init(&J.lock, NULL);
     if (nthreads < 1) nthreads = 1;

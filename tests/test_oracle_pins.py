@@ -119,6 +119,50 @@ def test_full_batch_is_one_gd_step_linear():
         np.testing.assert_allclose(z[0, h], q[0, h] @ W1, atol=1e-12)
 
 
+@pytest.mark.parametrize("epochs", [2, 3])
+def test_full_batch_epochs_are_repeated_gd_steps(epochs):
+    """b = T, non-causal, several inner epochs (ViT3 article, observation 2: an epoch
+    of full-batch inner training is one update over all N tokens): W_{e+1} =
+    W_e - grad(sum_s eta_s l_s)(W_e) by autograd, every query reads the last W."""
+    B, H, T, d = 1, 2, 13, 6
+    q, k, v = _qkv(B, H, T, d)
+    eta = rng.uniform(0.2, 1.0, (B, H, T))
+    W0 = rng.standard_normal((H, d, d)) * 0.2
+    z, Wf = oracle.linear(q, k, v, W0, b=T, causal=False, eta=eta, epochs=epochs)
+    for h in range(H):
+        W = torch.tensor(W0[h])
+        K, V = torch.tensor(k[0, h]), torch.tensor(v[0, h])
+        for _ in range(epochs):
+            Wg = W.clone().requires_grad_(True)
+            L = (torch.tensor(eta[0, h])[:, None] * 0.5 * (K @ Wg - V) ** 2).sum()
+            (g,) = torch.autograd.grad(L, Wg)
+            W = (Wg - g).detach()
+        np.testing.assert_allclose(Wf[0, h], W.numpy(), atol=1e-12)
+        np.testing.assert_allclose(z[0, h], q[0, h] @ W.numpy(), atol=1e-12)
+
+
+def test_full_batch_epochs_dot_loss_closed_form():
+    """Dot loss: the gradient -K^T V does not depend on W, so E epochs move W by
+    E * eta * K^T V exactly."""
+    B, H, T, d = 2, 1, 9, 5
+    q, k, v = _qkv(B, H, T, d, unit=False)
+    W0 = rng.standard_normal((H, d, d))
+    z, Wf = oracle.linear(q, k, v, W0, b=T, causal=False, eta_scalar=0.3, loss="dot", epochs=3)
+    for bi in range(B):
+        W = W0[0] + 3 * 0.3 * k[bi, 0].T @ v[bi, 0]
+        np.testing.assert_allclose(Wf[bi, 0], W, atol=1e-12)
+        np.testing.assert_allclose(z[bi, 0], q[bi, 0] @ W, atol=1e-12)
+
+
+def test_epochs_need_one_noncausal_block():
+    q, k, v = _qkv(1, 1, 8, 4)
+    W0 = np.zeros((1, 4, 4))
+    with pytest.raises(ValueError):
+        oracle.linear(q, k, v, W0, b=8, causal=True, epochs=2)
+    with pytest.raises(ValueError):
+        oracle.linear(q, k, v, W0, b=4, causal=False, epochs=2)
+
+
 @pytest.mark.parametrize("T,b,causal", [(11, 1, True), (11, 3, True), (11, 4, False),
                                         (12, 4, True), (10, 10, True), (9, 20, False)])
 def test_linear_matches_definition_autograd(T, b, causal):
