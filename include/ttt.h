@@ -65,6 +65,14 @@ typedef enum {
 
 typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
 
+/* Inner loss of TTT-Linear.
+ *   TTT_LOSS_MSE: l_t(W) = 1/2 || k_t W - v_t ||^2 (the reconstruction loss above).
+ *   TTT_LOSS_DOT: l_t(W) = -(k_t W) . v_t, the negative dot product ("TTT：Test-Time
+ *                 Training", section 如何理解; the inner loss of the ViT3 block).  Its
+ *                 gradient -k_t^T v_t does not depend on W, so the layer becomes
+ *                 linear attention with state W0 + sum eta_s k_s^T v_s. */
+typedef enum { TTT_LOSS_MSE = 0, TTT_LOSS_DOT = 1 } ttt_loss;
+
 /* TTT-Linear problem description. */
 typedef struct {
     int B, H, T, d;            /* batch, heads, tokens, head dim (d in {16,32,64,128}) */
@@ -73,6 +81,12 @@ typedef struct {
     ttt_dtype io_dtype;        /* dtype of q, k, v and z                               */
     long long w0_batch_stride; /* elements between batches of W0; 0 = W0 is [H,d,d]
                                   shared by every batch entry, H*d*d = [B,H,d,d]       */
+    int loss;                  /* ttt_loss (0 = TTT_LOSS_MSE)                          */
+    int epochs;                /* inner gradient steps on the mini-batch: 0 or 1 = one;
+                                  > 1 (the ViT3 article's inner epochs) needs causal = 0
+                                  and mini_batch >= T, every query reading the last W;
+                                  bf16 supports it for d = 64, T <= 256
+                                  (TTT_ERR_UNSUPPORTED otherwise)                       */
 } ttt_linear_desc;
 
 /*

@@ -28,7 +28,10 @@ EXPORTS = ("ttt_linear_fwd", "ttt_linear_seqpar_workspace", "ttt_linear_fwd_seqp
 class LinearDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
                 ("d", ctypes.c_int), ("mini_batch", ctypes.c_int), ("causal", ctypes.c_int),
-                ("io_dtype", ctypes.c_int), ("w0_batch_stride", ctypes.c_longlong)]
+                ("io_dtype", ctypes.c_int), ("w0_batch_stride", ctypes.c_longlong),
+                ("loss", ctypes.c_int), ("epochs", ctypes.c_int)]
+
+LOSSES = {"mse": 0, "dot": 1}
 
 
 class MlpDesc(ctypes.Structure):
@@ -115,10 +118,11 @@ def _f32(t, name):
 
 
 def ttt_linear_fwd(q, k, v, W0, mini_batch, causal=True, eta=None, eta_scalar=1.0,
-                   z=None, W_out=None, want_W=True, stream=None):
+                   z=None, W_out=None, want_W=True, stream=None, loss="mse", epochs=1):
     """TTT-Linear forward.  q,k,v: [B,H,T,d] bf16 or fp32 CUDA tensors; W0: fp32
-    [H,d,d] (shared over the batch) or [B,H,d,d]; eta: fp32 [B,H,T] or None.
-    Returns (z, W_final or None)."""
+    [H,d,d] (shared over the batch) or [B,H,d,d]; eta: fp32 [B,H,T] or None;
+    loss "mse" or "dot"; epochs > 1: repeated full-batch steps (causal=False,
+    mini_batch >= T).  Returns (z, W_final or None)."""
     io = _check_tokens(q, k, v)
     B, H, T, d = q.shape
     W0 = _f32(W0, "W0")
@@ -133,7 +137,8 @@ def ttt_linear_fwd(q, k, v, W0, mini_batch, causal=True, eta=None, eta_scalar=1.
         z = torch.empty_like(q)
     if W_out is None and want_W:
         W_out = torch.empty((B, H, d, d), device=q.device, dtype=torch.float32)
-    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, w0s)
+    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, w0s, LOSSES[loss],
+                      int(epochs))
     rc = lib().ttt_linear_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(eta),
                               float(eta_scalar), _ptr(W0), _ptr(z), _ptr(W_out), _stream(stream))
     if rc != 0:
@@ -141,16 +146,17 @@ def ttt_linear_fwd(q, k, v, W0, mini_batch, causal=True, eta=None, eta_scalar=1.
     return z, W_out
 
 
-def ttt_linear_seqpar_workspace(B, H, T, d, mini_batch, causal=True, dtype=torch.bfloat16) -> int:
+def ttt_linear_seqpar_workspace(B, H, T, d, mini_batch, causal=True, dtype=torch.bfloat16,
+                                loss="mse") -> int:
     """Workspace bytes ttt_linear_fwd_seqpar needs on the current device (0: the
     problem is not split)."""
     io = TTT_BF16 if dtype == torch.bfloat16 else TTT_F32
-    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, 0)
+    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, 0, LOSSES[loss], 1)
     return int(lib().ttt_linear_seqpar_workspace(ctypes.byref(desc)))
 
 
 def ttt_linear_fwd_seqpar(q, k, v, W0, mini_batch, causal=True, eta=None, eta_scalar=1.0,
-                          z=None, W_out=None, want_W=True, workspace=None, stream=None):
+                          z=None, W_out=None, want_W=True, workspace=None, stream=None, loss="mse"):
     """Sequence-parallel TTT-Linear forward (same arguments as ttt_linear_fwd).
     workspace: a CUDA uint8 tensor of at least ttt_linear_seqpar_workspace(...) bytes,
     allocated here when None.  Returns (z, W_final or None)."""
@@ -168,7 +174,7 @@ def ttt_linear_fwd_seqpar(q, k, v, W0, mini_batch, causal=True, eta=None, eta_sc
         z = torch.empty_like(q)
     if W_out is None and want_W:
         W_out = torch.empty((B, H, d, d), device=q.device, dtype=torch.float32)
-    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, w0s)
+    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, w0s, LOSSES[loss], 1)
     need = int(lib().ttt_linear_seqpar_workspace(ctypes.byref(desc)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -182,7 +188,7 @@ def ttt_linear_fwd_seqpar(q, k, v, W0, mini_batch, causal=True, eta=None, eta_sc
 
 
 def ttt_linear_fwd_seqpar_noalloc(q, k, v, W0, z, W_out, mini_batch, causal=True, eta=None,
-                                  eta_scalar=1.0, stream=None):
+                                  eta_scalar=1.0, stream=None, loss="mse"):
     """The sequence-parallel forward on the library's fixed scratch (no workspace,
     no allocation inside the call): z and W_out are the caller's output tensors."""
     io = _check_tokens(q, k, v)
@@ -198,7 +204,7 @@ def ttt_linear_fwd_seqpar_noalloc(q, k, v, W0, z, W_out, mini_batch, causal=True
         raise ValueError("W0 must be [H,d,d] or [B,H,d,d]")
     if z.shape != q.shape or z.dtype != q.dtype or not z.is_contiguous():
         raise ValueError("z must be a contiguous tensor shaped and typed like q")
-    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, w0s)
+    desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, w0s, LOSSES[loss], 1)
     rc = lib().ttt_linear_fwd_seqpar_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(eta),
                                              float(eta_scalar), _ptr(W0), _ptr(z), _ptr(W_out),
                                              _stream(stream))

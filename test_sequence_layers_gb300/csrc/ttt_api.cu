@@ -131,6 +131,9 @@ ttt_status linear_args(const ttt_linear_desc *desc, const void *q, const void *k
     if (D.io_dtype != TTT_F32 && D.io_dtype != TTT_BF16) return TTT_ERR_ARG;
     if (D.T > 0 && (!q || !k || !v || !z)) return TTT_ERR_ARG;
     if (D.d != 16 && D.d != 32 && D.d != 64 && D.d != 128) return TTT_ERR_UNSUPPORTED;
+    if (D.loss != TTT_LOSS_MSE && D.loss != TTT_LOSS_DOT) return TTT_ERR_ARG;
+    if (D.epochs < 0) return TTT_ERR_ARG;
+    if (D.epochs > 1 && (D.causal || D.mini_batch < D.T)) return TTT_ERR_UNSUPPORTED;
     const long long dd = (long long)D.d * D.d;
     if (D.w0_batch_stride != 0 && D.w0_batch_stride != (long long)D.H * dd) return TTT_ERR_ARG;
     if ((long long)D.B * D.H > 0x7fffffffLL) return TTT_ERR_UNSUPPORTED;
@@ -146,6 +149,8 @@ ttt_status linear_args(const ttt_linear_desc *desc, const void *q, const void *k
     a.d = D.d;
     a.b = D.T > 0 && D.mini_batch > D.T ? D.T : D.mini_batch;  // b >= T is one block
     a.causal = D.causal;
+    a.loss = D.loss;
+    a.epochs = D.epochs > 1 ? D.epochs : 1;
     a.q = q;
     a.k = k;
     a.v = v;
@@ -166,7 +171,7 @@ int launch_linear(const ttt::LinearArgs &a, ttt_dtype io)
     int rc;
     if (io == TTT_BF16) {
         rc = ttt::launch_linear_fb(a);  // full-batch mini-batch: no serial chain
-        if (rc == TTT_ERR_UNSUPPORTED)
+        if (rc == TTT_ERR_UNSUPPORTED && a.epochs == 1)  // repeated epochs: the full-batch kernel only
             rc = (a.b == 16 && a.d <= 64) ? ttt::launch_linear_b16(a) : ttt::launch_linear_bf16(a);
     } else
         rc = ttt::launch_linear_f32(a);
@@ -206,6 +211,8 @@ size_t ttt_linear_seqpar_workspace(const ttt_linear_desc *desc)
     a.T = desc->T;
     a.d = desc->d;
     a.b = desc->mini_batch > desc->T ? desc->T : desc->mini_batch;
+    a.loss = desc->loss;
+    a.epochs = desc->epochs > 1 ? desc->epochs : 1;
     return ttt::seqpar_workspace_bytes(seqpar_plan_for(desc, a));
 }
 

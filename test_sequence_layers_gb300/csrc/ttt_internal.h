@@ -9,6 +9,7 @@ namespace ttt {
 
 struct LinearArgs {
     int B, H, T, d, b, causal;
+    int loss = 0, epochs = 1;  // loss: 0 MSE, 1 negative dot product; inner GD steps per mini-batch
     const void *q, *k, *v;
     const float *eta;
     float eta_scalar;

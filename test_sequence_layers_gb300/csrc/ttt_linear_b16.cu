@@ -98,7 +98,9 @@ struct B16Params {
 
 // One unit (chain bh, segment seg) in role ROLE; the CTA has at least the role's
 // warps (extra warps leave after the barrier set-up).
-template <int D, int ROLE>
+// DOT: the negative dot-product loss, whose residual is -V whatever W is (no
+// product K W on the chain).
+template <int D, int ROLE, bool DOT = false>
 __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                                          const B16Params &p, const int bh, const int seg)
 {
@@ -266,7 +268,7 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
                 }
         }
 #pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {
+        for (int kk = 0; kk < NK && !DOT; ++kk) {
             mma_bf16(e[ONE ? 0 : kk & 1][0], wb[4 * kk], wb[4 * kk + 1], wb[4 * kk + 2], wb[4 * kk + 3],
                      F.kB[kk][0], F.kB[kk][1]);
             mma_bf16(e[ONE ? 0 : kk & 1][1], wb[4 * kk], wb[4 * kk + 1], wb[4 * kk + 2], wb[4 * kk + 3],
@@ -388,12 +390,12 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
 }
 
 // Output units: CTA u serves chain u / nseg, segment seg0 + u % nseg.
-template <int D>
+template <int D, bool DOT>
 __global__ void __launch_bounds__(B16Cfg<D, false>::THREADS, 1)
     ttt_linear_b16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                           const __grid_constant__ CUtensorMap tv, const B16Params p)
 {
-    b16_unit<D, kRoleOut>(&tq, &tk, &tv, p, blockIdx.x / p.nseg, p.seg0 + blockIdx.x % p.nseg);
+    b16_unit<D, kRoleOut, DOT>(&tq, &tk, &tv, p, blockIdx.x / p.nseg, p.seg0 + blockIdx.x % p.nseg);
 }
 
 // The work before a split run's later segments: CTAs 0 .. BH-1 run the state chain
@@ -415,7 +417,8 @@ template <int D, bool PREP>
 int launch_b16_t(const LinearArgs &a, const B16Params &p, int units, const CUtensorMap *maps)
 {
     using C = B16Cfg<D, PREP>;
-    auto kern = PREP ? ttt_linear_b16_prep_kernel<D> : ttt_linear_b16_kernel<D>;
+    auto kern = PREP ? ttt_linear_b16_prep_kernel<D>
+                     : (a.loss ? ttt_linear_b16_kernel<D, true> : ttt_linear_b16_kernel<D, false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return -4;
     kern<<<units, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);

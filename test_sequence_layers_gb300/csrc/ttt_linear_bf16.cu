@@ -71,7 +71,7 @@ __device__ __forceinline__ uint32_t toff(int r, int c)
 }
 
 struct LinParams {
-    int H, T, b, causal;
+    int H, T, b, causal, dot;  // dot: negative dot-product loss (residual -V)
     const float *eta;
     float eta_scalar;
     const float *W0;
@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(LinCfg<D>::THREADS, 1)
             float e[2][4] = {}, e2[2][4] = {};
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
+                if (p.dot) break;
                 uint32_t b00, b01, b10, b11;
                 ldsm_x4(tK + toff<D>(rowB, 16 * kk + colB), b00, b01, b10, b11);
                 float(&acc)[2][4] = (kk & 1) ? e2 : e;
@@ -343,6 +344,7 @@ static int launch_t(const LinearArgs &a, const CUtensorMap *maps)
     p.T = a.T;
     p.b = a.b;
     p.causal = a.causal;
+    p.dot = a.loss;
     p.eta = a.eta;
     p.eta_scalar = a.eta_scalar;
     p.W0 = a.W0;

@@ -8,6 +8,11 @@
 //
 //   E = K W0 - V,   W1 = W0 - K^T diag(eta) E,   Z = Q W1
 //
+// With several inner epochs (the same article, observation 2: one epoch of
+// full-batch inner training is one update over all N tokens) the E / update pass
+// repeats from the W the previous pass left while K and V are still on chip; with
+// the negative dot-product loss the residual is -V.
+//
 // are three independent passes over 16-token chunks.  One CTA per (batch, head):
 // the whole sequence's K and V land in shared memory with one TMA load per 64-token
 // box (one mbarrier per box, so the update pass starts on the first), Q replaces V
@@ -44,7 +49,7 @@ __device__ __forceinline__ uint32_t fboff(int r, int c)
 }
 
 struct FbParams {
-    int H, T;
+    int H, T, dot, epochs;
     const float *eta;
     float eta_scalar;
     const float *W0;
@@ -134,7 +139,8 @@ __global__ void __launch_bounds__(FbCfg::THREADS, 3)
         const uint32_t ck = sK + t0 * C::RB;
         float e[2][2][4] = {};
 #pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {  // E^T = W^T K^T
+        for (int kk = 0; kk < NK; ++kk) {  // E^T = W^T K^T (no product for the dot loss)
+            if (p.dot) break;
             uint32_t b0, b1, b2, b3;
             ldsm_x4(ck + offB[kk], b0, b1, b2, b3);
             mma_bf16(e[kk & 1][0], wb[4 * kk], wb[4 * kk + 1], wb[4 * kk + 2], wb[4 * kk + 3], b0, b1);
@@ -165,12 +171,14 @@ __global__ void __launch_bounds__(FbCfg::THREADS, 3)
             mma_bf16(wacc[2 * j2 + 1], ea0, ea1, ea2, ea3, k2, k3);
         }
     };
-    for (int c = 0; c < nch && ok; ++c) {
-        if ((c & 3) == 0) ok = mbar_wait(kv_bar + 8 * (c >> 2), 0, p.status, kSiteConsumerFull);
-        if (16 * c + 16 <= T) upd_chunk(std::true_type{}, 16 * c);
-        else upd_chunk(std::false_type{}, 16 * c);
+    for (int ep = 0; ep < p.epochs && ok; ++ep) {
+        for (int c = 0; c < nch && ok; ++c) {
+            if (ep == 0 && (c & 3) == 0) ok = mbar_wait(kv_bar + 8 * (c >> 2), 0, p.status, kSiteConsumerFull);
+            if (16 * c + 16 <= T) upd_chunk(std::true_type{}, 16 * c);
+            else upd_chunk(std::false_type{}, 16 * c);
+        }
+        convert();  // the next pass's residuals (and finally Z) read these weights
     }
-    convert();  // W1
     // Q into V's place once no warp reads V any more
     __syncthreads();
     if (threadIdx.x == 0 && nblk > 0 && ok) {
@@ -230,6 +238,8 @@ int launch_linear_fb(const LinearArgs &a)
     FbParams p;
     p.H = a.H;
     p.T = a.T;
+    p.dot = a.loss;
+    p.epochs = a.epochs;
     p.eta = a.eta;
     p.eta_scalar = a.eta_scalar;
     p.W0 = a.W0;

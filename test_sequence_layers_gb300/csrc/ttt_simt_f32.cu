@@ -18,7 +18,7 @@ namespace {
 constexpr int kThreads = 256;
 
 struct LinF32Params {
-    int H, T, d, b, causal;
+    int H, T, d, b, causal, dot, epochs;  // dot: negative dot-product loss; epochs: passes per block
     const float *q, *k, *v, *eta;
     float eta_scalar;
     const float *W0;
@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
 
     for (int n0 = 0; n0 < T; n0 += p.b) {
         const int n1 = min(n0 + p.b, T);
+        for (int ep = 0; ep < p.epochs; ++ep) {  // more than one only for one non-causal block
         __syncthreads();
         for (int i = tid; i < D * D; i += blockDim.x) Ws[i] = W[i];
         for (int t = n0; t < n1; ++t) {
@@ -50,9 +51,10 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
                 qq[tid] = q[(size_t)t * D + tid];
             }
             __syncthreads();
-            if (tid < D) {  // e = k_t W_start - v_t
+            if (tid < D) {  // e = k_t W_start - v_t (dot loss: e = -v_t)
                 float s = 0.f;
-                for (int i = 0; i < D; ++i) s = fmaf(kk[i], Ws[i * D + tid], s);
+                if (!p.dot)
+                    for (int i = 0; i < D; ++i) s = fmaf(kk[i], Ws[i * D + tid], s);
                 ee[tid] = s - vv[tid];
             }
             __syncthreads();
@@ -68,6 +70,7 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
                 }
             }
         }
+        }  // epochs
         if (!p.causal) {
             for (int t = n0; t < n1; ++t) {
                 __syncthreads();
@@ -101,6 +104,8 @@ int launch_linear_f32(const LinearArgs &a)
     p.d = D;
     p.b = a.b;
     p.causal = a.causal;
+    p.dot = a.loss;
+    p.epochs = a.epochs;
     p.q = static_cast<const float *>(a.q);
     p.k = static_cast<const float *>(a.k);
     p.v = static_cast<const float *>(a.v);

@@ -43,7 +43,7 @@ FAKE = 1 << 20  # an aligned address that is never dereferenced (validation fail
 
 def _lin(**kw):
     d = dict(B=1, H=1, T=32, d=64, mini_batch=16, causal=1, io_dtype=abi.TTT_BF16,
-             w0_batch_stride=0)
+             w0_batch_stride=0, loss=0, epochs=1)
     d.update(kw)
     return abi.LinearDesc(**d)
 
@@ -65,6 +65,10 @@ def test_linear_rejects_bad_arguments(L):
     assert _call_lin(L, _lin(), W0=None) == -1
     assert _call_lin(L, _lin(w0_batch_stride=7)) == -1
     assert _call_lin(L, _lin(d=48)) == -2
+    assert _call_lin(L, _lin(loss=2)) == -1
+    assert _call_lin(L, _lin(epochs=-1)) == -1
+    assert _call_lin(L, _lin(epochs=2)) == -2                     # causal
+    assert _call_lin(L, _lin(epochs=2, causal=0, mini_batch=16)) == -2  # b < T
     assert _call_lin(L, _lin(d=256)) == -2
     assert _call_lin(L, _lin(), q=FAKE + 8) == -3
     assert _call_lin(L, _lin(), z=FAKE + 2) == -3

@@ -156,3 +156,65 @@ def test_workload_vision_full_batch_sampled():
     inp = G.synth.workload("vision_linear")
     ez, eW = _check(inp, chains=[0, 5, 777, 1535])
     print(f"vision_linear rel err z {ez:.3e} W {eW:.3e}")
+
+
+# ------------------------------------------- dot-product loss and inner epochs
+
+
+def _check_variant(inp, loss="mse", epochs=1, tol=None):
+    """GPU vs oracle with the given inner loss and number of inner epochs."""
+    tol = tol or G.tol_for(inp)
+    dev = torch.device("cuda")
+    from test_sequence_layers_gb300 import abi
+    import oracle
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    eta = inp.eta.to(dev) if inp.eta is not None else None
+    z, W = abi.ttt_linear_fwd(q, k, v, inp.params["W0"].to(dev), inp.b, inp.causal, eta=eta,
+                              eta_scalar=inp.eta_scalar, loss=loss, epochs=epochs)
+    abi.ttt_sync_status()
+    zr, Wr = oracle.linear(inp.q, inp.k, inp.v, inp.params["W0"], inp.b, inp.causal, eta=inp.eta,
+                           eta_scalar=inp.eta_scalar, loss=loss, epochs=epochs)
+    ez, eW = G.rel_err(z.double().cpu(), zr), G.rel_err(W.double().cpu(), Wr)
+    assert ez <= tol and eW <= tol, (ez, eW, tol)
+
+
+@pytest.mark.parametrize("d,b,causal", [(16, 16, True), (64, 16, True), (64, 16, False), (32, 5, True),
+                                        (128, 16, True), (64, 1, True), (64, 196, False)])
+def test_dot_loss_bf16(d, b, causal):
+    """Negative dot-product loss (the ViT3 block's inner loss): residual -V; every
+    bf16 kernel (b = 16, general, full batch)."""
+    T = 196 if b == 196 else 150
+    inp = G.synth.make("linear", B=2, H=2, T=T, d=d, b=b, causal=causal, eta="sigmoid", seed=800 + d + b)
+    _check_variant(inp, loss="dot")
+
+
+@pytest.mark.parametrize("b,causal", [(3, True), (50, False)])
+def test_dot_loss_fp32(b, causal):
+    inp = G.synth.make("linear", B=2, H=2, T=50, d=16, b=b, causal=causal, dtype=torch.float32,
+                       eta="sigmoid", seed=810 + b)
+    _check_variant(inp, loss="dot", tol=G.TOL_F32)
+
+
+@pytest.mark.parametrize("loss", ["mse", "dot"])
+@pytest.mark.parametrize("epochs,T", [(2, 196), (3, 100), (2, 17)])
+def test_full_batch_epochs_bf16(loss, epochs, T):
+    """Several inner epochs of full-batch GD (ViT3 article, observation 2): b >= T,
+    non-causal, every query reads the last weights."""
+    inp = G.synth.make("linear", B=2, H=3, T=T, d=64, b=T, causal=False, eta="sigmoid", seed=820 + T + epochs)
+    _check_variant(inp, loss=loss, epochs=epochs)
+
+
+def test_full_batch_epochs_fp32():
+    inp = G.synth.make("linear", B=1, H=2, T=40, d=16, b=40, causal=False, dtype=torch.float32,
+                       eta=0.5, seed=830)
+    _check_variant(inp, epochs=3, tol=G.TOL_F32)
+
+
+def test_epochs_outside_the_full_batch_kernel_are_unsupported():
+    inp = G.synth.make("linear", B=1, H=1, T=64, d=32, b=64, causal=False, seed=840)
+    dev = torch.device("cuda")
+    from test_sequence_layers_gb300 import abi
+    with pytest.raises(abi.TTTError) as e:
+        abi.ttt_linear_fwd(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.params["W0"].to(dev), 64,
+                           causal=False, epochs=2)
+    assert e.value.code == -2

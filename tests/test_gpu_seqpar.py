@@ -95,3 +95,17 @@ def test_workload_long_context_gated_split_sampled():
     inp = G.synth.workload("linear_long_gated")
     ez, eW = _check(inp, chains=[0, 17, 63])
     print(f"linear_long_gated (split) rel err z {ez:.3e} W {eW:.3e}")
+
+
+def test_dot_loss_runs_unsplit():
+    """The negative dot-product loss has no serial chain to split: no workspace,
+    and the entry point gives ttt_linear_fwd's results."""
+    inp = G.synth.make("linear", B=1, H=2, T=1024, d=64, b=16, causal=True, seed=640)
+    assert abi.ttt_linear_seqpar_workspace(1, 2, 1024, 64, 16, loss="dot") == 0
+    dev = torch.device("cuda")
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    W0 = inp.params["W0"].to(dev)
+    zs, Ws = abi.ttt_linear_fwd_seqpar(q, k, v, W0, 16, loss="dot")
+    zp, Wp = abi.ttt_linear_fwd(q, k, v, W0, 16, loss="dot")
+    abi.ttt_sync_status()
+    assert torch.equal(zs, zp) and torch.equal(Ws, Wp)
