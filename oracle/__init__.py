@@ -42,7 +42,7 @@ def _load():
         lib.ttt_oracle_linear.argtypes = [i, i, i, i, i, i, i, i, dp, dp, dp, dp, d, dp, ll, dp, dp, i]
         lib.ttt_oracle_linear.restype = i
         lib.ttt_oracle_mlp.argtypes = [i, i, i, i, i, i, i, dp, dp, dp, dp, d,
-                                       dp, dp, dp, dp, i, dp, dp, dp, dp, dp, i]
+                                       dp, dp, dp, dp, i, dp, dp, dp, dp, dp, i, i]
         lib.ttt_oracle_mlp.restype = i
         _lib = lib
     return _lib
@@ -96,10 +96,12 @@ def linear(q, k, v, W0, b, causal=True, eta=None, eta_scalar=1.0, loss="mse",
     return z, Wf
 
 
-def mlp(q, k, v, W1, c1, W2, c2, b, causal=True, eta=None, eta_scalar=0.1, threads=None):
-    """TTT-MLP forward, fp64, f(x) = SiLU(x W1 + c1) W2 + c2.  Parameters are given
-    per head ([H,...], shared over the batch) or per (batch, head) ([B,H,...]).
-    Returns (z, W1_final, c1_final, W2_final, c2_final)."""
+def mlp(q, k, v, W1, c1, W2, c2, b, causal=True, eta=None, eta_scalar=0.1, threads=None,
+        activation="silu"):
+    """TTT-MLP forward, fp64, f(x) = act(x W1 + c1) W2 + c2, act "silu" or "gelu"
+    (erf form).  Parameters are given per head ([H,...], shared over the batch) or
+    per (batch, head) ([B,H,...]).  Returns (z, W1_final, c1_final, W2_final,
+    c2_final)."""
     q, k, v, eta = _f64(q), _f64(k), _f64(v), _f64(eta)
     W1, c1, W2, c2 = _f64(W1), _f64(c1), _f64(W2), _f64(c2)
     B, H, T, d = q.shape
@@ -117,7 +119,7 @@ def mlp(q, k, v, W1, c1, W2, c2, b, causal=True, eta=None, eta_scalar=0.1, threa
                                 _ptr(q), _ptr(k), _ptr(v), _ptr(eta), float(eta_scalar),
                                 _ptr(W1), _ptr(c1), _ptr(W2), _ptr(c2), per_batch,
                                 _ptr(z), _ptr(W1o), _ptr(c1o), _ptr(W2o), _ptr(c2o),
-                                threads or default_threads())
+                                threads or default_threads(), {"silu": 0, "gelu": 1}[activation])
     if rc != 0:
         raise ValueError("ttt_oracle_mlp rejected its arguments")
     return z, W1o, c1o, W2o, c2o

@@ -32,15 +32,18 @@
  *
  * Inner models (walkthrough section 2.2.1; ViT3 article observation 4):
  *   linear: f(x; W) = x W, W in R^{d x d} (row convention, x is a 1 x d row).
- *   mlp   : f(x) = SiLU(x W1 + c1) W2 + c2, W1 d x m, c1 1 x m, W2 m x d, c2 1 x d,
- *           SiLU(h) = h * sigma(h).
+ *   mlp   : f(x) = act(x W1 + c1) W2 + c2, W1 d x m, c1 1 x m, W2 m x d, c2 1 x d,
+ *           act = SiLU, SiLU(h) = h * sigma(h) (ViT3 article, observation 4), or
+ *           act = GELU, GELU(h) = h * Phi(h) with Phi the standard normal CDF
+ *           (the walkthrough's TTT-MLP, section 2.2.1; exact erf form).
  * Gradients are written out by hand from the chain rule:
  *   linear mse: e = k W - v,   dW = k^T e
  *   linear dot (negative dot-product loss l = -(k W) v^T, "TTT：Test-Time Training",
  *              section "如何理解"): dW = -k^T v
- *   mlp: h = k W1 + c1, a = SiLU(h), e = a W2 + c2 - v,
- *        dW2 = a^T e, dc2 = e, g = (e W2^T) * SiLU'(h), dW1 = k^T g, dc1 = g,
- *        SiLU'(h) = sigma(h) (1 + h (1 - sigma(h))).
+ *   mlp: h = k W1 + c1, a = act(h), e = a W2 + c2 - v,
+ *        dW2 = a^T e, dc2 = e, g = (e W2^T) * act'(h), dW1 = k^T g, dc1 = g,
+ *        SiLU'(h) = sigma(h) (1 + h (1 - sigma(h))), GELU'(h) = Phi(h) + h phi(h)
+ *        with phi the standard normal density.
  *
  * Layouts: all arrays are C-contiguous double.  q, k, v, z: [B,H,T,d];
  * eta: [B,H,T] or NULL (then eta_scalar is used for every token);
@@ -170,8 +173,26 @@ int ttt_oracle_linear(int B, int H, int T, int d, int b, int causal, int loss, i
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
+/* act(h) and act'(h); act 0 = SiLU, 1 = GELU (erf form) */
+static double act_f(int act, double h)
+{
+    if (act == 0) return h * sigmoid(h);
+    return h * 0.5 * (1.0 + erf(h / sqrt(2.0)));
+}
+
+static double act_d(int act, double h)
+{
+    if (act == 0) {
+        const double sg = sigmoid(h);
+        return sg * (1.0 + h * (1.0 - sg));
+    }
+    const double Phi = 0.5 * (1.0 + erf(h / sqrt(2.0)));
+    const double phi = exp(-0.5 * h * h) / sqrt(2.0 * 3.14159265358979323846);
+    return Phi + h * phi;
+}
+
 typedef struct {
-    int B, H, T, d, m, b, causal;
+    int B, H, T, d, m, b, causal, act;
     const double *q, *k, *v, *eta;
     double eta_scalar;
     const double *W1, *c1, *W2, *c2;
@@ -181,14 +202,14 @@ typedef struct {
     pthread_mutex_t lock;
 } mlp_job;
 
-/* z = SiLU(x W1 + c1) W2 + c2 with scratch h (length m) */
-static void mlp_forward(int d, int m, const double *x, const double *W1, const double *c1,
+/* z = act(x W1 + c1) W2 + c2 with scratch h (length m) */
+static void mlp_forward(int act, int d, int m, const double *x, const double *W1, const double *c1,
                         const double *W2, const double *c2, double *h, double *out)
 {
     for (int j = 0; j < m; ++j) {
         double s = c1[j];
         for (int i = 0; i < d; ++i) s += x[i] * W1[i * m + j];
-        h[j] = s * sigmoid(s);
+        h[j] = act_f(act, s);
     }
     for (int j = 0; j < d; ++j) {
         double s = c2[j];
@@ -233,19 +254,23 @@ static void mlp_chain(const mlp_job *J, int bh)
                 double s = c1s[j];
                 for (int i = 0; i < d; ++i) s += kt[i] * W1s[i * m + j];
                 h[j] = s;
-                a[j] = s * sigmoid(s);
+                a[j] = act_f(J->act, s);
             }
             for (int j = 0; j < d; ++j) {
                 double s = c2s[j];
                 for (int i = 0; i < m; ++i) s += a[i] * W2s[i * d + j];
                 e[j] = s - vt[j];
             }
-            /* backward: g = (e W2s^T) * SiLU'(h) */
+            /* backward: g = (e W2s^T) * act'(h) */
             for (int i = 0; i < m; ++i) {
                 double s = 0.0;
                 for (int j = 0; j < d; ++j) s += e[j] * W2s[i * d + j];
-                const double sg = sigmoid(h[i]);
-                g[i] = s * sg * (1.0 + h[i] * (1.0 - sg));
+                if (J->act == 0) {
+                    const double sg = sigmoid(h[i]);
+                    g[i] = s * sg * (1.0 + h[i] * (1.0 - sg));
+                } else {
+                    g[i] = s * act_d(J->act, h[i]);
+                }
             }
             /* descent step of token t */
             for (int i = 0; i < m; ++i)
@@ -255,11 +280,11 @@ static void mlp_chain(const mlp_job *J, int bh)
                 for (int j = 0; j < m; ++j) W1[i * m + j] -= et * kt[i] * g[j];
             for (int j = 0; j < m; ++j) c1[j] -= et * g[j];
             if (J->causal)
-                mlp_forward(d, m, q + (size_t)t * d, W1, c1, W2, c2, h, z + (size_t)t * d);
+                mlp_forward(J->act, d, m, q + (size_t)t * d, W1, c1, W2, c2, h, z + (size_t)t * d);
         }
         if (!J->causal)
             for (int t = n0; t < n1; ++t)
-                mlp_forward(d, m, q + (size_t)t * d, W1, c1, W2, c2, h, z + (size_t)t * d);
+                mlp_forward(J->act, d, m, q + (size_t)t * d, W1, c1, W2, c2, h, z + (size_t)t * d);
     }
     if (J->W1o) memcpy(J->W1o + (size_t)bh * d * m, W1, sizeof(double) * d * m);
     if (J->c1o) memcpy(J->c1o + (size_t)bh * m, c1, sizeof(double) * m);
@@ -288,12 +313,12 @@ int ttt_oracle_mlp(int B, int H, int T, int d, int m, int b, int causal,
                    const double *W1, const double *c1, const double *W2, const double *c2,
                    int per_batch,
                    double *z, double *W1o, double *c1o, double *W2o, double *c2o,
-                   int nthreads)
+                   int nthreads, int act)
 {
     if (B < 0 || H < 0 || T < 0 || d <= 0 || m <= 0 || b <= 0 || !W1 || !c1 || !W2 || !c2 ||
-        (T > 0 && (!q || !k || !v || !z)))
+        (T > 0 && (!q || !k || !v || !z)) || (act != 0 && act != 1))
         return -1;
-    mlp_job J = {B, H, T, d, m, b, causal ? 1 : 0, q, k, v, eta, eta_scalar,
+    mlp_job J = {B, H, T, d, m, b, causal ? 1 : 0, act, q, k, v, eta, eta_scalar,
                  W1, c1, W2, c2, per_batch ? 1 : 0, z, W1o, c1o, W2o, c2o, 0};
     pthread_mutex_init(&J.lock, NULL);
     if (nthreads < 1) nthreads = 1;

@@ -22,6 +22,11 @@ def f_mlp(x, P):
     return silu_t(x @ W1 + c1) @ W2 + c2
 
 
+def f_mlp_gelu(x, P):
+    W1, c1, W2, c2 = P
+    return torch.nn.functional.gelu(x @ W1 + c1) @ W2 + c2
+
+
 def definition_autograd(f, P0, q, k, v, eta, b, causal):
     """The layer exactly as defined, one chain, fp64 torch, gradients by autograd.
 
@@ -70,10 +75,18 @@ def dual_linear(q, k, v, W0, eta, b, causal):
     return z, W
 
 
-def dual_mlp(q, k, v, W1, c1, W2, c2, eta, b, causal):
+def dual_mlp(q, k, v, W1, c1, W2, c2, eta, b, causal, activation="silu"):
     """TTT-MLP mini-batch step in matrix form (numpy fp64, one chain).  The "+1"
     terms carry the bias writes: c_t = c - sum_{s<=t} eta_s * grad_c l_s."""
+    from scipy.special import erf
     sig = lambda x: 1.0 / (1.0 + np.exp(-x))
+    if activation == "silu":
+        act = lambda x: x * sig(x)
+        dact = lambda x: sig(x) * (1 + x * (1 - sig(x)))
+    else:
+        Phi = lambda x: 0.5 * (1 + erf(x / np.sqrt(2)))
+        act = lambda x: x * Phi(x)
+        dact = lambda x: Phi(x) + x * np.exp(-0.5 * x * x) / np.sqrt(2 * np.pi)
     T, d = q.shape
     W1, c1, W2, c2 = W1.copy(), c1.copy(), W2.copy(), c2.copy()
     z = np.zeros((T, d))
@@ -83,12 +96,12 @@ def dual_mlp(q, k, v, W1, c1, W2, c2, eta, b, causal):
         n = n1 - n0
         M = np.tril(np.ones((n, n))) if causal else np.ones((n, n))
         Hk = K @ W1 + c1
-        Ak = Hk * sig(Hk)
+        Ak = act(Hk)
         E = Ak @ W2 + c2 - V
-        D = (E @ W2.T) * (sig(Hk) * (1 + Hk * (1 - sig(Hk))))
+        D = (E @ W2.T) * dact(Hk)
         Et, Dt = et * E, et * D
         Hq = Q @ W1 + c1 - (M * (Q @ K.T + 1)) @ Dt
-        Aq = Hq * sig(Hq)
+        Aq = act(Hq)
         z[n0:n1] = Aq @ W2 + c2 - (M * (Aq @ Ak.T + 1)) @ Et
         W2 = W2 - Ak.T @ Et
         c2 = c2 - Et.sum(0)
