@@ -171,6 +171,12 @@ ttt_status ttt_linear_fwd_seqpar_noalloc(const ttt_linear_desc *desc,
                                          const float *eta, float eta_scalar,
                                          const float *W0, void *z, float *W_out, void *stream);
 
+/* Inner activation of TTT-MLP.
+ *   TTT_ACT_SILU: SiLU(h) = h sigma(h) (the ViT3 article, observation 4).
+ *   TTT_ACT_GELU: GELU(h) = h Phi(h), Phi the standard normal CDF, in its exact
+ *                 (erf) form (the walkthrough's TTT-MLP, section 2.2.1). */
+typedef enum { TTT_ACT_SILU = 0, TTT_ACT_GELU = 1 } ttt_activation;
+
 /* TTT-MLP problem description. */
 typedef struct {
     int B, H, T, d, m;         /* d in {16,32,64}; m = hidden width, multiple of 16    */
@@ -179,10 +185,11 @@ typedef struct {
     ttt_dtype io_dtype;
     int params_per_batch;      /* 0: W1,c1,W2,c2 are [H,...] shared over the batch;
                                   1: they are [B,H,...]                                */
+    int activation;            /* ttt_activation (0 = TTT_ACT_SILU)                    */
 } ttt_mlp_desc;
 
 /*
- * TTT-MLP forward, f(x) = SiLU(x W1 + c1) W2 + c2 (SiLU(h) = h * sigmoid(h)).
+ * TTT-MLP forward, f(x) = act(x W1 + c1) W2 + c2, act = SiLU or GELU (desc->activation).
  *   W1 [..,d,m], c1 [..,m], W2 [..,m,d], c2 [..,d] fp32 initial inner weights;
  *   the *_out arrays are [B,H,...] fp32 final weights (each may be NULL).
  * Other arguments as for ttt_linear_fwd.

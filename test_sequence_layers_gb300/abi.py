@@ -38,7 +38,9 @@ class MlpDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
                 ("d", ctypes.c_int), ("m", ctypes.c_int), ("mini_batch", ctypes.c_int),
                 ("causal", ctypes.c_int), ("io_dtype", ctypes.c_int),
-                ("params_per_batch", ctypes.c_int)]
+                ("params_per_batch", ctypes.c_int), ("activation", ctypes.c_int)]
+
+ACTIVATIONS = {"silu": 0, "gelu": 1}
 
 
 class TTTError(RuntimeError):
@@ -214,9 +216,10 @@ def ttt_linear_fwd_seqpar_noalloc(q, k, v, W0, z, W_out, mini_batch, causal=True
 
 
 def ttt_mlp_fwd(q, k, v, W1, c1, W2, c2, mini_batch, causal=True, eta=None, eta_scalar=0.1,
-                z=None, outs=None, want_W=True, stream=None):
-    """TTT-MLP forward, f(x) = SiLU(x W1 + c1) W2 + c2.  Parameters fp32, per head
-    ([H,...]) or per (batch, head) ([B,H,...]).  Returns (z, (W1,c1,W2,c2) final or None)."""
+                z=None, outs=None, want_W=True, stream=None, activation="silu"):
+    """TTT-MLP forward, f(x) = act(x W1 + c1) W2 + c2, activation "silu" or "gelu".
+    Parameters fp32, per head ([H,...]) or per (batch, head) ([B,H,...]).  Returns
+    (z, (W1,c1,W2,c2) final or None)."""
     io = _check_tokens(q, k, v)
     B, H, T, d = q.shape
     W1, c1, W2, c2 = (_f32(t, n) for t, n in ((W1, "W1"), (c1, "c1"), (W2, "W2"), (c2, "c2")))
@@ -234,7 +237,8 @@ def ttt_mlp_fwd(q, k, v, W1, c1, W2, c2, mini_batch, causal=True, eta=None, eta_
         outs = (torch.empty((B, H, d, m), device=dev), torch.empty((B, H, m), device=dev),
                 torch.empty((B, H, m, d), device=dev), torch.empty((B, H, d), device=dev))
     o = outs if outs is not None else (None, None, None, None)
-    desc = MlpDesc(B, H, T, d, m, int(mini_batch), 1 if causal else 0, io, per_batch)
+    desc = MlpDesc(B, H, T, d, m, int(mini_batch), 1 if causal else 0, io, per_batch,
+                   ACTIVATIONS[activation])
     rc = lib().ttt_mlp_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(eta),
                            float(eta_scalar), _ptr(W1), _ptr(c1), _ptr(W2), _ptr(c2), _ptr(z),
                            *(_ptr(t) for t in o), _stream(stream))

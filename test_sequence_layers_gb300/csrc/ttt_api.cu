@@ -253,6 +253,7 @@ ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc, const void *q, const void *k, c
     if (!W1 || !c1 || !W2 || !c2) return TTT_ERR_ARG;
     if (D.causal != 0 && D.causal != 1) return TTT_ERR_ARG;
     if (D.params_per_batch != 0 && D.params_per_batch != 1) return TTT_ERR_ARG;
+    if (D.activation != TTT_ACT_SILU && D.activation != TTT_ACT_GELU) return TTT_ERR_ARG;
     if (D.io_dtype != TTT_F32 && D.io_dtype != TTT_BF16) return TTT_ERR_ARG;
     if (D.T > 0 && (!q || !k || !v || !z)) return TTT_ERR_ARG;
     if (D.d != 16 && D.d != 32 && D.d != 64) return TTT_ERR_UNSUPPORTED;
@@ -280,6 +281,7 @@ ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc, const void *q, const void *k, c
     a.b = D.T > 0 && D.mini_batch > D.T ? D.T : D.mini_batch;
     a.causal = D.causal;
     a.per_batch = D.params_per_batch;
+    a.act = D.activation;
     a.q = q;
     a.k = k;
     a.v = v;

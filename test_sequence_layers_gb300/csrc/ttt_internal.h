@@ -23,6 +23,7 @@ struct LinearArgs {
 
 struct MlpArgs {
     int B, H, T, d, m, b, causal, per_batch;
+    int act = 0;  // inner activation: 0 SiLU, 1 GELU
     const void *q, *k, *v;
     const float *eta;
     float eta_scalar;

@@ -1,7 +1,9 @@
 // ttt_mlp_bf16.cu -- TTT-MLP forward on sm_103a: bf16 operands, fp32
 // accumulation, fp32 inner-weight state.
 //
-// Inner model f(x) = SiLU(x W1 + c1) W2 + c2 (two layers, hidden width m = 4d:
+// Inner model f(x) = act(x W1 + c1) W2 + c2, act = SiLU or GELU (template ACT; the
+// derivation below is written for SiLU and holds for any act with act' in place of
+// SiLU'), two layers, hidden width m = 4d (
 // "Learning to (Learn at Test Time)" walkthrough, section 2.2.1; SiLU and the
 // width ratio 4 of the ViT3 article, observation 4).  For one mini-batch
 // (chunk of <= 16 tokens here) with start weights, the per-token gradients of
@@ -102,6 +104,31 @@ __device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r
 // overflowing to +inf gives 0, the correct limit)
 __device__ __forceinline__ float sigmoid_f(float h) { return __fdividef(1.f, 1.f + __expf(-h)); }
 
+// Inner activation: ACT 0 = SiLU(h) = h sigma(h) (ViT3 article, observation 4),
+// ACT 1 = GELU(h) = h Phi(h), Phi the standard normal CDF written with erf (the
+// walkthrough's TTT-MLP, section 2.2.1).  act() gives the value, act_d() the value
+// and the derivative (SiLU' = sigma (1 + h (1 - sigma)), GELU' = Phi + h phi).
+template <int ACT>
+__device__ __forceinline__ float act(float h)
+{
+    if constexpr (ACT == 0) return h * sigmoid_f(h);
+    else return h * (0.5f + 0.5f * erff(h * 0.70710678118654752f));
+}
+
+template <int ACT>
+__device__ __forceinline__ void act_d(float h, float &a, float &ad)
+{
+    if constexpr (ACT == 0) {
+        const float sg = sigmoid_f(h);
+        a = h * sg;
+        ad = sg * (1.f + h * (1.f - sg));
+    } else {
+        const float Phi = 0.5f + 0.5f * erff(h * 0.70710678118654752f);
+        a = h * Phi;
+        ad = Phi + h * 0.39894228040143268f * __expf(-0.5f * h * h);
+    }
+}
+
 struct MlpParams {
     int H, T, b, causal, per_batch;
     const float *eta;
@@ -115,7 +142,7 @@ struct MlpParams {
 // MULTI: causal with mini-batches longer than one 16-token chunk, so the chunk's
 // queries read weights that already include the earlier chunks' writes while its
 // residuals are taken at the mini-batch's start weights.
-template <int D, bool MULTI>
+template <int D, bool MULTI, int ACT>
 __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
     ttt_mlp_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const MlpParams p)
@@ -313,10 +340,7 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float h = hk[nt][i] + c1s[nt][i & 1];
-                    const float sg = sigmoid_f(h);
-                    ak[nt][i] = h * sg;
-                    sp[nt][i] = sg * (1.f + h * (1.f - sg));
+                    act_d<ACT>(hk[nt][i] + c1s[nt][i & 1], ak[nt][i], sp[nt][i]);
                 }
             akp[0] = pack_bf16(ak[0][0], ak[0][1]);  // (tok 0-7, hidden 0-7)
             akp[1] = pack_bf16(ak[0][2], ak[0][3]);  // (tok 8-15, hidden 0-7)
@@ -483,8 +507,7 @@ __global__ void __launch_bounds__(MlpCfg<D>::THREADS, 1)
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float h = hq[nt][i] + c1r[nt][i & 1];
-                    aq[nt][i] = h * sigmoid_f(h);
+                    aq[nt][i] = act<ACT>(hq[nt][i] + c1r[nt][i & 1]);
                 }
             stsm_x4(AQ + rowA * C::AR + (h0 + colA) * 2, pack_bf16(aq[0][0], aq[0][1]),
                     pack_bf16(aq[0][2], aq[0][3]), pack_bf16(aq[1][0], aq[1][1]),
@@ -617,7 +640,8 @@ static int launch_mlp_t(const MlpArgs &a, const CUtensorMap *maps)
 {
     using C = MlpCfg<D>;
     const bool multi = a.causal && a.b > 16;
-    auto kern = multi ? ttt_mlp_bf16_kernel<D, true> : ttt_mlp_bf16_kernel<D, false>;
+    auto kern = multi ? (a.act ? ttt_mlp_bf16_kernel<D, true, 1> : ttt_mlp_bf16_kernel<D, true, 0>)
+                      : (a.act ? ttt_mlp_bf16_kernel<D, false, 1> : ttt_mlp_bf16_kernel<D, false, 0>);
     const int smem = multi ? C::SMEM_MULTI : C::SMEM_DBL;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return -4;
@@ -680,6 +704,7 @@ struct W8Cfg {
 static_assert(MlpCfg<64>::RB == 128, "tile rows of 128 bytes");
 static_assert(W8Cfg::SMEM <= 227 * 1024, "shared memory");
 
+template <int ACT>
 __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
     ttt_mlp_w8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const MlpParams p)
@@ -903,10 +928,7 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float h = hk[nt][i] + c1r[hg][nt][i & 1];
-                    const float sg = sigmoid_f(h);
-                    ak[nt][i] = h * sg;
-                    sp[hg][nt][i] = sg * (1.f + h * (1.f - sg));
+                    act_d<ACT>(hk[nt][i] + c1r[hg][nt][i & 1], ak[nt][i], sp[hg][nt][i]);
                 }
             akp[hg][0] = pack_bf16(ak[0][0], ak[0][1]);  // (tok 0-7, hidden 0-7 of the group)
             akp[hg][1] = pack_bf16(ak[0][2], ak[0][3]);  // (tok 8-15, hidden 0-7)
@@ -1037,8 +1059,7 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float h = hq[nt][i] + c1r[hg][nt][i & 1];
-                        aq[hg][nt][i] = h * sigmoid_f(h);
+                        aq[hg][nt][i] = act<ACT>(hq[nt][i] + c1r[hg][nt][i & 1]);
                     }
                 stsm_x4(AQ + rowA * C::AR + (32 * w + 16 * hg + colA) * 2, pack_bf16(aq[hg][0][0], aq[hg][0][1]),
                         pack_bf16(aq[hg][0][2], aq[hg][0][3]), pack_bf16(aq[hg][1][0], aq[hg][1][1]),
@@ -1170,7 +1191,8 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
 static int launch_mlp_w8(const MlpArgs &a, const CUtensorMap *maps)
 {
     using C = W8Cfg;
-    if (cudaFuncSetAttribute(ttt_mlp_w8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    auto kern = a.act ? ttt_mlp_w8_kernel<1> : ttt_mlp_w8_kernel<0>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return -4;
     MlpParams p;
     p.H = a.H;
@@ -1190,7 +1212,7 @@ static int launch_mlp_w8(const MlpArgs &a, const CUtensorMap *maps)
     p.W2o = a.W2o;
     p.c2o = a.c2o;
     p.status = a.status;
-    ttt_mlp_w8_kernel<<<a.B * a.H, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
+    kern<<<a.B * a.H, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
@@ -1221,6 +1243,7 @@ struct FbmCfg {
 };
 static_assert(FbmCfg::SMEM <= 227 * 1024, "shared memory");
 
+template <int ACT>
 __global__ void __launch_bounds__(FbmCfg::THREADS, 1)
     ttt_mlp_fb_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const MlpParams p)
@@ -1401,10 +1424,7 @@ __global__ void __launch_bounds__(FbmCfg::THREADS, 1)
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float h = hk[nt][i] + c1s[hg][nt][i & 1];
-                        const float sg = sigmoid_f(h);
-                        ak[nt][i] = h * sg;
-                        sp[hg][nt][i] = sg * (1.f + h * (1.f - sg));
+                        act_d<ACT>(hk[nt][i] + c1s[hg][nt][i & 1], ak[nt][i], sp[hg][nt][i]);
                     }
                 akp[hg][0] = pack_bf16(ak[0][0], ak[0][1]);
                 akp[hg][1] = pack_bf16(ak[0][2], ak[0][3]);
@@ -1523,8 +1543,7 @@ __global__ void __launch_bounds__(FbmCfg::THREADS, 1)
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float h = hq[nt][i] + c1r[hg][nt][i & 1];
-                        aq[nt][i] = h * sigmoid_f(h);
+                        aq[nt][i] = act<ACT>(hq[nt][i] + c1r[hg][nt][i & 1]);
                     }
                 stsm_x4(AX + rowA * C::AR + (32 * w + 16 * hg + colA) * 2, pack_bf16(aq[0][0], aq[0][1]),
                         pack_bf16(aq[0][2], aq[0][3]), pack_bf16(aq[1][0], aq[1][1]), pack_bf16(aq[1][2], aq[1][3]));
@@ -1592,7 +1611,8 @@ __global__ void __launch_bounds__(FbmCfg::THREADS, 1)
 static int launch_mlp_fb(const MlpArgs &a, const CUtensorMap *maps)
 {
     using C = FbmCfg;
-    if (cudaFuncSetAttribute(ttt_mlp_fb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    auto kern = a.act ? ttt_mlp_fb_kernel<1> : ttt_mlp_fb_kernel<0>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return -4;
     MlpParams p;
     p.H = a.H;
@@ -1612,7 +1632,7 @@ static int launch_mlp_fb(const MlpArgs &a, const CUtensorMap *maps)
     p.W2o = a.W2o;
     p.c2o = a.c2o;
     p.status = a.status;
-    ttt_mlp_fb_kernel<<<a.B * a.H, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
+    kern<<<a.B * a.H, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

@@ -123,7 +123,7 @@ int launch_linear_f32(const LinearArgs &a)
 namespace {
 
 struct MlpF32Params {
-    int H, T, d, m, b, causal, per_batch;
+    int H, T, d, m, b, causal, per_batch, act;  // act: 0 SiLU, 1 GELU (h Phi(h), erf form)
     const float *q, *k, *v, *eta;
     float eta_scalar;
     const float *W1, *c1, *W2, *c2;
@@ -132,13 +132,29 @@ struct MlpF32Params {
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
 
+// act(h) and act'(h) of the inner MLP
+__device__ __forceinline__ float act_f32(int act, float h)
+{
+    return act ? h * (0.5f + 0.5f * erff(h * 0.70710678118654752f)) : h * sigmoidf_(h);
+}
+
+__device__ __forceinline__ float act_d_f32(int act, float h)
+{
+    if (act) {
+        const float Phi = 0.5f + 0.5f * erff(h * 0.70710678118654752f);
+        return Phi + h * 0.39894228040143268f * expf(-0.5f * h * h);
+    }
+    const float sg = sigmoidf_(h);
+    return sg * (1.f + h * (1.f - sg));
+}
+
 // floats of shared memory used by the fp32 MLP kernel
 __host__ __device__ inline size_t mlp_f32_floats(int d, int m)
 {
     return 2 * ((size_t)d * m + m + (size_t)m * d + d) + 4 * (size_t)m + 4 * (size_t)d;
 }
 
-// z = SiLU(x W1 + c1) W2 + c2 for the query in xq; hbuf (m) is scratch
+// z = act(x W1 + c1) W2 + c2 for the query in xq; hbuf (m) is scratch
 __device__ void mlp_query(const MlpF32Params &p, const float *xq, const float *W1, const float *c1,
                           const float *W2, const float *c2, float *hbuf, float *zrow)
 {
@@ -146,7 +162,7 @@ __device__ void mlp_query(const MlpF32Params &p, const float *xq, const float *W
     for (int j = tid; j < m; j += blockDim.x) {
         float s = c1[j];
         for (int i = 0; i < d; ++i) s = fmaf(xq[i], W1[i * m + j], s);
-        hbuf[j] = s * sigmoidf_(s);
+        hbuf[j] = act_f32(p.act, s);
     }
     __syncthreads();
     for (int j = tid; j < d; j += blockDim.x) {
@@ -197,7 +213,7 @@ __global__ void __launch_bounds__(kThreads) ttt_mlp_f32_kernel(const MlpF32Param
                 float s = c1s[j];
                 for (int i = 0; i < d; ++i) s = fmaf(kk[i], W1s[i * m + j], s);
                 hh[j] = s;
-                aa[j] = s * sigmoidf_(s);
+                aa[j] = act_f32(p.act, s);
             }
             __syncthreads();
             for (int j = tid; j < d; j += nt) {
@@ -206,11 +222,10 @@ __global__ void __launch_bounds__(kThreads) ttt_mlp_f32_kernel(const MlpF32Param
                 ee[j] = s - vv[j];
             }
             __syncthreads();
-            for (int i = tid; i < m; i += nt) {  // g = (e W2s^T) * SiLU'(h)
+            for (int i = tid; i < m; i += nt) {  // g = (e W2s^T) * act'(h)
                 float s = 0.f;
                 for (int j = 0; j < d; ++j) s = fmaf(ee[j], W2s[i * d + j], s);
-                const float sg = sigmoidf_(hh[i]);
-                gg[i] = s * sg * (1.f + hh[i] * (1.f - sg));
+                gg[i] = s * act_d_f32(p.act, hh[i]);
             }
             __syncthreads();
             const float et = p.eta ? p.eta[(size_t)bh * T + t] : p.eta_scalar;
@@ -258,6 +273,7 @@ int launch_mlp_f32(const MlpArgs &a)
     p.b = a.b;
     p.causal = a.causal;
     p.per_batch = a.per_batch;
+    p.act = a.act;
     p.q = static_cast<const float *>(a.q);
     p.k = static_cast<const float *>(a.k);
     p.v = static_cast<const float *>(a.v);

@@ -79,7 +79,7 @@ def test_linear_rejects_bad_arguments(L):
 
 def _mlp(**kw):
     d = dict(B=1, H=1, T=32, d=64, m=256, mini_batch=16, causal=1, io_dtype=abi.TTT_BF16,
-             params_per_batch=0)
+             params_per_batch=0, activation=0)
     d.update(kw)
     return abi.MlpDesc(**d)
 
@@ -94,6 +94,7 @@ def test_mlp_rejects_bad_arguments(L):
     assert _call_mlp(L, _mlp(m=0)) == -1
     assert _call_mlp(L, _mlp(), c1=None) == -1
     assert _call_mlp(L, _mlp(params_per_batch=3)) == -1
+    assert _call_mlp(L, _mlp(activation=2)) == -1
     assert _call_mlp(L, _mlp(d=128)) == -2
     assert _call_mlp(L, _mlp(m=40)) == -2
     assert _call_mlp(L, _mlp(), q=FAKE + 4) == -3

@@ -137,3 +137,33 @@ def test_workload_vision_mlp_sampled():
     inp = G.synth.workload("vision_mlp")
     errs = _check(inp, chains=[0, 9, 1000, 1535])
     print("vision_mlp rel err z, W1, W2:", errs)
+
+
+# ----------------------------------------------------------- GELU inner model
+
+
+@pytest.mark.parametrize("d,b,causal,T,dtype", [
+    (64, 16, True, 150, torch.bfloat16),   # eight-warp kernel
+    (64, 16, False, 150, torch.bfloat16),
+    (64, 40, True, 150, torch.bfloat16),   # general kernel, mini-batches longer than 16 tokens
+    (32, 16, True, 100, torch.bfloat16),
+    (16, 5, False, 100, torch.bfloat16),
+    (64, 196, False, 196, torch.bfloat16),  # full-batch kernel
+    (16, 7, True, 40, torch.float32),       # fp32 path
+])
+def test_gelu_inner_model(d, b, causal, T, dtype):
+    """f(x) = GELU(x W1 + c1) W2 + c2 (the walkthrough's TTT-MLP, GELU in its erf
+    form), every MLP kernel, against the oracle with the same activation."""
+    import oracle
+    inp = _mlp_inputs(B=2, H=2, T=T, d=d, b=b, causal=causal, dtype=dtype, eta=0.05, seed=900 + d + b,
+                      bias=0.1)
+    dev = torch.device("cuda")
+    P = [inp.params[n] for n in ("W1", "c1", "W2", "c2")]
+    z, outs = abi.ttt_mlp_fwd(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), *[p.to(dev) for p in P], b,
+                              causal, eta_scalar=inp.eta_scalar, activation="gelu")
+    abi.ttt_sync_status()
+    zr, *Wr = oracle.mlp(inp.q, inp.k, inp.v, *P, b, causal, eta_scalar=inp.eta_scalar, activation="gelu")
+    assert np.isfinite(zr).all() and np.abs(zr).max() < 1e4
+    errs = [G.rel_err(z.double().cpu().numpy(), zr)]
+    errs += [G.rel_err(o.double().cpu().numpy(), r) for o, r in zip(outs, Wr) if np.abs(r).max() > 0]
+    assert max(errs) <= G.tol_for(inp), errs
