@@ -44,6 +44,8 @@ def _load():
         lib.ttt_oracle_mlp.argtypes = [i, i, i, i, i, i, i, dp, dp, dp, dp, d,
                                        dp, dp, dp, dp, i, dp, dp, dp, dp, dp, i, i]
         lib.ttt_oracle_mlp.restype = i
+        lib.ttt_oracle_dwconv.argtypes = [i, i, i, i, i, i, i, dp, dp, dp, dp, d, dp, ll, dp, dp, i]
+        lib.ttt_oracle_dwconv.restype = i
         _lib = lib
     return _lib
 
@@ -123,3 +125,29 @@ def mlp(q, k, v, W1, c1, W2, c2, b, causal=True, eta=None, eta_scalar=0.1, threa
     if rc != 0:
         raise ValueError("ttt_oracle_mlp rejected its arguments")
     return z, W1o, c1o, W2o, c2o
+
+
+def dwconv(q, k, v, W0, height, width, eta=None, eta_scalar=1.0, loss="mse", epochs=1,
+           threads=None):
+    """Depthwise 3x3 convolution inner model, full-batch inner GD (non-causal), fp64.
+    q,k,v: [B,H,N,d] with N = height*width tokens in row-major grid order; W0:
+    [H,9,d] (shared over the batch) or [B,H,9,d], tap o = (di+1)*3 + (dj+1).
+    Returns (z [B,H,N,d], W_final [B,H,9,d])."""
+    q, k, v, W0, eta = _f64(q), _f64(k), _f64(v), _f64(W0), _f64(eta)
+    B, H, N, d = q.shape
+    assert N == height * width and k.shape == q.shape and v.shape == q.shape
+    if W0.ndim == 3:
+        assert W0.shape == (H, 9, d)
+        w0_bstride = 0
+    else:
+        assert W0.shape == (B, H, 9, d)
+        w0_bstride = H * 9 * d
+    z = np.zeros((B, H, N, d))
+    Wf = np.zeros((B, H, 9, d))
+    rc = _load().ttt_oracle_dwconv(B, H, height, width, d, {"mse": 0, "dot": 1}[loss], int(epochs),
+                                   _ptr(q), _ptr(k), _ptr(v), _ptr(eta), float(eta_scalar),
+                                   _ptr(W0), w0_bstride, _ptr(z), _ptr(Wf),
+                                   threads or default_threads())
+    if rc != 0:
+        raise ValueError("ttt_oracle_dwconv rejected its arguments")
+    return z, Wf

@@ -329,3 +329,108 @@ int ttt_oracle_mlp(int B, int H, int T, int d, int m, int b, int causal,
     pthread_mutex_destroy(&J.lock);
     return 0;
 }
+
+/* ------------------------------------------------------- depthwise conv */
+/*
+ * Depthwise 3x3 convolution as the inner model (ViT3 article, observation 6: the
+ * inner model of vision TTT can be a small convolution; the ViT3 block uses a
+ * depthwise one).  The N = height * width tokens of a sequence are the pixels of a
+ * height x width grid in row-major order; f(X; W)[p][c] = sum over the 3 x 3
+ * offsets (di, dj) in {-1,0,1}^2 of X[p + (di, dj)][c] * W[(di+1)*3 + (dj+1)][c],
+ * with zero outside the grid (cross-correlation, "same" padding).  One full-batch
+ * inner step per epoch over all N tokens (observation 2), non-causal: every query
+ * reads the final W.  loss 0: l_p = 1/2 || f(K)[p] - v_p ||^2, gradient
+ * dW[o][c] = sum_p eta_p e[p][c] K[p + o][c] with e = f(K) - V at the epoch's start
+ * weights; loss 1: l_p = -f(K)[p] . v_p, e = -V.
+ * Layouts: q, k, v, z [B,H,N,d]; eta [B,H,N] or NULL; W0 [.., H, 9, d] with batch
+ * stride w0_bstride elements (0 = shared over the batch); W_out [B,H,9,d] or NULL.
+ */
+typedef struct {
+    int B, H, hh, ww, d, loss, epochs;
+    const double *q, *k, *v, *eta;
+    double eta_scalar;
+    const double *W0;
+    long long w0_bstride;
+    double *z, *W_out;
+    int next;
+    pthread_mutex_t lock;
+} dwconv_job;
+
+/* X[p + o][c] for offset o = (di+1)*3 + (dj+1), zero outside the grid */
+static double dw_tap(const double *X, int hh, int ww, int d, int p, int o, int c)
+{
+    const int y = p / ww + o / 3 - 1, x = p % ww + o % 3 - 1;
+    if (y < 0 || y >= hh || x < 0 || x >= ww) return 0.0;
+    return X[((size_t)y * ww + x) * d + c];
+}
+
+static void dwconv_chain(const dwconv_job *J, int bh)
+{
+    const int N = J->hh * J->ww, d = J->d, hh = J->hh, ww = J->ww;
+    const int bi = bh / J->H, hi = bh % J->H;
+    const double *q = J->q + (size_t)bh * N * d, *k = J->k + (size_t)bh * N * d;
+    const double *v = J->v + (size_t)bh * N * d;
+    const double *eta = J->eta ? J->eta + (size_t)bh * N : NULL;
+    double *W = malloc(sizeof(double) * 9 * d), *Ws = malloc(sizeof(double) * 9 * d);
+    double *e = malloc(sizeof(double) * (size_t)N * d);
+    memcpy(W, J->W0 + (size_t)bi * J->w0_bstride + (size_t)hi * 9 * d, sizeof(double) * 9 * d);
+    for (int ep = 0; ep < J->epochs; ++ep) {
+        memcpy(Ws, W, sizeof(double) * 9 * d);
+        for (int p = 0; p < N; ++p)
+            for (int c = 0; c < d; ++c) {
+                double f = 0.0;
+                if (J->loss == 0)
+                    for (int o = 0; o < 9; ++o) f += dw_tap(k, hh, ww, d, p, o, c) * Ws[o * d + c];
+                e[(size_t)p * d + c] = f - v[(size_t)p * d + c];
+            }
+        for (int o = 0; o < 9; ++o)
+            for (int c = 0; c < d; ++c) {
+                double g = 0.0;
+                for (int p = 0; p < N; ++p)
+                    g += (eta ? eta[p] : J->eta_scalar) * e[(size_t)p * d + c] * dw_tap(k, hh, ww, d, p, o, c);
+                W[o * d + c] -= g;
+            }
+    }
+    double *z = J->z + (size_t)bh * N * d;
+    for (int p = 0; p < N; ++p)
+        for (int c = 0; c < d; ++c) {
+            double s = 0.0;
+            for (int o = 0; o < 9; ++o) s += dw_tap(q, hh, ww, d, p, o, c) * W[o * d + c];
+            z[(size_t)p * d + c] = s;
+        }
+    if (J->W_out) memcpy(J->W_out + (size_t)bh * 9 * d, W, sizeof(double) * 9 * d);
+    free(W); free(Ws); free(e);
+}
+
+static void *dwconv_worker(void *arg)
+{
+    dwconv_job *J = (dwconv_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        const int bh = J->next++;
+        pthread_mutex_unlock(&J->lock);
+        if (bh >= J->B * J->H) break;
+        dwconv_chain(J, bh);
+    }
+    return NULL;
+}
+
+int ttt_oracle_dwconv(int B, int H, int hh, int ww, int d, int loss, int epochs,
+                      const double *q, const double *k, const double *v,
+                      const double *eta, double eta_scalar,
+                      const double *W0, long long w0_bstride,
+                      double *z, double *W_out, int nthreads)
+{
+    if (B < 0 || H < 0 || hh < 0 || ww < 0 || d <= 0 || epochs < 1 || !W0 || (loss != 0 && loss != 1) ||
+        (hh * ww > 0 && (!q || !k || !v || !z)))
+        return -1;
+    dwconv_job J = {B, H, hh, ww, d, loss, epochs, q, k, v, eta, eta_scalar, W0, w0_bstride, z, W_out, 0};
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads < 1) nthreads = 1;
+    pthread_t *th = malloc(sizeof(pthread_t) * nthreads);
+    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, dwconv_worker, &J);
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    return 0;
+}

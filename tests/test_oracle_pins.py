@@ -358,3 +358,61 @@ def test_empty_sequence():
     z, Wf = oracle.linear(q, q, q, W0, b=4)
     assert z.shape == (1, 1, 0, 4)
     np.testing.assert_array_equal(Wf[0], W0)
+
+
+# ------------------------------------------------ depthwise convolution inner model
+
+
+def _dw_torch(x, W, hh, ww):
+    """Depthwise 3x3 'same' cross-correlation of a [N,d] token map (row-major grid)
+    with taps W [9,d], by torch.nn.functional.conv2d (groups = d)."""
+    N, d = x.shape
+    img = x.T.reshape(1, d, hh, ww)
+    w = W.T.reshape(d, 1, 3, 3)
+    return torch.nn.functional.conv2d(img, w, padding=1, groups=d).reshape(d, N).T
+
+
+@pytest.mark.parametrize("epochs", [1, 2])
+@pytest.mark.parametrize("hh,ww", [(4, 5), (3, 3), (1, 6)])
+def test_dwconv_full_batch_steps_by_autograd(hh, ww, epochs):
+    """Depthwise-convolution inner model (ViT3 article, observation 6), full-batch
+    MSE steps: W_{e+1} = W_e - grad(sum_p eta_p 1/2 ||f(K)_p - v_p||^2) by autograd
+    through torch's grouped conv2d; every query reads the last W."""
+    B, H, d = 1, 2, 3
+    N = hh * ww
+    q, k, v = _qkv(B, H, N, d)
+    eta = rng.uniform(0.2, 1.0, (B, H, N))
+    W0 = rng.standard_normal((H, 9, d)) * 0.3
+    z, Wf = oracle.dwconv(q, k, v, W0, hh, ww, eta=eta, epochs=epochs)
+    for h in range(H):
+        W = torch.tensor(W0[h])
+        K, V, Q = (torch.tensor(x[0, h]) for x in (k, v, q))
+        for _ in range(epochs):
+            Wg = W.clone().requires_grad_(True)
+            L = (torch.tensor(eta[0, h])[:, None] * 0.5 * (_dw_torch(K, Wg, hh, ww) - V) ** 2).sum()
+            (g,) = torch.autograd.grad(L, Wg)
+            W = (Wg - g).detach()
+        np.testing.assert_allclose(Wf[0, h], W.numpy(), atol=1e-12)
+        np.testing.assert_allclose(z[0, h], _dw_torch(Q, W, hh, ww).numpy(), atol=1e-12)
+
+
+def test_dwconv_dot_loss_closed_form():
+    """Dot loss: W1[o][c] = W0[o][c] + eta sum_p v_p[c] K[p + o][c], written here with
+    explicit zero padding of the grid."""
+    B, H, hh, ww, d = 2, 1, 3, 4, 2
+    q, k, v = _qkv(B, H, hh * ww, d, unit=False)
+    W0 = rng.standard_normal((H, 9, d))
+    z, Wf = oracle.dwconv(q, k, v, W0, hh, ww, eta_scalar=0.5, loss="dot")
+    for bi in range(B):
+        Kp = np.zeros((hh + 2, ww + 2, d))
+        Kp[1:-1, 1:-1] = k[bi, 0].reshape(hh, ww, d)
+        V = v[bi, 0].reshape(hh, ww, d)
+        W = W0[0].copy()
+        for o in range(9):
+            di, dj = o // 3, o % 3
+            W[o] += 0.5 * (V * Kp[di:di + hh, dj:dj + ww]).sum((0, 1))
+        np.testing.assert_allclose(Wf[bi, 0], W, atol=1e-12)
+        Qp = np.zeros((hh + 2, ww + 2, d))
+        Qp[1:-1, 1:-1] = q[bi, 0].reshape(hh, ww, d)
+        Z = sum(Qp[o // 3:o // 3 + hh, o % 3:o % 3 + ww] * W[o] for o in range(9))
+        np.testing.assert_allclose(z[bi, 0], Z.reshape(hh * ww, d), atol=1e-12)
