@@ -56,6 +56,16 @@ def flops_per_token_head(inp):
     """Algorithmic FLOPs of one token-head (masked products counted exactly:
     (b+1)/2 visible pairs per token in a causal block of b)."""
     d, m, b = inp.d, inp.m, inp.b
+    o = inp.options
+    if inp.kind == "dwconv":
+        # per channel and epoch: residual 9 FMAs (none for the dot loss), gradient 9
+        # FMAs; output 9 FMAs
+        per_epoch = 18 * d + (18 * d if o.get("loss", "mse") == "mse" else 0)
+        return o.get("epochs", 1) * per_epoch + 18 * d
+    if inp.kind == "linear" and (o.get("loss") == "dot" or o.get("epochs", 1) > 1):
+        # dot loss: no K W product; epochs: the E / update pass repeats
+        upd = (2 if o.get("loss") == "dot" else 4) * d * d
+        return o.get("epochs", 1) * upd + 2 * d * d + (2 * (b + 1) * d if inp.causal else 0)
     if inp.kind == "linear":
         # E = K W, update K^T Et, Q W (2d^2 each); causal: masked (Q K^T) and its product
         # with Et over (b+1)/2 visible pairs (2d each); non-causal: Z = Q W_end
@@ -81,6 +91,8 @@ def bytes_per_launch(inp):
 
 def kernel_name(inp):
     """The kernel the library dispatches this workload to (mirrors the C ABI's choice)."""
+    if inp.kind == "dwconv":
+        return "ttt_dwconv_kernel"
     if inp.q.element_size() == 4:
         return "ttt_linear_f32_kernel" if inp.kind == "linear" else "ttt_mlp_f32_kernel"
     if inp.kind == "linear":
@@ -201,13 +213,27 @@ def run_ours(args, rank, world, inp, peaks):
             B, H, inp.T, d, inp.b, inp.causal, dtype=inp.q.dtype)
         ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
 
+        loss, epochs = inp.options.get("loss", "mse"), inp.options.get("epochs", 1)
+        if loss != "mse" or epochs != 1:
+            ws = None
+
         def step(qq=q, kk=k, vv=v, ee=eta, zz=z):
             if ws is not None:
                 abi.ttt_linear_fwd_seqpar(qq, kk, vv, params["W0"], inp.b, inp.causal, eta=ee,
                                           eta_scalar=inp.eta_scalar, z=zz, W_out=outs, workspace=ws)
             else:
                 abi.ttt_linear_fwd(qq, kk, vv, params["W0"], inp.b, inp.causal, eta=ee,
-                                   eta_scalar=inp.eta_scalar, z=zz, W_out=outs)
+                                   eta_scalar=inp.eta_scalar, z=zz, W_out=outs, loss=loss,
+                                   epochs=epochs)
+        out_bytes = [z, outs]
+    elif inp.kind == "dwconv":
+        outs = torch.empty((B, H, 9, d), device=dev)
+        o = inp.options
+
+        def step(qq=q, kk=k, vv=v, ee=eta, zz=z):
+            abi.ttt_dwconv_fwd(qq, kk, vv, params["W0"], o["height"], o["width"], eta=ee,
+                               eta_scalar=inp.eta_scalar, loss=o.get("loss", "mse"),
+                               epochs=o.get("epochs", 1), z=zz, W_out=outs)
         out_bytes = [z, outs]
     else:
         m = inp.m
@@ -216,7 +242,8 @@ def run_ours(args, rank, world, inp, peaks):
 
         def step(qq=q, kk=k, vv=v, ee=eta, zz=z):
             abi.ttt_mlp_fwd(qq, kk, vv, params["W1"], params["c1"], params["W2"], params["c2"],
-                            inp.b, inp.causal, eta=ee, eta_scalar=inp.eta_scalar, z=zz, outs=outs)
+                            inp.b, inp.causal, eta=ee, eta_scalar=inp.eta_scalar, z=zz, outs=outs,
+                            activation=inp.options.get("activation", "silu"))
         out_bytes = [z, *outs]
 
     flush_w = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -327,15 +354,20 @@ def oracle_sample(inp, budget_s):
         q, k, v = flat(inp.q), flat(inp.k), flat(inp.v)
         eta = flat(inp.eta) if inp.eta is not None else None
         t0 = time.perf_counter()
+        o = inp.options
         if inp.kind == "linear":
             W0 = torch.stack([inp.params["W0"][c % inp.H] for c in sel]).unsqueeze(0)
             oracle.linear(q, k, v, W0, inp.b, inp.causal, eta=eta, eta_scalar=inp.eta_scalar,
-                          threads=threads)
+                          threads=threads, loss=o.get("loss", "mse"), epochs=o.get("epochs", 1))
+        elif inp.kind == "dwconv":
+            W0 = torch.stack([inp.params["W0"][c % inp.H] for c in sel]).unsqueeze(0)
+            oracle.dwconv(q, k, v, W0, o["height"], o["width"], eta=eta, eta_scalar=inp.eta_scalar,
+                          loss=o.get("loss", "mse"), epochs=o.get("epochs", 1), threads=threads)
         else:
             P = [torch.stack([inp.params[nm][c % inp.H] for c in sel]).unsqueeze(0)
                  for nm in ("W1", "c1", "W2", "c2")]
             oracle.mlp(q, k, v, *P, inp.b, inp.causal, eta=eta, eta_scalar=inp.eta_scalar,
-                       threads=threads)
+                       threads=threads, activation=o.get("activation", "silu"))
         elapsed += time.perf_counter() - t0
         done += take
         n = min(2 * n, BH)
@@ -413,7 +445,7 @@ def main():
     tflops = flops / (ms * 1e-3) / 1e12
     nbytes = bytes_per_launch(inp)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    if inp.kind == "linear":
+    if inp.kind in ("linear", "dwconv"):  # arithmetic intensity below the ridge
         roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": gbs / peaks["hbm_gbs"]}
     else:

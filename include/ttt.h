@@ -201,6 +201,36 @@ ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc,
                        void *z, float *W1_out, float *c1_out, float *W2_out, float *c2_out,
                        void *stream);
 
+/* Depthwise-convolution TTT problem description. */
+typedef struct {
+    int B, H;                  /* batch, heads                                          */
+    int height, width;         /* token grid: N = height * width tokens per sequence,
+                                  row-major (token y * width + x)                       */
+    int d;                     /* channels per head, a multiple of 8                    */
+    ttt_dtype io_dtype;        /* dtype of q, k, v and z                                */
+    int loss;                  /* ttt_loss                                              */
+    int epochs;                /* full-batch inner steps, >= 1                          */
+    long long w0_batch_stride; /* 0: W0 is [H,9,d] shared over the batch; H*9*d: [B,H,9,d] */
+} ttt_dwconv_desc;
+
+/*
+ * TTT with a depthwise 3x3 convolution as the inner model, full-batch inner GD over
+ * all N tokens, non-causal (the ViT3 article, observation 6, a small convolution as
+ * the inner model of vision TTT, and observation 2, full-batch inner training):
+ *     f(X; W)[p][c] = sum_{o = (di+1)*3 + (dj+1), di, dj in {-1,0,1}} X[p + (di,dj)][c] W[o][c]
+ * on the token grid with zero padding.  Each epoch takes the gradient of
+ * sum_p eta_p l_p at the epoch's start taps and steps by it; z = f(q; W_final).
+ *   q, k, v, z : [B,H,N,d] io_dtype; eta: [B,H,N] fp32 or NULL (eta_scalar)
+ *   W0         : fp32 taps, see w0_batch_stride; W_out: [B,H,9,d] fp32 or NULL
+ * The sequence is held on chip: 2 N d sizeof(io) + 4 (9 d + N + 9 * 512) bytes must
+ * fit in 227 KB (bf16, d = 64: N <= 800), else TTT_ERR_UNSUPPORTED.  Pointers: q, k,
+ * v, z 16-byte aligned (TTT_ERR_ALIGN), fp32 arrays 4-byte aligned.
+ */
+ttt_status ttt_dwconv_fwd(const ttt_dwconv_desc *desc,
+                          const void *q, const void *k, const void *v,
+                          const float *eta, float eta_scalar,
+                          const float *W0, void *z, float *W_out, void *stream);
+
 /* Waits for `stream`, then reports (and clears) a kernel wait timeout recorded on
  * the current device, or a CUDA error seen while waiting. */
 ttt_status ttt_sync_status(void *stream);

@@ -21,7 +21,7 @@ STATUS = {0: "TTT_OK", -1: "TTT_ERR_ARG", -2: "TTT_ERR_UNSUPPORTED", -3: "TTT_ER
 
 # every symbol include/ttt.h declares
 EXPORTS = ("ttt_linear_fwd", "ttt_linear_seqpar_workspace", "ttt_linear_fwd_seqpar",
-           "ttt_linear_fwd_seqpar_noalloc",
+           "ttt_linear_fwd_seqpar_noalloc", "ttt_dwconv_fwd",
            "ttt_mlp_fwd", "ttt_sync_status", "ttt_status_str", "ttt_launch_count")
 
 
@@ -32,6 +32,13 @@ class LinearDesc(ctypes.Structure):
                 ("loss", ctypes.c_int), ("epochs", ctypes.c_int)]
 
 LOSSES = {"mse": 0, "dot": 1}
+
+
+class DwconvDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("height", ctypes.c_int),
+                ("width", ctypes.c_int), ("d", ctypes.c_int), ("io_dtype", ctypes.c_int),
+                ("loss", ctypes.c_int), ("epochs", ctypes.c_int),
+                ("w0_batch_stride", ctypes.c_longlong)]
 
 
 class MlpDesc(ctypes.Structure):
@@ -71,6 +78,8 @@ def lib():
         L.ttt_linear_fwd_seqpar_noalloc.argtypes = [ctypes.POINTER(LinearDesc), vp, vp, vp, fp, f, fp, vp,
                                                     fp, vp]
         L.ttt_linear_fwd_seqpar_noalloc.restype = ctypes.c_int
+        L.ttt_dwconv_fwd.argtypes = [ctypes.POINTER(DwconvDesc), vp, vp, vp, fp, f, fp, vp, fp, vp]
+        L.ttt_dwconv_fwd.restype = ctypes.c_int
         L.ttt_mlp_fwd.argtypes = [ctypes.POINTER(MlpDesc), vp, vp, vp, fp, f, fp, fp, fp, fp,
                                   vp, fp, fp, fp, fp, vp]
         L.ttt_mlp_fwd.restype = ctypes.c_int
@@ -212,6 +221,35 @@ def ttt_linear_fwd_seqpar_noalloc(q, k, v, W0, z, W_out, mini_batch, causal=True
                                              _stream(stream))
     if rc != 0:
         raise TTTError("ttt_linear_fwd_seqpar_noalloc", rc)
+    return z, W_out
+
+
+def ttt_dwconv_fwd(q, k, v, W0, height, width, eta=None, eta_scalar=1.0, loss="mse", epochs=1,
+                   z=None, W_out=None, want_W=True, stream=None):
+    """Depthwise 3x3 convolution inner model, full-batch inner GD.  q,k,v: [B,H,N,d]
+    with N = height*width tokens in row-major grid order; W0: fp32 taps [H,9,d] or
+    [B,H,9,d].  Returns (z, W_final [B,H,9,d] or None)."""
+    io = _check_tokens(q, k, v)
+    B, H, N, d = q.shape
+    if N != height * width:
+        raise ValueError("q has N tokens, the grid height*width")
+    W0 = _f32(W0, "W0")
+    eta = _f32(eta, "eta")
+    if W0.shape == (H, 9, d):
+        w0s = 0
+    elif W0.shape == (B, H, 9, d):
+        w0s = H * 9 * d
+    else:
+        raise ValueError("W0 must be [H,9,d] or [B,H,9,d]")
+    if z is None:
+        z = torch.empty_like(q)
+    if W_out is None and want_W:
+        W_out = torch.empty((B, H, 9, d), device=q.device, dtype=torch.float32)
+    desc = DwconvDesc(B, H, height, width, d, io, LOSSES[loss], int(epochs), w0s)
+    rc = lib().ttt_dwconv_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(eta),
+                              float(eta_scalar), _ptr(W0), _ptr(z), _ptr(W_out), _stream(stream))
+    if rc != 0:
+        raise TTTError("ttt_dwconv_fwd", rc)
     return z, W_out
 
 

@@ -333,6 +333,49 @@ ttt_status ttt_linear_fwd_seqpar_noalloc(const ttt_linear_desc *desc, const void
     return code(rc);
 }
 
+ttt_status ttt_dwconv_fwd(const ttt_dwconv_desc *desc, const void *q, const void *k, const void *v,
+                          const float *eta, float eta_scalar, const float *W0, void *z, float *W_out,
+                          void *stream)
+{
+    if (!desc) return TTT_ERR_ARG;
+    const ttt_dwconv_desc D = *desc;
+    if (D.B < 1 || D.H < 1 || D.height < 0 || D.width < 0 || D.d < 1 || D.epochs < 1 || !W0)
+        return TTT_ERR_ARG;
+    if (D.io_dtype != TTT_F32 && D.io_dtype != TTT_BF16) return TTT_ERR_ARG;
+    if (D.loss != TTT_LOSS_MSE && D.loss != TTT_LOSS_DOT) return TTT_ERR_ARG;
+    const long long N = (long long)D.height * D.width;
+    if (N > 0 && (!q || !k || !v || !z)) return TTT_ERR_ARG;
+    if (D.w0_batch_stride != 0 && D.w0_batch_stride != (long long)D.H * 9 * D.d) return TTT_ERR_ARG;
+    if (D.d % 8 != 0 || D.d > 512 || (long long)D.B * D.H > 0x7fffffffLL || N > (1 << 20))
+        return TTT_ERR_UNSUPPORTED;
+    if (ttt::dwconv_smem(D.height, D.width, D.d, D.io_dtype == TTT_BF16 ? 2 : 4) > 227 * 1024)
+        return TTT_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16)) return TTT_ERR_ALIGN;
+    if (!aligned(W0, 4) || !aligned(eta, 4) || !aligned(W_out, 4)) return TTT_ERR_ALIGN;
+    ttt::DwconvArgs a;
+    a.B = D.B;
+    a.H = D.H;
+    a.hh = D.height;
+    a.ww = D.width;
+    a.d = D.d;
+    a.loss = D.loss;
+    a.epochs = D.epochs;
+    a.bf16 = D.io_dtype == TTT_BF16;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.eta = eta;
+    a.eta_scalar = eta_scalar;
+    a.W0 = W0;
+    a.w0_bstride = D.w0_batch_stride;
+    a.z = z;
+    a.W_out = W_out;
+    a.stream = static_cast<cudaStream_t>(stream);
+    const int rc = ttt::launch_dwconv(a);
+    if (rc == 0) g_launches.fetch_add(1, std::memory_order_relaxed);
+    return code(rc);
+}
+
 ttt_status ttt_sync_status(void *stream)
 {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTT_ERR_LAUNCH;

@@ -34,6 +34,18 @@ struct MlpArgs {
     cudaStream_t stream;
 };
 
+struct DwconvArgs {
+    int B, H, hh, ww, d, loss, epochs, bf16;
+    const void *q, *k, *v;
+    const float *eta;
+    float eta_scalar;
+    const float *W0;
+    long long w0_bstride;
+    void *z;
+    float *W_out;
+    cudaStream_t stream;
+};
+
 // TMA descriptor of a bf16 token tensor viewed as [BH][T][d]: boxes of `rows`
 // tokens x `cols` features (0: min(d, 64)), swizzled to the box row length, rows
 // past T zero-filled on loads and dropped on stores.  Returns false if the driver
@@ -81,6 +93,11 @@ int launch_linear_seqpar(const LinearArgs &a, const SeqparPlan &pl, void *ws);
 // every segment's outputs in one launch (equal segments; seqpar_plan_serial).
 bool seqpar_plan_serial(const LinearArgs &a, SeqparPlan &pl);
 int launch_linear_seqpar_serial(const LinearArgs &a, const SeqparPlan &pl, void *ws);
+
+// Depthwise 3x3 convolution inner model (ttt_dwconv.cu): shared memory bytes of
+// one CTA and the launch.
+size_t dwconv_smem(int hh, int ww, int d, int es);
+int launch_dwconv(const DwconvArgs &a);
 
 // Largest d*m the fp32 MLP path holds on chip.
 bool mlp_f32_fits(int d, int m);

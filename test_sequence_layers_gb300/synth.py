@@ -39,6 +39,20 @@ WORKLOADS = {
     # full-batch non-causal vision variant (b = N = 196 tokens)
     "vision_linear": ("linear", 256, 6, 196, 64, 0, 196, False, torch.bfloat16, 1.0, 5),
     "vision_mlp": ("mlp", 256, 6, 196, 64, 256, 196, False, torch.bfloat16, 1.0, 6),
+    # variants of the pages' other inner losses, epochs, activations and models
+    "vision_linear_dot": ("linear", 256, 6, 196, 64, 0, 196, False, torch.bfloat16, 1.0, 8),
+    "vision_linear_3ep": ("linear", 256, 6, 196, 64, 0, 196, False, torch.bfloat16, 1.0, 9),
+    "mlp_125m_gelu": ("mlp", 8, 12, 2048, 64, 256, 16, True, torch.bfloat16, 0.1, 10),
+    "vision_dwconv": ("dwconv", 256, 6, 196, 64, 0, 196, False, torch.bfloat16, 1.0, 7),
+}
+
+# options beyond the base layer: inner loss ("dot"), inner epochs, MLP activation,
+# token grid of the convolution inner model
+OPTIONS = {
+    "vision_linear_dot": {"loss": "dot"},                   # the ViT3 block's inner loss
+    "vision_linear_3ep": {"epochs": 3},                     # several full-batch epochs
+    "mlp_125m_gelu": {"activation": "gelu"},                # the walkthrough's TTT-MLP
+    "vision_dwconv": {"height": 14, "width": 14, "loss": "dot"},  # ViT3: depthwise conv, dot loss
 }
 
 
@@ -58,6 +72,7 @@ class Inputs:
     eta: torch.Tensor | None   # [B,H,T] fp32 or None
     eta_scalar: float
     params: dict = field(default_factory=dict)   # fp32 CPU tensors: W0 | W1,c1,W2,c2
+    options: dict = field(default_factory=dict)  # loss, epochs, activation, height, width
 
     @property
     def token_heads(self) -> int:
@@ -92,6 +107,8 @@ def make(kind, B, H, T, d, b, causal, dtype=torch.bfloat16, eta=1.0, seed=0, m=0
         eta_t, eta_scalar = None, float(eta)
     if kind == "linear":
         params = {"W0": torch.randn((H, d, d), generator=g) * 0.02}
+    elif kind == "dwconv":  # nine taps per channel of a depthwise 3x3 convolution
+        params = {"W0": torch.randn((H, 9, d), generator=g) * 0.02}
     elif kind == "mlp":
         params = {"W1": torch.randn((H, d, m), generator=g) * 0.02,
                   "c1": torch.zeros((H, m)),
@@ -109,4 +126,6 @@ def workload(name, **override):
     kw = dict(kind=kind, B=B, H=H, T=T, d=d, m=m, b=b, causal=causal, dtype=dtype,
               eta=eta, seed=seed)
     kw.update(override)
-    return make(**kw)
+    inp = make(**kw)
+    inp.options = dict(OPTIONS.get(name, {}))
+    return inp

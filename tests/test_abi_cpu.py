@@ -121,3 +121,24 @@ def test_seqpar_rejects_bad_arguments_and_reports_no_workspace_without_gpu(L):
     assert L.ttt_linear_seqpar_workspace(None) == 0
     # no device visible: the call would not split, so no workspace is needed
     assert L.ttt_linear_seqpar_workspace(ctypes.byref(_lin(T=4096))) == 0
+
+
+def test_dwconv_rejects_bad_arguments(L):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+
+    def call(**kw):
+        d = dict(B=1, H=1, height=14, width=14, d=64, io_dtype=abi.TTT_BF16, loss=0, epochs=1,
+                 w0_batch_stride=0)
+        d.update(kw)
+        desc = abi.DwconvDesc(**d)
+        return L.ttt_dwconv_fwd(ctypes.byref(desc), vp(FAKE), vp(FAKE), vp(FAKE), None, 1.0,
+                                vp(FAKE), vp(FAKE), None, None)
+
+    assert L.ttt_dwconv_fwd(None, None, None, None, None, 1.0, None, None, None, None) == -1
+    assert call(B=0) == -1
+    assert call(epochs=0) == -1
+    assert call(loss=3) == -1
+    assert call(io_dtype=7) == -1
+    assert call(w0_batch_stride=5) == -1
+    assert call(d=12) == -2                      # channels must be a multiple of 8
+    assert call(height=64, width=64) == -2       # the sequence does not fit on chip
