@@ -39,7 +39,8 @@ def _load():
         lib = ctypes.CDLL(build())
         dp = ctypes.POINTER(ctypes.c_double)
         i, d, ll = ctypes.c_int, ctypes.c_double, ctypes.c_longlong
-        lib.ttt_oracle_linear.argtypes = [i, i, i, i, i, i, i, i, dp, dp, dp, dp, d, dp, ll, dp, dp, i]
+        lib.ttt_oracle_linear.argtypes = [i, i, i, i, i, i, i, i, dp, dp, dp, dp, d, dp, ll, dp, dp, i,
+                                          dp, dp, d]
         lib.ttt_oracle_linear.restype = i
         lib.ttt_oracle_mlp.argtypes = [i, i, i, i, i, i, i, dp, dp, dp, dp, d,
                                        dp, dp, dp, dp, i, dp, dp, dp, dp, dp, i, i]
@@ -69,11 +70,11 @@ def default_threads() -> int:
 
 
 def linear(q, k, v, W0, b, causal=True, eta=None, eta_scalar=1.0, loss="mse",
-           threads=None, epochs=1):
+           threads=None, epochs=1, ln_gamma=None, ln_beta=None, ln_eps=1e-6):
     """TTT-Linear forward, fp64.  q,k,v: [B,H,T,d]; W0: [H,d,d] (shared over the
     batch) or [B,H,d,d]; eta: [B,H,T] or None (then eta_scalar for every token);
     loss "mse" or "dot"; epochs > 1 only with causal=False and b >= T (repeated
-    full-batch steps).  Returns (z [B,H,T,d], W_final [B,H,d,d]) as float64 numpy
+    full-batch steps); ln_gamma, ln_beta [H,d]: inner model x + LN(x W) (MSE only).  Returns (z [B,H,T,d], W_final [B,H,d,d]) as float64 numpy
     arrays."""
     q, k, v, W0, eta = _f64(q), _f64(k), _f64(v), _f64(W0), _f64(eta)
     B, H, T, d = q.shape
@@ -88,11 +89,14 @@ def linear(q, k, v, W0, b, causal=True, eta=None, eta_scalar=1.0, loss="mse",
         assert eta.shape == (B, H, T)
     z = np.zeros((B, H, T, d))
     Wf = np.zeros((B, H, d, d))
+    gam, bet = _f64(ln_gamma), _f64(ln_beta)
+    if gam is not None:
+        assert gam.shape == (H, d) and bet.shape == (H, d)
     rc = _load().ttt_oracle_linear(B, H, T, d, int(b), 1 if causal else 0,
                                    {"mse": 0, "dot": 1}[loss], int(epochs),
                                    _ptr(q), _ptr(k), _ptr(v), _ptr(eta), float(eta_scalar),
                                    _ptr(W0), w0_bstride, _ptr(z), _ptr(Wf),
-                                   threads or default_threads())
+                                   threads or default_threads(), _ptr(gam), _ptr(bet), float(ln_eps))
     if rc != 0:
         raise ValueError("ttt_oracle_linear rejected its arguments")
     return z, Wf

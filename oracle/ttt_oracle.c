@@ -24,6 +24,13 @@
  *   causal = 0: every query of a block reads the W at the end of that block
  *   (b = T gives the single full-batch step of the vision variant, ViT3 article,
  *   observation 2).
+ *   norm (linear): f(x; W) = x + LN(x W), LN(y) = gamma * (y - mean(y)) /
+ *   sqrt(var(y) + eps) + beta over the d outputs (the walkthrough's TTT-Linear,
+ *   section 2.2.1: the inner model always carries a layer norm and a residual
+ *   connection); gamma, beta per head are inputs, not trained by the inner step.
+ *   With e = f(k; Ws) - v, yh = (y - mean) / s (s = sqrt(var + eps)) and
+ *   g = gamma * e, the gradient is dW = k^T dy with
+ *   dy = (g - mean(g) - yh * mean(g * yh)) / s.
  *   epochs (linear, causal = 0 with one block b >= T only): the block's gradient
  *   step is taken `epochs` times, each pass with its gradients at the W the
  *   previous pass left, before the queries read W (the ViT3 article, observation
@@ -68,9 +75,47 @@ typedef struct {
     const double *W0;
     long long w0_bstride;
     double *z, *W_out;
+    const double *ln_gamma, *ln_beta;  /* [H][d] each, or NULL: no norm / residual */
+    double ln_eps;
     int next;               /* next (batch, head) chain to process */
     pthread_mutex_t lock;
 } linear_job;
+
+/* y -> LN(y) in place over d entries; returns s = sqrt(var + eps) and leaves the
+ * normalised values in yh */
+static double layer_norm(int d, const double *gamma, const double *beta, double eps, const double *y,
+                         double *yh, double *out)
+{
+    double mu = 0.0, var = 0.0;
+    for (int j = 0; j < d; ++j) mu += y[j];
+    mu /= d;
+    for (int j = 0; j < d; ++j) var += (y[j] - mu) * (y[j] - mu);
+    var /= d;
+    const double s = sqrt(var + eps);
+    for (int j = 0; j < d; ++j) {
+        yh[j] = (y[j] - mu) / s;
+        out[j] = gamma[j] * yh[j] + beta[j];
+    }
+    return s;
+}
+
+/* z_t = f(q_t; W): q_t W, or q_t + LN(q_t W) with the norm */
+static void linear_out(const linear_job *J, int hi, const double *qt, const double *W, double *zt,
+                       double *tmp, double *tmp2)
+{
+    const int d = J->d;
+    for (int j = 0; j < d; ++j) {
+        double s = 0.0;
+        for (int i = 0; i < d; ++i) s += qt[i] * W[i * d + j];
+        tmp[j] = s;
+    }
+    if (!J->ln_gamma) {
+        for (int j = 0; j < d; ++j) zt[j] = tmp[j];
+        return;
+    }
+    layer_norm(d, J->ln_gamma + (size_t)hi * d, J->ln_beta + (size_t)hi * d, J->ln_eps, tmp, tmp2, zt);
+    for (int j = 0; j < d; ++j) zt[j] += qt[j];
+}
 
 static void linear_chain(const linear_job *J, int bh)
 {
@@ -86,6 +131,8 @@ static void linear_chain(const linear_job *J, int bh)
     double *W = malloc(sizeof(double) * d * d);    /* running weights          */
     double *Ws = malloc(sizeof(double) * d * d);   /* block's gradient point   */
     double *e = malloc(sizeof(double) * d);
+    double *y = malloc(sizeof(double) * d), *yh = malloc(sizeof(double) * d);
+    double *ln = malloc(sizeof(double) * d);
     memcpy(W, W0, sizeof(double) * d * d);
 
     for (int n0 = 0; n0 < T; n0 += b) {
@@ -95,7 +142,27 @@ static void linear_chain(const linear_job *J, int bh)
         for (int t = n0; t < n1; ++t) {
             const double *kt = k + (size_t)t * d, *vt = v + (size_t)t * d;
             const double et = eta ? eta[t] : J->eta_scalar;
-            if (J->loss == 0) {
+            if (J->loss == 0 && J->ln_gamma) {
+                /* e = k_t + LN(k_t Ws) - v_t; the gradient w.r.t. y = k_t Ws
+                 * through the layer norm replaces e below */
+                const double *gam = J->ln_gamma + (size_t)hi * d, *bet = J->ln_beta + (size_t)hi * d;
+                for (int j = 0; j < d; ++j) {
+                    double s = 0.0;
+                    for (int i = 0; i < d; ++i) s += kt[i] * Ws[i * d + j];
+                    y[j] = s;
+                }
+                const double sd = layer_norm(d, gam, bet, J->ln_eps, y, yh, ln);
+                double mg = 0.0, mgy = 0.0;
+                for (int j = 0; j < d; ++j) {
+                    const double g = gam[j] * (kt[j] + ln[j] - vt[j]);
+                    mg += g;
+                    mgy += g * yh[j];
+                    e[j] = g;
+                }
+                mg /= d;
+                mgy /= d;
+                for (int j = 0; j < d; ++j) e[j] = (e[j] - mg - yh[j] * mgy) / sd;
+            } else if (J->loss == 0) {
                 /* e = k_t Ws - v_t */
                 for (int j = 0; j < d; ++j) {
                     double s = 0.0;
@@ -109,29 +176,14 @@ static void linear_chain(const linear_job *J, int bh)
             /* W -= eta_t k_t^T e */
             for (int i = 0; i < d; ++i)
                 for (int j = 0; j < d; ++j) W[i * d + j] -= et * kt[i] * e[j];
-            if (J->causal) {
-                const double *qt = q + (size_t)t * d;
-                for (int j = 0; j < d; ++j) {
-                    double s = 0.0;
-                    for (int i = 0; i < d; ++i) s += qt[i] * W[i * d + j];
-                    z[(size_t)t * d + j] = s;
-                }
-            }
+            if (J->causal) linear_out(J, hi, q + (size_t)t * d, W, z + (size_t)t * d, y, yh);
         }
         }  /* epochs */
-        if (!J->causal) {
-            for (int t = n0; t < n1; ++t) {
-                const double *qt = q + (size_t)t * d;
-                for (int j = 0; j < d; ++j) {
-                    double s = 0.0;
-                    for (int i = 0; i < d; ++i) s += qt[i] * W[i * d + j];
-                    z[(size_t)t * d + j] = s;
-                }
-            }
-        }
+        if (!J->causal)
+            for (int t = n0; t < n1; ++t) linear_out(J, hi, q + (size_t)t * d, W, z + (size_t)t * d, y, yh);
     }
     if (J->W_out) memcpy(J->W_out + (size_t)bh * d * d, W, sizeof(double) * d * d);
-    free(W); free(Ws); free(e);
+    free(W); free(Ws); free(e); free(y); free(yh); free(ln);
 }
 
 static void *linear_worker(void *arg)
@@ -151,14 +203,16 @@ int ttt_oracle_linear(int B, int H, int T, int d, int b, int causal, int loss, i
                       const double *q, const double *k, const double *v,
                       const double *eta, double eta_scalar,
                       const double *W0, long long w0_bstride,
-                      double *z, double *W_out, int nthreads)
+                      double *z, double *W_out, int nthreads,
+                      const double *ln_gamma, const double *ln_beta, double ln_eps)
 {
+    if ((ln_gamma == NULL) != (ln_beta == NULL) || (ln_gamma && loss != 0)) return -1;
     if (B < 0 || H < 0 || T < 0 || d <= 0 || b <= 0 || !W0 || (T > 0 && (!q || !k || !v || !z)))
         return -1;
     if (loss != 0 && loss != 1) return -1;
     if (epochs < 1 || (epochs > 1 && (causal || b < T))) return -1;
     linear_job J = {B, H, T, d, b, causal ? 1 : 0, loss, epochs, q, k, v, eta, eta_scalar,
-                    W0, w0_bstride, z, W_out, 0};
+                    W0, w0_bstride, z, W_out, ln_gamma, ln_beta, ln_eps, 0};
     pthread_mutex_init(&J.lock, NULL);
     if (nthreads < 1) nthreads = 1;
     pthread_t *th = malloc(sizeof(pthread_t) * nthreads);

@@ -22,6 +22,14 @@ def f_mlp(x, P):
     return silu_t(x @ W1 + c1) @ W2 + c2
 
 
+def make_f_linear_ln(gamma, beta, eps=1e-6):
+    """f(x; W) = x + LN(x W) with fixed scale / shift (torch's layer_norm)."""
+    def f(x, P):
+        y = x @ P[0]
+        return x + torch.nn.functional.layer_norm(y, (y.shape[-1],), gamma, beta, eps)
+    return f
+
+
 def f_mlp_gelu(x, P):
     W1, c1, W2, c2 = P
     return torch.nn.functional.gelu(x @ W1 + c1) @ W2 + c2

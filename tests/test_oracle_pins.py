@@ -416,3 +416,35 @@ def test_dwconv_dot_loss_closed_form():
         Qp[1:-1, 1:-1] = q[bi, 0].reshape(hh, ww, d)
         Z = sum(Qp[o // 3:o // 3 + hh, o % 3:o % 3 + ww] * W[o] for o in range(9))
         np.testing.assert_allclose(z[bi, 0], Z.reshape(hh * ww, d), atol=1e-12)
+
+
+# ---------------------------------------------- inner layer norm + residual (Linear)
+
+
+@pytest.mark.parametrize("T,b,causal", [(11, 1, True), (11, 4, True), (12, 4, False), (9, 9, False),
+                                        (10, 16, True)])
+def test_linear_layer_norm_residual_matches_definition_autograd(T, b, causal):
+    """f(x; W) = x + LN(x W) (the walkthrough's TTT-Linear, section 2.2.1): the
+    oracle's hand LN backward equals the layer's definition evaluated with torch's
+    layer_norm and autograd, every mini-batch size, both masks."""
+    B, H, d = 1, 2, 6
+    q, k, v = _qkv(B, H, T, d)
+    eta = rng.uniform(0.1, 1.0, (B, H, T))
+    W0 = rng.standard_normal((H, d, d)) * 0.3
+    gam = rng.uniform(0.5, 1.5, (H, d))
+    bet = rng.standard_normal((H, d)) * 0.1
+    z, Wf = oracle.linear(q, k, v, W0, b, causal=causal, eta=eta, ln_gamma=gam, ln_beta=bet)
+    t = lambda a: torch.tensor(a)
+    for h in range(H):
+        f = _defs.make_f_linear_ln(t(gam[h]), t(bet[h]))
+        zr, (Wr,) = _defs.definition_autograd(f, [t(W0[h])], t(q[0, h]), t(k[0, h]), t(v[0, h]),
+                                              t(eta[0, h]), b, causal)
+        np.testing.assert_allclose(z[0, h], zr.numpy(), rtol=1e-10, atol=1e-11)
+        np.testing.assert_allclose(Wf[0, h], Wr.numpy(), rtol=1e-10, atol=1e-11)
+
+
+def test_linear_layer_norm_needs_mse():
+    q, k, v = _qkv(1, 1, 4, 4)
+    with pytest.raises(ValueError):
+        oracle.linear(q, k, v, np.zeros((1, 4, 4)), 2, loss="dot", ln_gamma=np.ones((1, 4)),
+                      ln_beta=np.zeros((1, 4)))
