@@ -62,6 +62,10 @@ def flops_per_token_head(inp):
         # FMAs; output 9 FMAs
         per_epoch = 18 * d + (18 * d if o.get("loss", "mse") == "mse" else 0)
         return o.get("epochs", 1) * per_epoch + 18 * d
+    if inp.kind == "linear" and o.get("ln"):
+        # plus the inner norm: statistics, normalisation and its backward on k W (about
+        # 12 d) and on q W (about 6 d)
+        return 6 * d * d + (2 * (b + 1) * d if inp.causal else 0) + 18 * d
     if inp.kind == "linear" and (o.get("loss") == "dot" or o.get("epochs", 1) > 1):
         # dot loss: no K W product; epochs: the E / update pass repeats
         upd = (2 if o.get("loss") == "dot" else 4) * d * d
@@ -214,7 +218,7 @@ def run_ours(args, rank, world, inp, peaks):
         ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
 
         loss, epochs = inp.options.get("loss", "mse"), inp.options.get("epochs", 1)
-        if loss != "mse" or epochs != 1:
+        if loss != "mse" or epochs != 1 or "ln_gamma" in params:
             ws = None
 
         def step(qq=q, kk=k, vv=v, ee=eta, zz=z):
@@ -224,7 +228,8 @@ def run_ours(args, rank, world, inp, peaks):
             else:
                 abi.ttt_linear_fwd(qq, kk, vv, params["W0"], inp.b, inp.causal, eta=ee,
                                    eta_scalar=inp.eta_scalar, z=zz, W_out=outs, loss=loss,
-                                   epochs=epochs)
+                                   epochs=epochs, ln_gamma=params.get("ln_gamma"),
+                                   ln_beta=params.get("ln_beta"))
         out_bytes = [z, outs]
     elif inp.kind == "dwconv":
         outs = torch.empty((B, H, 9, d), device=dev)
@@ -357,8 +362,12 @@ def oracle_sample(inp, budget_s):
         o = inp.options
         if inp.kind == "linear":
             W0 = torch.stack([inp.params["W0"][c % inp.H] for c in sel]).unsqueeze(0)
+            ln = {}
+            if "ln_gamma" in inp.params:
+                ln = {"ln_gamma": torch.stack([inp.params["ln_gamma"][c % inp.H] for c in sel]),
+                      "ln_beta": torch.stack([inp.params["ln_beta"][c % inp.H] for c in sel])}
             oracle.linear(q, k, v, W0, inp.b, inp.causal, eta=eta, eta_scalar=inp.eta_scalar,
-                          threads=threads, loss=o.get("loss", "mse"), epochs=o.get("epochs", 1))
+                          threads=threads, loss=o.get("loss", "mse"), epochs=o.get("epochs", 1), **ln)
         elif inp.kind == "dwconv":
             W0 = torch.stack([inp.params["W0"][c % inp.H] for c in sel]).unsqueeze(0)
             oracle.dwconv(q, k, v, W0, o["height"], o["width"], eta=eta, eta_scalar=inp.eta_scalar,

@@ -87,6 +87,16 @@ typedef struct {
                                   and mini_batch >= T, every query reading the last W;
                                   bf16 supports it for d = 64, T <= 256
                                   (TTT_ERR_UNSUPPORTED otherwise)                       */
+    const float *ln_gamma;     /* inner layer norm + residual: f(x) = x + LN(x W) with
+                                  LN(y) = ln_gamma * (y - mean) / sqrt(var + ln_eps)
+                                  + ln_beta over the d outputs ("Learning to (Learn at
+                                  Test Time)" walkthrough, section 2.2.1); [H,d] fp32
+                                  device arrays, fixed (not trained by the inner step),
+                                  or both NULL for f(x) = x W.  MSE loss and one epoch
+                                  only; bf16 needs mini_batch 16 and d <= 64
+                                  (TTT_ERR_UNSUPPORTED otherwise)                       */
+    const float *ln_beta;
+    float ln_eps;              /* > 0 when the norm is used (1e-6 in the paper's code)  */
 } ttt_linear_desc;
 
 /*

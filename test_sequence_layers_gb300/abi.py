@@ -29,7 +29,8 @@ class LinearDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
                 ("d", ctypes.c_int), ("mini_batch", ctypes.c_int), ("causal", ctypes.c_int),
                 ("io_dtype", ctypes.c_int), ("w0_batch_stride", ctypes.c_longlong),
-                ("loss", ctypes.c_int), ("epochs", ctypes.c_int)]
+                ("loss", ctypes.c_int), ("epochs", ctypes.c_int),
+                ("ln_gamma", ctypes.c_void_p), ("ln_beta", ctypes.c_void_p), ("ln_eps", ctypes.c_float)]
 
 LOSSES = {"mse": 0, "dot": 1}
 
@@ -129,11 +130,13 @@ def _f32(t, name):
 
 
 def ttt_linear_fwd(q, k, v, W0, mini_batch, causal=True, eta=None, eta_scalar=1.0,
-                   z=None, W_out=None, want_W=True, stream=None, loss="mse", epochs=1):
+                   z=None, W_out=None, want_W=True, stream=None, loss="mse", epochs=1,
+                   ln_gamma=None, ln_beta=None, ln_eps=1e-6):
     """TTT-Linear forward.  q,k,v: [B,H,T,d] bf16 or fp32 CUDA tensors; W0: fp32
     [H,d,d] (shared over the batch) or [B,H,d,d]; eta: fp32 [B,H,T] or None;
     loss "mse" or "dot"; epochs > 1: repeated full-batch steps (causal=False,
-    mini_batch >= T).  Returns (z, W_final or None)."""
+    mini_batch >= T); ln_gamma, ln_beta: fp32 [H,d] for the inner model
+    x + LN(x W).  Returns (z, W_final or None)."""
     io = _check_tokens(q, k, v)
     B, H, T, d = q.shape
     W0 = _f32(W0, "W0")
@@ -148,8 +151,9 @@ def ttt_linear_fwd(q, k, v, W0, mini_batch, causal=True, eta=None, eta_scalar=1.
         z = torch.empty_like(q)
     if W_out is None and want_W:
         W_out = torch.empty((B, H, d, d), device=q.device, dtype=torch.float32)
+    ln_gamma, ln_beta = _f32(ln_gamma, "ln_gamma"), _f32(ln_beta, "ln_beta")
     desc = LinearDesc(B, H, T, d, int(mini_batch), 1 if causal else 0, io, w0s, LOSSES[loss],
-                      int(epochs))
+                      int(epochs), _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps))
     rc = lib().ttt_linear_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(eta),
                               float(eta_scalar), _ptr(W0), _ptr(z), _ptr(W_out), _stream(stream))
     if rc != 0:

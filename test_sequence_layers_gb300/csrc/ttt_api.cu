@@ -134,6 +134,10 @@ ttt_status linear_args(const ttt_linear_desc *desc, const void *q, const void *k
     if (D.loss != TTT_LOSS_MSE && D.loss != TTT_LOSS_DOT) return TTT_ERR_ARG;
     if (D.epochs < 0) return TTT_ERR_ARG;
     if (D.epochs > 1 && (D.causal || D.mini_batch < D.T)) return TTT_ERR_UNSUPPORTED;
+    const bool ln = D.ln_gamma || D.ln_beta;
+    if (ln && (!D.ln_gamma || !D.ln_beta || !(D.ln_eps > 0.f) || D.loss != TTT_LOSS_MSE)) return TTT_ERR_ARG;
+    if (ln && (!aligned(D.ln_gamma, 4) || !aligned(D.ln_beta, 4))) return TTT_ERR_ALIGN;
+    if (ln && D.epochs > 1) return TTT_ERR_UNSUPPORTED;
     const long long dd = (long long)D.d * D.d;
     if (D.w0_batch_stride != 0 && D.w0_batch_stride != (long long)D.H * dd) return TTT_ERR_ARG;
     if ((long long)D.B * D.H > 0x7fffffffLL) return TTT_ERR_UNSUPPORTED;
@@ -151,6 +155,9 @@ ttt_status linear_args(const ttt_linear_desc *desc, const void *q, const void *k
     a.causal = D.causal;
     a.loss = D.loss;
     a.epochs = D.epochs > 1 ? D.epochs : 1;
+    a.ln_gamma = ln ? D.ln_gamma : nullptr;
+    a.ln_beta = ln ? D.ln_beta : nullptr;
+    a.ln_eps = D.ln_eps;
     a.q = q;
     a.k = k;
     a.v = v;
@@ -169,7 +176,11 @@ ttt_status linear_args(const ttt_linear_desc *desc, const void *q, const void *k
 int launch_linear(const ttt::LinearArgs &a, ttt_dtype io)
 {
     int rc;
-    if (io == TTT_BF16) {
+    if (io == TTT_BF16 && a.ln_gamma) {  // inner norm: the b = 16 kernel only (one mini-batch of
+                                         // T <= 16 tokens is one of its chunks)
+        const bool b16 = a.b == 16 || (a.b == a.T && a.T < 16);
+        rc = (b16 && a.d <= 64) ? ttt::launch_linear_b16(a) : TTT_ERR_UNSUPPORTED;
+    } else if (io == TTT_BF16) {
         rc = ttt::launch_linear_fb(a);  // full-batch mini-batch: no serial chain
         if (rc == TTT_ERR_UNSUPPORTED && a.epochs == 1)  // repeated epochs: the full-batch kernel only
             rc = (a.b == 16 && a.d <= 64) ? ttt::launch_linear_b16(a) : ttt::launch_linear_bf16(a);
@@ -213,6 +224,7 @@ size_t ttt_linear_seqpar_workspace(const ttt_linear_desc *desc)
     a.b = desc->mini_batch > desc->T ? desc->T : desc->mini_batch;
     a.loss = desc->loss;
     a.epochs = desc->epochs > 1 ? desc->epochs : 1;
+    a.ln_gamma = desc->ln_gamma;
     return ttt::seqpar_workspace_bytes(seqpar_plan_for(desc, a));
 }
 

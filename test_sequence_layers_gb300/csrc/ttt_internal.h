@@ -10,6 +10,8 @@ namespace ttt {
 struct LinearArgs {
     int B, H, T, d, b, causal;
     int loss = 0, epochs = 1;  // loss: 0 MSE, 1 negative dot product; inner GD steps per mini-batch
+    const float *ln_gamma = nullptr, *ln_beta = nullptr;  // inner norm [H][d] (null: f(x) = x W)
+    float ln_eps = 1e-6f;
     const void *q, *k, *v;
     const float *eta;
     float eta_scalar;

@@ -54,7 +54,8 @@ struct B16Cfg {
     static constexpr int SLOT = ((3 * BLK + 1023) / 1024) * 1024;  // Q, K, V of one block
     static constexpr int ETA_OFF = NB * SLOT;        // 64 fp32 per block
     static constexpr int BAR_OFF = ETA_OFF + NB * 256;
-    static constexpr int SMEM = BAR_OFF + 2 * NB * 8 + 1024;
+    static constexpr int RED_OFF = BAR_OFF + 2 * NB * 8;  // inner-norm partial sums [3][NCW][16] float2
+    static constexpr int SMEM = RED_OFF + 3 * NCW * 16 * 8 + 1024;
     static constexpr uint32_t SWM = RB == 128 ? 7u : (RB == 64 ? 3u : 1u);
 };
 
@@ -75,6 +76,8 @@ struct Frag {
     uint32_t qa[D / 16][4];  // Q as the A operand of Z = Q W
     uint32_t vv[2][2];       // V^T in accumulator layout
     float et[2][2];          // eta of tokens 8nt + 2t4 + i of the chunk
+    uint32_t kc[2][2];       // inner norm: K^T of this warp's columns in accumulator layout
+    uint32_t qz[4];          // inner norm: Q of this warp's columns in the layout of Z
 };
 
 enum { kRoleOut = 0, kRoleChain = 1, kRoleMap = 2 };
@@ -94,17 +97,47 @@ struct B16Params {
     int len0, seg_len, nseg, seg0, nsplit;  // nsplit: segments per chain in the whole pass
     float *Wst;   // [BH][nsplit-1][d][d] start weights of segments 1 .. nsplit-1
     float *maps;  // [BH][nsplit-2][2][d][d] affine maps A, B of segments 1 .. nsplit-2
+    const float *ln_gamma, *ln_beta;  // [H][d] inner norm scale / shift (VAR 2)
+    float ln_eps;
 };
+
+// Named barrier of the compute warps (the producer warp does not take part).
+__device__ __forceinline__ void bar_compute(int nthreads)
+{
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// The same barrier with an AND vote: true when every compute thread passed true.
+__device__ __forceinline__ bool bar_compute_and(int nthreads, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 
 // One unit (chain bh, segment seg) in role ROLE; the CTA has at least the role's
 // warps (extra warps leave after the barrier set-up).
-// DOT: the negative dot-product loss, whose residual is -V whatever W is (no
-// product K W on the chain).
-template <int D, int ROLE, bool DOT = false>
+// VAR 0: the MSE loss on f(x) = x W.  VAR 1 (DOT): the negative dot-product
+// loss, whose residual is -V whatever W is (no product K W on the chain).  VAR 2
+// (inner norm, output role only): f(x) = x + LN(x W); the per-token layer-norm
+// statistics over the d columns, which four warps hold 16 apiece, are summed
+// through shared memory with the compute warps' named barrier (forward statistics
+// and backward statistics on the chain, the output's statistics beside it), and the
+// block-boundary wait becomes a CTA-uniform vote so every warp meets every barrier.
+template <int D, int ROLE, int VAR = 0>
 __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMap *tk, const CUtensorMap *tv,
                                          const B16Params &p, const int bh, const int seg)
 {
     constexpr bool MAP = ROLE == kRoleMap, QSIDE = ROLE == kRoleOut;
+    constexpr bool DOT = VAR == 1, LN = VAR == 2;
+    static_assert(!LN || QSIDE, "the inner norm runs in the output role");
     using C = B16Cfg<D, MAP>;
     constexpr int NJ = C::NJ, NK = C::NK, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
@@ -206,6 +239,24 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
         offB[kk] = boff<D>(rowB, 16 * kk + colB);
     }
     const uint32_t offV = boff<D>(rowB, col0 + colB);
+    [[maybe_unused]] const uint32_t offQz = boff<D>(rowA, col0 + colA);
+    // inner norm scale / shift of this lane's columns: as rows of E^T (col0 + g,
+    // col0 + g + 8) and as columns of Z (col0 + 8hh + 2t4 + j)
+    [[maybe_unused]] float ge[2] = {}, be[2] = {}, gz[2][2] = {}, bz[2][2] = {};
+    if constexpr (LN) {
+        const float *gm = p.ln_gamma + (size_t)(bh % p.H) * D, *bt = p.ln_beta + (size_t)(bh % p.H) * D;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            ge[r] = gm[col0 + g + 8 * r];
+            be[r] = bt[col0 + g + 8 * r];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                gz[r][j] = gm[col0 + 8 * r + 2 * t4 + j];
+                bz[r][j] = bt[col0 + 8 * r + 2 * t4 + j];
+            }
+        }
+    }
+    float2 *const red = reinterpret_cast<float2 *>(gbase + C::RED_OFF);  // [3][NCW][16]
 
     // fragments of chunk (L, Q) from block slot L % NB (the block has landed)
     auto load = [&](auto qc, Frag<D> &F, int L) {
@@ -221,6 +272,10 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
             F.vv[0][0] = F.vv[0][1] = F.vv[1][0] = F.vv[1][1] = 0u;
         else
             ldsm_x4_t(st + 2 * C::BLK + offV, F.vv[0][0], F.vv[0][1], F.vv[1][0], F.vv[1][1]);
+        if constexpr (LN) {
+            ldsm_x4_t(st + C::BLK + offV, F.kc[0][0], F.kc[0][1], F.kc[1][0], F.kc[1][1]);
+            ldsm_x4(st + offQz, F.qz[0], F.qz[1], F.qz[2], F.qz[3]);
+        }
         if (has_eta) {
             const float *e = reinterpret_cast<const float *>(gbase + C::ETA_OFF + (L & (NB - 1)) * 256) +
                              16 * Q + 2 * t4;
@@ -243,6 +298,42 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
 
     bool next_ready = false;  // the next block has landed (tested in chunk 2 of a block)
 
+    // Inner norm: sums over all d columns of per-token partials (a, b).  Layout of E^T
+    // (this lane: tokens 8nt + 2t4 + j, two columns): reduce over the lanes of equal t4,
+    // then over the warps through shared-memory buffer `buf`.
+    [[maybe_unused]] auto tok_sums_e = [&](int buf, float (&a)[2][2], float (&b)[2][2]) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int m = 4; m < 32; m <<= 1) {
+                    a[nt][j] += __shfl_xor_sync(0xffffffffu, a[nt][j], m);
+                    b[nt][j] += __shfl_xor_sync(0xffffffffu, b[nt][j], m);
+                }
+        if (g == 0)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    red[(buf * C::NCW + w) * 16 + 8 * nt + 2 * t4 + j] = make_float2(a[nt][j], b[nt][j]);
+        bar_compute(C::NCW * 32);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float sa = 0.f, sb = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < C::NCW; ++ww) {
+                    const float2 v = red[(buf * C::NCW + ww) * 16 + 8 * nt + 2 * t4 + j];
+                    sa += v.x;
+                    sb += v.y;
+                }
+                a[nt][j] = sa;
+                b[nt][j] = sb;
+            }
+    };
+
     // one chunk (L, Q) on fragments F; fetches chunk (L, Q+1) or (L+1, 0) into Fn.
     // FULL: the chunk has 16 tokens (no bounds masks).  Returns false when there
     // is no next chunk (or a wait gave up).
@@ -258,7 +349,7 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
         constexpr bool ONE = true;
         float e[2][2][4] = {};
         [[maybe_unused]] float sc[2][4] = {}, zc[2][4] = {};
-        if constexpr (ONE) {
+        if constexpr (ONE && !LN) {  // (the inner norm takes V after the norm)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -292,10 +383,60 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
         } else if (more) {
             __syncwarp();
             if (lane == 0) mbar_arrive(blk_empty + 8 * (L & (NB - 1)));
-            if (!next_ready && !mbar_wait(blk_full + 8 * ((L + 1) & (NB - 1)), ((L + 1) / NB) & 1, p.status,
-                                          kSiteConsumerFull))
-                return false;
+            bool ok = next_ready || mbar_wait(blk_full + 8 * ((L + 1) & (NB - 1)), ((L + 1) / NB) & 1, p.status,
+                                              kSiteConsumerFull);
+            if constexpr (LN) ok = bar_compute_and(C::NCW * 32, ok);  // all warps go on, or none
+            if (!ok) return false;
             load(std::integral_constant<int, 0>{}, Fn, L + 1);
+        }
+        if constexpr (LN) {
+            // e currently holds Y^T = (K W)^T.  Forward statistics of each token's row.
+            float a[2][2], b[2][2], mu[2][2], rs[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float y0 = e[0][nt][j], y1 = e[0][nt][2 + j];
+                    a[nt][j] = y0 + y1;
+                    b[nt][j] = y0 * y0 + y1 * y1;
+                }
+            tok_sums_e(0, a, b);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    mu[nt][j] = a[nt][j] * (1.f / D);
+                    const float var = fmaxf(b[nt][j] * (1.f / D) - mu[nt][j] * mu[nt][j], 0.f);
+                    rs[nt][j] = rsqrtf(var + p.ln_eps);
+                }
+            // residual through the norm, e = k + LN(y) - v, and g = gamma e
+            float yh[2][4], gg[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = i >> 1, j = i & 1;
+                    yh[nt][i] = (e[0][nt][i] - mu[nt][j]) * rs[nt][j];
+                    const float kv = j ? bf16_hi(F.kc[nt][r]) : bf16_lo(F.kc[nt][r]);
+                    const float vv = j ? bf16_hi(F.vv[nt][r]) : bf16_lo(F.vv[nt][r]);
+                    gg[nt][i] = ge[r] * (kv + fmaf(ge[r], yh[nt][i], be[r]) - vv);
+                }
+            // backward statistics: means of g and g * yh over the row
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    a[nt][j] = gg[nt][j] + gg[nt][2 + j];
+                    b[nt][j] = gg[nt][j] * yh[nt][j] + gg[nt][2 + j] * yh[nt][2 + j];
+                }
+            tok_sums_e(1, a, b);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int j = i & 1;
+                    e[0][nt][i] = (gg[nt][i] - a[nt][j] * (1.f / D) - yh[nt][i] * (b[nt][j] * (1.f / D))) * rs[nt][j];
+                }
         }
         // -Et^T as an A fragment
         float ne[2][4];
@@ -338,6 +479,46 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
             mma_bf16(zc[1], pack_bf16(sm[0][0], sm[0][1]), pack_bf16(sm[0][2], sm[0][3]),
                      pack_bf16(sm[1][0], sm[1][1]), pack_bf16(sm[1][2], sm[1][3]), ea1, ea3);
         }
+        if constexpr (LN) {
+            // zc holds Q W_t: z = q + LN(q W_t) per token (rows g, g + 8 of Z)
+            float a[2], b[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                a[r] = zc[0][2 * r] + zc[0][2 * r + 1] + zc[1][2 * r] + zc[1][2 * r + 1];
+                b[r] = zc[0][2 * r] * zc[0][2 * r] + zc[0][2 * r + 1] * zc[0][2 * r + 1] +
+                       zc[1][2 * r] * zc[1][2 * r] + zc[1][2 * r + 1] * zc[1][2 * r + 1];
+#pragma unroll
+                for (int m = 1; m < 4; m <<= 1) {
+                    a[r] += __shfl_xor_sync(0xffffffffu, a[r], m);
+                    b[r] += __shfl_xor_sync(0xffffffffu, b[r], m);
+                }
+            }
+            if (t4 == 0)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) red[(2 * C::NCW + w) * 16 + g + 8 * r] = make_float2(a[r], b[r]);
+            bar_compute(C::NCW * 32);
+            float mu[2], rs[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                float sa = 0.f, sb = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < C::NCW; ++ww) {
+                    const float2 v = red[(2 * C::NCW + ww) * 16 + g + 8 * r];
+                    sa += v.x;
+                    sb += v.y;
+                }
+                mu[r] = sa * (1.f / D);
+                rs[r] = rsqrtf(fmaxf(sb * (1.f / D) - mu[r] * mu[r], 0.f) + p.ln_eps);
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = i >> 1, j = i & 1;
+                    const float qv = j ? bf16_hi(F.qz[2 * hh + r]) : bf16_lo(F.qz[2 * hh + r]);
+                    zc[hh][i] = qv + fmaf(gz[hh][j], (zc[hh][i] - mu[r]) * rs[r], bz[hh][j]);
+                }
+        }
         convert();
         if constexpr (QSIDE) {
             __nv_bfloat16 *zb = zlane + (size_t)t0 * D;
@@ -361,7 +542,10 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
                chunk(I3{}, fullc, FB, FA, L);
     };
 
-    if (nblk > 0 && mbar_wait(blk_full, 0, p.status, kSiteConsumerFull)) {
+    bool first = nblk > 0 && mbar_wait(blk_full, 0, p.status, kSiteConsumerFull);
+    if constexpr (LN)  // the chunks meet at named barriers: every compute warp starts, or none
+        if (nblk > 0) first = bar_compute_and(C::NCW * 32, first);
+    if (first) {
         Frag<D> FA, FB;
         load(std::integral_constant<int, 0>{}, FA, 0);
         for (int L = 0;; ++L) {  // two fragment sets alternate: no register copies
@@ -390,12 +574,12 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
 }
 
 // Output units: CTA u serves chain u / nseg, segment seg0 + u % nseg.
-template <int D, bool DOT>
+template <int D, int VAR>
 __global__ void __launch_bounds__(B16Cfg<D, false>::THREADS, 1)
     ttt_linear_b16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                           const __grid_constant__ CUtensorMap tv, const B16Params p)
 {
-    b16_unit<D, kRoleOut, DOT>(&tq, &tk, &tv, p, blockIdx.x / p.nseg, p.seg0 + blockIdx.x % p.nseg);
+    b16_unit<D, kRoleOut, VAR>(&tq, &tk, &tv, p, blockIdx.x / p.nseg, p.seg0 + blockIdx.x % p.nseg);
 }
 
 // The work before a split run's later segments: CTAs 0 .. BH-1 run the state chain
@@ -417,8 +601,10 @@ template <int D, bool PREP>
 int launch_b16_t(const LinearArgs &a, const B16Params &p, int units, const CUtensorMap *maps)
 {
     using C = B16Cfg<D, PREP>;
-    auto kern = PREP ? ttt_linear_b16_prep_kernel<D>
-                     : (a.loss ? ttt_linear_b16_kernel<D, true> : ttt_linear_b16_kernel<D, false>);
+    auto kern = PREP     ? ttt_linear_b16_prep_kernel<D>
+                : a.ln_gamma ? ttt_linear_b16_kernel<D, 2>
+                : a.loss     ? ttt_linear_b16_kernel<D, 1>
+                             : ttt_linear_b16_kernel<D, 0>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return -4;
     kern<<<units, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
@@ -445,6 +631,9 @@ B16Params b16_params(const LinearArgs &a)
     p.nsplit = 1;
     p.Wst = nullptr;
     p.maps = nullptr;
+    p.ln_gamma = a.ln_gamma;
+    p.ln_beta = a.ln_beta;
+    p.ln_eps = a.ln_eps;
     return p;
 }
 

@@ -119,7 +119,9 @@ double split_time(int len0, int len1, int nsplit)
 bool seqpar_plan(const LinearArgs &a, SeqparPlan &pl)
 {
     pl = SeqparPlan{};
-    if (a.b != 16 || (a.d != 16 && a.d != 32 && a.d != 64) || a.loss != 0 || a.epochs != 1) return false;
+    // (the inner norm makes a step non-affine in W: no maps)
+    if (a.b != 16 || (a.d != 16 && a.d != 32 && a.d != 64) || a.loss != 0 || a.epochs != 1 || a.ln_gamma)
+        return false;
     int dev = 0, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -199,7 +201,8 @@ int launch_linear_seqpar(const LinearArgs &a, const SeqparPlan &pl, void *ws)
 bool seqpar_plan_serial(const LinearArgs &a, SeqparPlan &pl)
 {
     pl = SeqparPlan{};
-    if (a.b != 16 || (a.d != 16 && a.d != 32 && a.d != 64) || a.loss != 0 || a.epochs != 1) return false;
+    if (a.b != 16 || (a.d != 16 && a.d != 32 && a.d != 64) || a.loss != 0 || a.epochs != 1 || a.ln_gamma)
+        return false;
     int dev = 0, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

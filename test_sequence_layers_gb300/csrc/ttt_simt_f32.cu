@@ -19,6 +19,8 @@ constexpr int kThreads = 256;
 
 struct LinF32Params {
     int H, T, d, b, causal, dot, epochs;  // dot: negative dot-product loss; epochs: passes per block
+    const float *ln_gamma, *ln_beta;      // inner norm f(x) = x + LN(x W), [H][d] (or null)
+    float ln_eps;
     const float *q, *k, *v, *eta;
     float eta_scalar;
     const float *W0;
@@ -26,11 +28,34 @@ struct LinF32Params {
     float *z, *W_out;
 };
 
+// mean and 1 / sqrt(var + eps) of the D values x (every calling thread reads all)
+__device__ __forceinline__ void row_stats(const float *x, int D, float eps, float &mu, float &rs)
+{
+    float s = 0.f, s2 = 0.f;
+    for (int i = 0; i < D; ++i) s += x[i];
+    mu = s / D;
+    for (int i = 0; i < D; ++i) s2 += (x[i] - mu) * (x[i] - mu);
+    rs = rsqrtf(s2 / D + eps);
+}
+
+// z = q + LN(y) for the row y (threads tid < D; y already in shared memory)
+__device__ __forceinline__ float ln_out(const LinF32Params &p, const float *gm, const float *bt, const float *y,
+                                        const float *qq, int D, int tid)
+{
+    float mu, rs;
+    row_stats(y, D, p.ln_eps, mu, rs);
+    return qq[tid] + fmaf(gm[tid], (y[tid] - mu) * rs, bt[tid]);
+}
+
 __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Params p)
 {
     extern __shared__ float sm[];
     const int D = p.d, T = p.T, tid = threadIdx.x;
     float *W = sm, *Ws = W + D * D, *kk = Ws + D * D, *vv = kk + D, *qq = vv + D, *ee = qq + D;
+    float *yh = ee + D, *gs = yh + D;  // inner norm scratch
+    const bool ln = p.ln_gamma != nullptr;
+    const float *gm = ln ? p.ln_gamma + (size_t)(blockIdx.x % p.H) * D : nullptr;
+    const float *bt = ln ? p.ln_beta + (size_t)(blockIdx.x % p.H) * D : nullptr;
     const int bh = blockIdx.x;
     const float *W0 = p.W0 + (size_t)(bh / p.H) * p.w0_bstride + (size_t)(bh % p.H) * D * D;
     for (int i = tid; i < D * D; i += blockDim.x) W[i] = W0[i];
@@ -51,23 +76,46 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
                 qq[tid] = q[(size_t)t * D + tid];
             }
             __syncthreads();
-            if (tid < D) {  // e = k_t W_start - v_t (dot loss: e = -v_t)
+            if (tid < D) {  // e = k_t W_start - v_t (dot loss: e = -v_t; norm: y = k_t W_start)
                 float s = 0.f;
                 if (!p.dot)
                     for (int i = 0; i < D; ++i) s = fmaf(kk[i], Ws[i * D + tid], s);
-                ee[tid] = s - vv[tid];
+                ee[tid] = ln ? s : s - vv[tid];
             }
             __syncthreads();
+            if (ln) {  // gradient through x + LN(y): dy = (g - mean g - yh mean(g yh)) / s, g = gamma e
+                float mu = 0.f, rs = 0.f;
+                if (tid < D) {
+                    row_stats(ee, D, p.ln_eps, mu, rs);
+                    yh[tid] = (ee[tid] - mu) * rs;
+                    gs[tid] = gm[tid] * (kk[tid] + fmaf(gm[tid], yh[tid], bt[tid]) - vv[tid]);
+                }
+                __syncthreads();
+                if (tid < D) {
+                    float mg = 0.f, mgy = 0.f;
+                    for (int i = 0; i < D; ++i) {
+                        mg += gs[i];
+                        mgy += gs[i] * yh[i];
+                    }
+                    ee[tid] = (gs[tid] - mg / D - yh[tid] * (mgy / D)) * rs;
+                }
+                __syncthreads();
+            }
             const float et = p.eta ? p.eta[(size_t)bh * T + t] : p.eta_scalar;
             for (int i = tid; i < D * D; i += blockDim.x)  // W -= eta k_t^T e
                 W[i] = fmaf(-et * kk[i / D], ee[i % D], W[i]);
             if (p.causal) {
                 __syncthreads();
+                float s = 0.f;
                 if (tid < D) {
-                    float s = 0.f;
                     for (int i = 0; i < D; ++i) s = fmaf(qq[i], W[i * D + tid], s);
-                    z[(size_t)t * D + tid] = s;
+                    if (ln) yh[tid] = s;
                 }
+                if (ln) {
+                    __syncthreads();
+                    if (tid < D) s = ln_out(p, gm, bt, yh, qq, D, tid);
+                }
+                if (tid < D) z[(size_t)t * D + tid] = s;
             }
         }
         }  // epochs
@@ -76,11 +124,16 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
                 __syncthreads();
                 if (tid < D) qq[tid] = q[(size_t)t * D + tid];
                 __syncthreads();
+                float s = 0.f;
                 if (tid < D) {
-                    float s = 0.f;
                     for (int i = 0; i < D; ++i) s = fmaf(qq[i], W[i * D + tid], s);
-                    z[(size_t)t * D + tid] = s;
+                    if (ln) yh[tid] = s;
                 }
+                if (ln) {
+                    __syncthreads();
+                    if (tid < D) s = ln_out(p, gm, bt, yh, qq, D, tid);
+                }
+                if (tid < D) z[(size_t)t * D + tid] = s;
             }
         }
     }
@@ -94,7 +147,7 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
 int launch_linear_f32(const LinearArgs &a)
 {
     const int D = a.d;
-    const size_t smem = sizeof(float) * (2 * D * D + 4 * D);
+    const size_t smem = sizeof(float) * (2 * D * D + 6 * D);
     if (cudaFuncSetAttribute(ttt_linear_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return -4;
@@ -106,6 +159,9 @@ int launch_linear_f32(const LinearArgs &a)
     p.causal = a.causal;
     p.dot = a.loss;
     p.epochs = a.epochs;
+    p.ln_gamma = a.ln_gamma;
+    p.ln_beta = a.ln_beta;
+    p.ln_eps = a.ln_eps;
     p.q = static_cast<const float *>(a.q);
     p.k = static_cast<const float *>(a.k);
     p.v = static_cast<const float *>(a.v);

@@ -44,6 +44,7 @@ WORKLOADS = {
     "vision_linear_3ep": ("linear", 256, 6, 196, 64, 0, 196, False, torch.bfloat16, 1.0, 9),
     "mlp_125m_gelu": ("mlp", 8, 12, 2048, 64, 256, 16, True, torch.bfloat16, 0.1, 10),
     "vision_dwconv": ("dwconv", 256, 6, 196, 64, 0, 196, False, torch.bfloat16, 1.0, 7),
+    "linear_125m_ln": ("linear", 8, 12, 2048, 64, 0, 16, True, torch.bfloat16, 1.0, 11),
 }
 
 # options beyond the base layer: inner loss ("dot"), inner epochs, MLP activation,
@@ -53,6 +54,7 @@ OPTIONS = {
     "vision_linear_3ep": {"epochs": 3},                     # several full-batch epochs
     "mlp_125m_gelu": {"activation": "gelu"},                # the walkthrough's TTT-MLP
     "vision_dwconv": {"height": 14, "width": 14, "loss": "dot"},  # ViT3: depthwise conv, dot loss
+    "linear_125m_ln": {"ln": True},                         # x + LN(x W): the walkthrough's TTT-Linear
 }
 
 
@@ -93,8 +95,10 @@ def _unit_rows(x):
     return x / x.norm(dim=-1, keepdim=True)
 
 
-def make(kind, B, H, T, d, b, causal, dtype=torch.bfloat16, eta=1.0, seed=0, m=0):
-    """Draw one input set.  ``eta`` is a float (constant) or "sigmoid"."""
+def make(kind, B, H, T, d, b, causal, dtype=torch.bfloat16, eta=1.0, seed=0, m=0, ln=False):
+    """Draw one input set.  ``eta`` is a float (constant) or "sigmoid"; ``ln`` adds
+    the inner layer norm's scale ~ 1 + N(0, 0.1^2) and shift ~ N(0, 0.1^2) per head
+    (drawn after the weights, so the other draws do not change)."""
     g = torch.Generator().manual_seed(seed)
     shape = (B, H, T, d)
     q = _unit_rows(_normal(shape, g)).to(dtype)
@@ -116,6 +120,9 @@ def make(kind, B, H, T, d, b, causal, dtype=torch.bfloat16, eta=1.0, seed=0, m=0
                   "c2": torch.zeros((H, d))}
     else:
         raise ValueError(kind)
+    if ln:
+        params["ln_gamma"] = 1.0 + 0.1 * torch.randn((H, d), generator=g)
+        params["ln_beta"] = 0.1 * torch.randn((H, d), generator=g)
     return Inputs(kind, B, H, T, d, m, b, bool(causal), q, k, v, eta_t, eta_scalar, params)
 
 
@@ -126,6 +133,7 @@ def workload(name, **override):
     kw = dict(kind=kind, B=B, H=H, T=T, d=d, m=m, b=b, causal=causal, dtype=dtype,
               eta=eta, seed=seed)
     kw.update(override)
+    kw.setdefault("ln", bool(OPTIONS.get(name, {}).get("ln", False)))
     inp = make(**kw)
     inp.options = dict(OPTIONS.get(name, {}))
     return inp

@@ -69,6 +69,12 @@ def test_linear_rejects_bad_arguments(L):
     assert _call_lin(L, _lin(epochs=-1)) == -1
     assert _call_lin(L, _lin(epochs=2)) == -2                     # causal
     assert _call_lin(L, _lin(epochs=2, causal=0, mini_batch=16)) == -2  # b < T
+    g = ctypes.c_void_p(FAKE)
+    assert _call_lin(L, _lin(ln_gamma=g)) == -1                          # scale without shift
+    assert _call_lin(L, _lin(ln_gamma=g, ln_beta=g, ln_eps=0.0)) == -1
+    assert _call_lin(L, _lin(ln_gamma=g, ln_beta=g, ln_eps=1e-6, loss=1)) == -1
+    assert _call_lin(L, _lin(ln_gamma=g, ln_beta=g, ln_eps=1e-6, causal=0, mini_batch=32,
+                             epochs=2)) == -2
     assert _call_lin(L, _lin(d=256)) == -2
     assert _call_lin(L, _lin(), q=FAKE + 8) == -3
     assert _call_lin(L, _lin(), z=FAKE + 2) == -3

@@ -218,3 +218,73 @@ def test_epochs_outside_the_full_batch_kernel_are_unsupported():
         abi.ttt_linear_fwd(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.params["W0"].to(dev), 64,
                            causal=False, epochs=2)
     assert e.value.code == -2
+
+
+# ------------------------------------------------- inner layer norm + residual
+
+
+def _check_ln(inp, tol=None, per_batch_w0=False, chains=None):
+    """GPU vs oracle for f(x; W) = x + LN(x W) (scale / shift from the inputs)."""
+    import oracle
+    from test_sequence_layers_gb300 import abi
+    tol = tol or G.tol_for(inp)
+    dev = torch.device("cuda")
+    W0 = inp.params["W0"]
+    if per_batch_w0:
+        W0 = W0.expand(inp.B, *W0.shape).contiguous()
+    gam, bet = inp.params["ln_gamma"], inp.params["ln_beta"]
+    eta = inp.eta.to(dev) if inp.eta is not None else None
+    z, W = abi.ttt_linear_fwd(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), W0.to(dev), inp.b, inp.causal,
+                              eta=eta, eta_scalar=inp.eta_scalar, ln_gamma=gam.to(dev), ln_beta=bet.to(dev))
+    abi.ttt_sync_status()
+    zg, Wg = z.double().cpu().numpy(), W.double().cpu().numpy()
+    if chains is None:
+        zr, Wr = oracle.linear(inp.q, inp.k, inp.v, W0, inp.b, inp.causal, eta=inp.eta,
+                               eta_scalar=inp.eta_scalar, ln_gamma=gam, ln_beta=bet)
+    else:
+        sel = lambda x: x.reshape(-1, *x.shape[2:])[chains].unsqueeze(0)
+        W0s = torch.stack([W0[c % inp.H] for c in chains]).unsqueeze(0)
+        gs = torch.stack([gam[c % inp.H] for c in chains])
+        bs = torch.stack([bet[c % inp.H] for c in chains])
+        zr, Wr = oracle.linear(sel(inp.q), sel(inp.k), sel(inp.v), W0s, inp.b, inp.causal,
+                               eta=sel(inp.eta) if inp.eta is not None else None,
+                               eta_scalar=inp.eta_scalar, ln_gamma=gs, ln_beta=bs)
+        zg, Wg = G.pick(zg, chains), G.pick(Wg, chains)
+    ez, eW = G.rel_err(zg, zr), G.rel_err(Wg, Wr)
+    assert ez <= tol and eW <= tol, (ez, eW, tol)
+    return ez, eW
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("T", [150, 64, 13])
+def test_inner_norm_bf16(d, causal, T):
+    """x + LN(x W) (the walkthrough's TTT-Linear) on the b = 16 kernel: several
+    blocks, a partial last block and a partial last mini-batch, per-token eta."""
+    inp = G.synth.make("linear", B=2, H=3, T=T, d=d, b=16, causal=causal, eta="sigmoid",
+                       seed=1400 + d + T, ln=True)
+    _check_ln(inp, per_batch_w0=(T == 64))
+
+
+@pytest.mark.parametrize("b,causal", [(16, True), (3, True), (20, False)])
+def test_inner_norm_fp32(b, causal):
+    inp = G.synth.make("linear", B=2, H=2, T=40, d=16, b=b, causal=causal, dtype=torch.float32,
+                       eta=0.5, seed=1500 + b, ln=True)
+    _check_ln(inp, tol=G.TOL_F32)
+
+
+def test_inner_norm_other_mini_batches_unsupported_in_bf16():
+    from test_sequence_layers_gb300 import abi
+    inp = G.synth.make("linear", B=1, H=1, T=40, d=64, b=5, causal=True, seed=1600, ln=True)
+    dev = torch.device("cuda")
+    with pytest.raises(abi.TTTError) as e:
+        abi.ttt_linear_fwd(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.params["W0"].to(dev), 5,
+                           ln_gamma=inp.params["ln_gamma"].to(dev), ln_beta=inp.params["ln_beta"].to(dev))
+    assert e.value.code == -2
+
+
+def test_workload_125m_inner_norm_full():
+    """B8 H12 T2048 d64 b16 causal with the inner norm: every chain."""
+    inp = G.synth.workload("linear_125m_ln")
+    ez, eW = _check_ln(inp)
+    print(f"linear_125m_ln rel err z {ez:.3e} W {eW:.3e}")
