@@ -302,21 +302,27 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
     // (this lane: tokens 8nt + 2t4 + j, two columns): reduce over the lanes of equal t4,
     // then over the warps through shared-memory buffer `buf`.
     [[maybe_unused]] auto tok_sums_e = [&](int buf, float (&a)[2][2], float (&b)[2][2]) {
+        // reduce-scatter over the 8 lanes of equal t4: value k = 4 nt + 2 j + stat ends in
+        // the lane whose bits (4, 3, 2) are the bits of k
+        float v[8];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < 2; ++j) {
+                v[4 * nt + 2 * j] = a[nt][j];
+                v[4 * nt + 2 * j + 1] = b[nt][j];
+            }
+        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+        float u[4], x[2];
 #pragma unroll
-                for (int m = 4; m < 32; m <<= 1) {
-                    a[nt][j] += __shfl_xor_sync(0xffffffffu, a[nt][j], m);
-                    b[nt][j] += __shfl_xor_sync(0xffffffffu, b[nt][j], m);
-                }
-        if (g == 0)
+        for (int i = 0; i < 4; ++i)
+            u[i] = (b4 ? v[4 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[4 + i], 16);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    red[(buf * C::NCW + w) * 16 + 8 * nt + 2 * t4 + j] = make_float2(a[nt][j], b[nt][j]);
+        for (int i = 0; i < 2; ++i)
+            x[i] = (b3 ? u[2 + i] : u[i]) + __shfl_xor_sync(0xffffffffu, b3 ? u[i] : u[2 + i], 8);
+        const float tot = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[1], 4);
+        float *redf = reinterpret_cast<float *>(red);
+        redf[((buf * C::NCW + w) * 16 + 8 * b4 + 2 * t4 + b3) * 2 + b2] = tot;
         bar_compute(C::NCW * 32);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -325,9 +331,9 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
                 float sa = 0.f, sb = 0.f;
 #pragma unroll
                 for (int ww = 0; ww < C::NCW; ++ww) {
-                    const float2 v = red[(buf * C::NCW + ww) * 16 + 8 * nt + 2 * t4 + j];
-                    sa += v.x;
-                    sb += v.y;
+                    const float2 t = red[(buf * C::NCW + ww) * 16 + 8 * nt + 2 * t4 + j];
+                    sa += t.x;
+                    sb += t.y;
                 }
                 a[nt][j] = sa;
                 b[nt][j] = sb;
@@ -388,6 +394,14 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
             if constexpr (LN) ok = bar_compute_and(C::NCW * 32, ok);  // all warps go on, or none
             if (!ok) return false;
             load(std::integral_constant<int, 0>{}, Fn, L + 1);
+        }
+        if constexpr (LN) {  // Z = Q W first: the tensor pipe works through the norm's exchanges
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                mma_bf16(zc[0], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk], wb[4 * kk + 2]);
+                mma_bf16(zc[1], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk + 1],
+                         wb[4 * kk + 3]);
+            }
         }
         if constexpr (LN) {
             // e currently holds Y^T = (K W)^T.  Forward statistics of each token's row.
@@ -461,7 +475,7 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
         if constexpr (QSIDE) {
             // Z = Q W + (mask .* S)(-Et), masked scores as an A fragment from registers
     #pragma unroll
-            for (int kk = 0; kk < NK; ++kk) {
+            for (int kk = 0; kk < NK && !LN; ++kk) {
                 mma_bf16(zc[0], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk], wb[4 * kk + 2]);
                 mma_bf16(zc[1], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], wb[4 * kk + 1],
                          wb[4 * kk + 3]);
