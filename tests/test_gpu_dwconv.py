@@ -59,6 +59,18 @@ def test_head_dims_and_epochs(d, epochs):
     _check(inp, 8, 10, epochs=epochs, per_batch=True)
 
 
+def test_largest_grid_on_chip():
+    """22 x 22 tokens at d = 64 in bf16: the largest square grid one CTA holds (the
+    padded fp32 grid, V and the partial sums); 23 x 23 is rejected."""
+    inp = G.synth.make("dwconv", B=1, H=2, T=484, d=64, b=484, causal=False, eta="sigmoid", seed=1150)
+    _check(inp, 22, 22, loss="mse")
+    big = G.synth.make("dwconv", B=1, H=1, T=529, d=64, b=529, causal=False, seed=1151)
+    dev = torch.device("cuda")
+    with pytest.raises(abi.TTTError) as e:
+        abi.ttt_dwconv_fwd(big.q.to(dev), big.k.to(dev), big.v.to(dev), big.params["W0"].to(dev), 23, 23)
+    assert e.value.code == -2
+
+
 def test_fp32_io():
     inp = G.synth.make("dwconv", B=1, H=2, T=42, d=32, b=42, causal=False, dtype=torch.float32,
                        eta="sigmoid", seed=1200)

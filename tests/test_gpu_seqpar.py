@@ -48,6 +48,18 @@ def test_segments_match_oracle(d, T):
     _check(inp)
 
 
+def test_more_than_two_segments_use_maps_and_scan():
+    """Two chains over 4096 tokens split into more than two segments: the workspace
+    holds affine maps (segments 1 .. P-2) besides the start weights, so the map role
+    and the scan run; the result still matches the oracle."""
+    d = 64
+    ws = abi.ttt_linear_seqpar_workspace(1, 2, 4096, d, 16)
+    start_weights_of_two = 2 * 1 * d * d * 4
+    assert ws > start_weights_of_two, ws
+    inp = G.synth.make("linear", B=1, H=2, T=4096, d=d, b=16, causal=True, eta="sigmoid", seed=560)
+    _check(inp)
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_segments_noncausal_and_per_batch_w0(causal):
     inp = G.synth.make("linear", B=2, H=3, T=1500, d=64, b=16, causal=causal, eta=1.0, seed=600 + causal)
