@@ -382,7 +382,9 @@ ttt_status ttt_dwconv_fwd(const ttt_dwconv_desc *desc, const void *q, const void
     a.w0_bstride = D.w0_batch_stride;
     a.z = z;
     a.W_out = W_out;
+    a.status = status_word();
     a.stream = static_cast<cudaStream_t>(stream);
+    if (!a.status) return TTT_ERR_LAUNCH;
     const int rc = ttt::launch_dwconv(a);
     if (rc == 0) g_launches.fetch_add(1, std::memory_order_relaxed);
     return code(rc);

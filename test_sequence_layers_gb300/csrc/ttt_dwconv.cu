@@ -16,13 +16,16 @@
 // CUDA cores: one CTA per (batch, head) holds K and V in shared memory in the I/O
 // type; each thread owns a pair of channels and a stride of positions, forms each
 // residual on the fly and accumulates the nine tap gradients in registers; the
-// per-thread partial sums are reduced through shared memory.  K (then Q) sits in
-// shared memory as fp32 in a zero-bordered grid, so the taps need no bounds tests,
-// and each thread walks whole rows with a 3 x 3 register window (three new taps per
-// position instead of nine).
+// per-thread partial sums are reduced through shared memory.  K and Q sit in
+// shared memory in zero-bordered grids (I/O type), so the taps need no bounds
+// tests; each thread walks whole rows with a 3 x 3 register window (three new taps
+// per position instead of nine).  All of a sequence's token copies (K, V, then Q)
+// are issued at the start as bulk asynchronous copies (one per grid row), so Q lands
+// while the epochs run; channel pairs use the paired fp32 FMA.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "ttt_device.cuh"
 #include "ttt_internal.h"
 
 namespace ttt {
@@ -39,6 +42,7 @@ struct DwParams {
     long long w0_bstride;
     void *z;
     float *W_out;
+    int *status;
 };
 
 template <typename TIO>
@@ -61,67 +65,73 @@ __device__ __forceinline__ void st2(TIO *p, float a, float b)
         *reinterpret_cast<float2 *>(p) = make_float2(a, b);
 }
 
-// shared memory: a zero-bordered (height+2) x (width+2) grid of fp32 tokens
-// (K, then Q), V [N][d] in the I/O type, taps W [9][d], eta [N], partial tap
-// gradients [parts][9][d]
+// shared memory: two mbarriers, two zero-bordered (height+2) x (width+2) token
+// grids in the I/O type (K, Q), V [N][d], taps W [9][d], partial tap gradients
+// [parts][9][d] (paired 8-byte accesses, so ahead of the odd-length eta), eta [N]
 __host__ __device__ inline size_t dw_smem_bytes(int hh, int ww, int d, int es)
 {
     const int parts = kDwThreads / (d / 2);
-    return 4 * (size_t)(hh + 2) * (ww + 2) * d + (size_t)hh * ww * d * es +
+    return 16 + 2 * (size_t)(hh + 2) * (ww + 2) * d * es + (size_t)hh * ww * d * es +
            4 * (9 * (size_t)d + (size_t)hh * ww + (size_t)parts * 9 * d);
 }
 
-// The tokens of one sequence into the interior of the padded fp32 grid (the border
-// is left as it is).  Every thread first issues all of its 16-byte loads, then
-// converts and stores, so the loads of a thread are in flight together.
-template <typename TIO>
-__device__ __forceinline__ void stage_grid(float *grid, const TIO *src, int hh, int ww, int d)
+// Untiled bulk copy global -> shared (both 16-byte aligned, bytes a multiple of
+// 16), completion counted on the mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
-    constexpr int EPV = 16 / sizeof(TIO);  // elements per 16-byte vector
-    const int nvec = hh * ww * d / EPV, vpr = d / EPV;  // vectors in all / per token
-    constexpr int U = 8;
-    for (int v0 = threadIdx.x; v0 < nvec; v0 += U * kDwThreads) {
-        uint4 buf[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int v = v0 + u * kDwThreads;
-            if (v < nvec) buf[u] = reinterpret_cast<const uint4 *>(src)[v];
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int v = v0 + u * kDwThreads;
-            if (v >= nvec) break;
-            const int tok = v / vpr, c = (v - tok * vpr) * EPV;
-            const int y = tok / ww, x = tok - y * ww;
-            float *dst = grid + ((size_t)(y + 1) * (ww + 2) + x + 1) * d + c;
-            if constexpr (sizeof(TIO) == 2) {
-                const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&buf[u]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 f = __bfloat1622float2(h[i]);
-                    dst[2 * i] = f.x;
-                    dst[2 * i + 1] = f.y;
-                }
-            } else {
-                *reinterpret_cast<uint4 *>(dst) = buf[u];
-            }
-        }
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// zero border (rows 0 and hh+1, columns 0 and ww+1) of a padded grid
+template <typename TIO>
+__device__ __forceinline__ void zero_border(TIO *grid, int hh, int ww, int d)
+{
+    const int gw = ww + 2;
+    for (int i = threadIdx.x; i < 2 * (gw + hh) * d; i += kDwThreads) {
+        const int cell = i / d, cc = i - cell * d;
+        int y, x;
+        if (cell < gw) { y = 0; x = cell; }
+        else if (cell < 2 * gw) { y = hh + 1; x = cell - gw; }
+        else { const int r = cell - 2 * gw; y = 1 + (r >> 1); x = (r & 1) ? ww + 1 : 0; }
+        grid[((size_t)y * gw + x) * d + cc] = TIO(0.f);
     }
 }
 
-template <typename TIO>
-__device__ __forceinline__ void stage_flat(TIO *dst, const TIO *src, int n_elem)
+// Walks output row y of a padded grid with a 3 x 3 window for channel pair c.
+// The window's columns rotate through three register triples (unrolled by three,
+// so no moves); step(x, a, b, n) gets the columns x, x+1, x+2 of padded rows
+// y .. y+2, i.e. tap (r, j) of output (y, x) is {a, b, n}[j][r].
+template <typename TIO, typename Step>
+__device__ __forceinline__ void walk_row(const TIO *g, int y, int ww, int d, int c, Step &&step)
 {
-    const int nv = n_elem * (int)sizeof(TIO) / 16;
-    constexpr int U = 8;
-    for (int v0 = threadIdx.x; v0 < nv; v0 += U * kDwThreads) {
-        uint4 buf[U];
+    const int gw = ww + 2;
+    float2 A[3], B[3], C[3];
+    auto col = [&](int xc, float2 (&cc)[3]) {
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (v0 + u * kDwThreads < nv) buf[u] = reinterpret_cast<const uint4 *>(src)[v0 + u * kDwThreads];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (v0 + u * kDwThreads < nv) reinterpret_cast<uint4 *>(dst)[v0 + u * kDwThreads] = buf[u];
+        for (int r = 0; r < 3; ++r) cc[r] = ld2(g + ((size_t)(y + r) * gw + xc) * d + c);
+    };
+    col(0, A);
+    col(1, B);
+    int x = 0;
+    for (; x + 3 <= ww; x += 3) {
+        col(x + 2, C);
+        step(x, A, B, C);
+        col(x + 3, A);
+        step(x + 1, B, C, A);
+        col(x + 4, B);
+        step(x + 2, C, A, B);
+    }
+    if (x < ww) {
+        col(x + 2, C);
+        step(x, A, B, C);
+        if (x + 1 < ww) {
+            col(x + 3, A);
+            step(x + 1, B, C, A);
+        }
     }
 }
 
@@ -130,87 +140,92 @@ __global__ void __launch_bounds__(kDwThreads) ttt_dwconv_kernel(const DwParams p
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const int d = p.d, hh = p.hh, ww = p.ww, N = hh * ww, gw = ww + 2;
-    float *sG = reinterpret_cast<float *>(smem);                 // padded grid: K, then Q
-    TIO *sV = reinterpret_cast<TIO *>(sG + (size_t)(hh + 2) * gw * d);
-    float *sW = reinterpret_cast<float *>(sV + (size_t)N * d);
-    float *sEta = sW + 9 * d;
-    float *sPart = sEta + N;
+    const size_t gsz = (size_t)(hh + 2) * gw * d;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // [0]: K and V, [1]: Q
+    TIO *sK = reinterpret_cast<TIO *>(smem + 16);         // padded grid of K
+    TIO *sQ = sK + gsz;                                   // padded grid of Q
+    TIO *sV = sQ + gsz;                                   // V [N][d]
+    float *sW = reinterpret_cast<float *>(sV + (size_t)N * d);  // 16-byte aligned
+    float *sPart = sW + 9 * d;                                   // 8-byte aligned (d % 8 == 0)
+    float *sEta = sPart + (size_t)(kDwThreads / (d / 2)) * 9 * d;
     const int bh = blockIdx.x, tid = threadIdx.x;
     const int npair = d / 2, parts = kDwThreads / npair;
-    const int cp = tid % npair, part = tid / npair, c = 2 * cp;
+    const int part = tid / npair, c = 2 * (tid % npair);
     const size_t off = (size_t)bh * N * d;
+    const uint32_t bar_kv = smem_u32(bars), bar_q = smem_u32(bars + 1);
 
-    // zero border of the grid (rows 0 and hh+1, columns 0 and ww+1)
-    for (int i = tid; i < 2 * (gw + hh) * d; i += kDwThreads) {
-        const int cell = i / d, cc = i - cell * d;
-        int y, x;
-        if (cell < gw) { y = 0; x = cell; }
-        else if (cell < 2 * gw) { y = hh + 1; x = cell - gw; }
-        else { const int r = cell - 2 * gw; y = 1 + (r >> 1); x = (r & 1) ? ww + 1 : 0; }
-        sG[((size_t)y * gw + x) * d + cc] = 0.f;
+    if (tid == 0) {
+        mbar_init(bar_kv, 1);
+        mbar_init(bar_q, 1);
+        fence_barrier_init();
     }
-    stage_grid(sG, static_cast<const TIO *>(p.k) + off, hh, ww, d);
-    stage_flat(sV, static_cast<const TIO *>(p.v) + off, N * d);
+    __syncthreads();
+    // warp 0 issues every token copy at once, one bulk copy per grid row (the
+    // interior of a padded row is contiguous) and one for V: K and V complete on
+    // bar_kv, Q on bar_q, so Q lands while the epochs run
+    if (tid < 32) {
+        const uint32_t row = (uint32_t)(ww * d * sizeof(TIO));
+        if (tid == 0) {
+            mbar_arrive_expect_tx(bar_kv, 2u * (uint32_t)hh * row);
+            mbar_arrive_expect_tx(bar_q, (uint32_t)hh * row);
+        }
+        __syncwarp();
+        if (N > 0) {
+            const TIO *gk = static_cast<const TIO *>(p.k) + off, *gq = static_cast<const TIO *>(p.q) + off;
+            for (int y = tid; y < hh; y += 32) {
+                const uint32_t o = (uint32_t)(((size_t)(y + 1) * gw + 1) * d * sizeof(TIO));
+                bulk_load(smem_u32(sK) + o, gk + (size_t)y * ww * d, row, bar_kv);
+                bulk_load(smem_u32(sQ) + o, gq + (size_t)y * ww * d, row, bar_q);
+            }
+            if (tid == 0) bulk_load(smem_u32(sV), static_cast<const TIO *>(p.v) + off, (uint32_t)hh * row, bar_kv);
+        }
+    }
+    zero_border(sK, hh, ww, d);
+    zero_border(sQ, hh, ww, d);
     const float *W0 = p.W0 + (size_t)(bh / p.H) * p.w0_bstride + (size_t)(bh % p.H) * 9 * d;
     for (int i = tid; i < 9 * d; i += kDwThreads) sW[i] = W0[i];
     for (int i = tid; i < N; i += kDwThreads) sEta[i] = p.eta ? p.eta[(size_t)bh * N + i] : p.eta_scalar;
-    __syncthreads();
+    // K and V landed (every thread observes the barrier) and the generic stores
+    // above are visible; a timeout (never expected) is CTA-uniform after the vote
+    if (!__syncthreads_and(mbar_wait(bar_kv, 0, p.status, kSiteStage))) {
+        mbar_wait(bar_q, 0, p.status, kSiteStage);
+        return;
+    }
 
     const bool active = tid < parts * npair;
-    // taps of grid cell (y, x) of the padded grid for this thread's channel pair
-    auto tap = [&](int y, int x) { return *reinterpret_cast<const float2 *>(sG + ((size_t)y * gw + x) * d + c); };
-
     for (int ep = 0; ep < p.epochs; ++ep) {
-        float w[9][2], g[9][2];
+        float2 w[9], g[9];
 #pragma unroll
         for (int o = 0; o < 9; ++o) {
-            w[o][0] = sW[o * d + c];
-            w[o][1] = sW[o * d + c + 1];
-            g[o][0] = g[o][1] = 0.f;
+            w[o] = *reinterpret_cast<const float2 *>(sW + o * d + c);
+            g[o] = make_float2(0.f, 0.f);
         }
         if (active) {
             for (int y = part; y < hh; y += parts) {
-                // sliding 3 x 3 window over padded rows y .. y+2; column j of the
-                // window holds padded column x + j for output column x
-                float2 win[3][3];
-#pragma unroll
-                for (int r = 0; r < 3; ++r) {
-                    win[r][0] = tap(y + r, 0);
-                    win[r][1] = tap(y + r, 1);
-                }
-                for (int x = 0; x < ww; ++x) {
-#pragma unroll
-                    for (int r = 0; r < 3; ++r) win[r][2] = tap(y + r, x + 2);
+                walk_row(sK, y, ww, d, c, [&](int x, const float2(&a)[3], const float2(&b)[3], const float2(&n)[3]) {
                     const int pos = y * ww + x;
                     const float2 vv = ld2(sV + (size_t)pos * d + c);
-                    float e0 = -vv.x, e1 = -vv.y;
+                    float2 e = make_float2(-vv.x, -vv.y);
                     if (!p.dot) {
 #pragma unroll
-                        for (int o = 0; o < 9; ++o) {
-                            e0 = fmaf(win[o / 3][o % 3].x, w[o][0], e0);
-                            e1 = fmaf(win[o / 3][o % 3].y, w[o][1], e1);
+                        for (int r = 0; r < 3; ++r) {
+                            e = fma2(a[r], w[3 * r], e);
+                            e = fma2(b[r], w[3 * r + 1], e);
+                            e = fma2(n[r], w[3 * r + 2], e);
                         }
                     }
                     const float et = sEta[pos];
-                    e0 *= et;
-                    e1 *= et;
-#pragma unroll
-                    for (int o = 0; o < 9; ++o) {
-                        g[o][0] = fmaf(e0, win[o / 3][o % 3].x, g[o][0]);
-                        g[o][1] = fmaf(e1, win[o / 3][o % 3].y, g[o][1]);
-                    }
+                    e = __fmul2_rn(e, make_float2(et, et));
 #pragma unroll
                     for (int r = 0; r < 3; ++r) {
-                        win[r][0] = win[r][1];
-                        win[r][1] = win[r][2];
+                        g[3 * r] = fma2(e, a[r], g[3 * r]);
+                        g[3 * r + 1] = fma2(e, b[r], g[3 * r + 1]);
+                        g[3 * r + 2] = fma2(e, n[r], g[3 * r + 2]);
                     }
-                }
+                });
             }
 #pragma unroll
-            for (int o = 0; o < 9; ++o) {
-                sPart[((size_t)part * 9 + o) * d + c] = g[o][0];
-                sPart[((size_t)part * 9 + o) * d + c + 1] = g[o][1];
-            }
+            for (int o = 0; o < 9; ++o) *reinterpret_cast<float2 *>(sPart + ((size_t)part * 9 + o) * d + c) = g[o];
         }
         __syncthreads();  // partial sums visible; every read of sW is done
         for (int i = tid; i < 9 * d; i += kDwThreads) {
@@ -218,43 +233,27 @@ __global__ void __launch_bounds__(kDwThreads) ttt_dwconv_kernel(const DwParams p
             for (int r = 0; r < parts; ++r) s += sPart[(size_t)r * 9 * d + i];
             sW[i] -= s;
         }
-        __syncthreads();  // the epoch's taps visible; every read of the grid is done
+        __syncthreads();  // the epoch's taps visible
     }
 
-    // output pass: Q in K's place (the border stays zero)
-    stage_grid(sG, static_cast<const TIO *>(p.q) + off, hh, ww, d);
-    __syncthreads();
+    // output pass over the Q grid
+    if (!__syncthreads_and(mbar_wait(bar_q, 0, p.status, kSiteStage))) return;
     if (active) {
-        float w[9][2];
+        float2 w[9];
 #pragma unroll
-        for (int o = 0; o < 9; ++o) {
-            w[o][0] = sW[o * d + c];
-            w[o][1] = sW[o * d + c + 1];
-        }
+        for (int o = 0; o < 9; ++o) w[o] = *reinterpret_cast<const float2 *>(sW + o * d + c);
         TIO *z = static_cast<TIO *>(p.z) + off;
         for (int y = part; y < hh; y += parts) {
-            float2 win[3][3];
-#pragma unroll
-            for (int r = 0; r < 3; ++r) {
-                win[r][0] = tap(y + r, 0);
-                win[r][1] = tap(y + r, 1);
-            }
-            for (int x = 0; x < ww; ++x) {
-#pragma unroll
-                for (int r = 0; r < 3; ++r) win[r][2] = tap(y + r, x + 2);
-                float z0 = 0.f, z1 = 0.f;
-#pragma unroll
-                for (int o = 0; o < 9; ++o) {
-                    z0 = fmaf(win[o / 3][o % 3].x, w[o][0], z0);
-                    z1 = fmaf(win[o / 3][o % 3].y, w[o][1], z1);
-                }
-                st2(z + (size_t)(y * ww + x) * d + c, z0, z1);
+            walk_row(sQ, y, ww, d, c, [&](int x, const float2(&a)[3], const float2(&b)[3], const float2(&n)[3]) {
+                float2 zz = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int r = 0; r < 3; ++r) {
-                    win[r][0] = win[r][1];
-                    win[r][1] = win[r][2];
+                    zz = fma2(a[r], w[3 * r], zz);
+                    zz = fma2(b[r], w[3 * r + 1], zz);
+                    zz = fma2(n[r], w[3 * r + 2], zz);
                 }
-            }
+                st2(z + (size_t)(y * ww + x) * d + c, zz.x, zz.y);
+            });
         }
     }
     if (p.W_out)
@@ -285,6 +284,7 @@ int launch_dwconv(const DwconvArgs &a)
     p.w0_bstride = a.w0_bstride;
     p.z = a.z;
     p.W_out = a.W_out;
+    p.status = a.status;
     if (a.bf16) {
         if (cudaFuncSetAttribute(ttt_dwconv_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)

@@ -45,6 +45,7 @@ struct DwconvArgs {
     long long w0_bstride;
     void *z;
     float *W_out;
+    int *status;  // device status word (timeouts)
     cudaStream_t stream;
 };
 

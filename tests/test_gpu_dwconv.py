@@ -61,7 +61,7 @@ def test_head_dims_and_epochs(d, epochs):
 
 def test_largest_grid_on_chip():
     """22 x 22 tokens at d = 64 in bf16: the largest square grid one CTA holds (the
-    padded fp32 grid, V and the partial sums); 23 x 23 is rejected."""
+    padded K and Q grids, V and the partial sums); 23 x 23 is rejected."""
     inp = G.synth.make("dwconv", B=1, H=2, T=484, d=64, b=484, causal=False, eta="sigmoid", seed=1150)
     _check(inp, 22, 22, loss="mse")
     big = G.synth.make("dwconv", B=1, H=1, T=529, d=64, b=529, causal=False, seed=1151)
