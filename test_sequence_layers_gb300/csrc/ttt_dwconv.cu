@@ -86,53 +86,98 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
-// zero border (rows 0 and hh+1, columns 0 and ww+1) of a padded grid
+// zero border (rows 0 and hh+1, columns 0 and ww+1) of a padded grid, in 16-byte
+// pieces (a cell is d * sizeof(TIO) bytes, a multiple of 16)
 template <typename TIO>
 __device__ __forceinline__ void zero_border(TIO *grid, int hh, int ww, int d)
 {
-    const int gw = ww + 2;
-    for (int i = threadIdx.x; i < 2 * (gw + hh) * d; i += kDwThreads) {
-        const int cell = i / d, cc = i - cell * d;
+    const int gw = ww + 2, vpc = d * (int)sizeof(TIO) / 16;
+    uint4 *g4 = reinterpret_cast<uint4 *>(grid);
+    for (int i = threadIdx.x; i < 2 * (gw + hh) * vpc; i += kDwThreads) {
+        const int cell = i / vpc, piece = i - cell * vpc;
         int y, x;
         if (cell < gw) { y = 0; x = cell; }
         else if (cell < 2 * gw) { y = hh + 1; x = cell - gw; }
         else { const int r = cell - 2 * gw; y = 1 + (r >> 1); x = (r & 1) ? ww + 1 : 0; }
-        grid[((size_t)y * gw + x) * d + cc] = TIO(0.f);
+        g4[((size_t)y * gw + x) * vpc + piece] = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
-// Walks output row y of a padded grid with a 3 x 3 window for channel pair c.
-// The window's columns rotate through three register triples (unrolled by three,
-// so no moves); step(x, a, b, n) gets the columns x, x+1, x+2 of padded rows
-// y .. y+2, i.e. tap (r, j) of output (y, x) is {a, b, n}[j][r].
+// Walks the positions p0 .. p1-1 (row-major) of a padded grid with a 3 x 3 window
+// for channel pair c, one row segment at a time.  The window's columns rotate
+// through three register triples (unrolled by three, so no moves);
+// step(pos, a, b, n) gets the padded columns x, x+1, x+2 of padded rows y .. y+2
+// for output (y, x) = pos, i.e. tap (r, j) is {a, b, n}[j][r].
 template <typename TIO, typename Step>
-__device__ __forceinline__ void walk_row(const TIO *g, int y, int ww, int d, int c, Step &&step)
+__device__ __forceinline__ void walk_run(const TIO *g, int p0, int p1, int ww, int d, int c, Step &&step)
 {
     const int gw = ww + 2;
-    float2 A[3], B[3], C[3];
-    auto col = [&](int xc, float2 (&cc)[3]) {
+    int y = p0 < p1 ? p0 / ww : 0, x0 = p0 - y * ww;  // (ww > 0 whenever the run is not empty)
+    while (p0 < p1) {
+        const int x1 = min(ww, x0 + (p1 - p0)), base = y * ww;
+        float2 A[3], B[3], C[3];
+        auto col = [&](int xc, float2 (&cc)[3]) {
 #pragma unroll
-        for (int r = 0; r < 3; ++r) cc[r] = ld2(g + ((size_t)(y + r) * gw + xc) * d + c);
-    };
-    col(0, A);
-    col(1, B);
-    int x = 0;
-    for (; x + 3 <= ww; x += 3) {
-        col(x + 2, C);
-        step(x, A, B, C);
-        col(x + 3, A);
-        step(x + 1, B, C, A);
-        col(x + 4, B);
-        step(x + 2, C, A, B);
-    }
-    if (x < ww) {
-        col(x + 2, C);
-        step(x, A, B, C);
-        if (x + 1 < ww) {
+            for (int r = 0; r < 3; ++r) cc[r] = ld2(g + ((size_t)(y + r) * gw + xc) * d + c);
+        };
+        col(x0, A);
+        col(x0 + 1, B);
+        int x = x0;
+        for (; x + 3 <= x1; x += 3) {
+            col(x + 2, C);
+            step(base + x, A, B, C);
             col(x + 3, A);
-            step(x + 1, B, C, A);
+            step(base + x + 1, B, C, A);
+            col(x + 4, B);
+            step(base + x + 2, C, A, B);
         }
+        if (x < x1) {
+            col(x + 2, C);
+            step(base + x, A, B, C);
+            if (x + 1 < x1) {
+                col(x + 3, A);
+                step(base + x + 1, B, C, A);
+            }
+        }
+        p0 += x1 - x0;
+        ++y;
+        x0 = 0;
     }
+}
+
+// One epoch's partial tap gradients of this thread's channel pair over its run:
+// g[o] += s_p e_p K[p + o], with e_p = f(K; W)_p - V_p (MSE) or V_p (DOT, whose
+// true residual -V_p has its sign applied in the update), s_p = eta_p (ETA) or 1
+// (a scalar eta is applied in the update).
+template <typename TIO, bool DOT, bool ETA>
+__device__ __forceinline__ void epoch_grad(const TIO *sK, const TIO *sV, const float *sEta, const float2 (&w)[9],
+                                           float2 (&g)[9], int p0, int p1, int ww, int d, int c)
+{
+    walk_run(sK, p0, p1, ww, d, c, [&](int pos, const float2(&a)[3], const float2(&b)[3], const float2(&n)[3]) {
+        const float2 vv = ld2(sV + (size_t)pos * d + c);
+        float2 e;
+        if constexpr (DOT) {
+            e = vv;
+        } else {
+            e = make_float2(-vv.x, -vv.y);
+#pragma unroll
+            for (int r = 0; r < 3; ++r) {
+                e = fma2(a[r], w[3 * r], e);
+                e = fma2(b[r], w[3 * r + 1], e);
+                e = fma2(n[r], w[3 * r + 2], e);
+            }
+        }
+        if constexpr (ETA) {
+            const float et = sEta[pos];
+            e = __fmul2_rn(e, make_float2(et, et));
+        }
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+            g[3 * r] = fma2(e, a[r], g[3 * r]);
+            g[3 * r + 1] = fma2(e, b[r], g[3 * r + 1]);
+            g[3 * r + 2] = fma2(e, n[r], g[3 * r + 2]);
+        }
+    });
 }
 
 template <typename TIO>
@@ -184,7 +229,8 @@ __global__ void __launch_bounds__(kDwThreads) ttt_dwconv_kernel(const DwParams p
     zero_border(sQ, hh, ww, d);
     const float *W0 = p.W0 + (size_t)(bh / p.H) * p.w0_bstride + (size_t)(bh % p.H) * 9 * d;
     for (int i = tid; i < 9 * d; i += kDwThreads) sW[i] = W0[i];
-    for (int i = tid; i < N; i += kDwThreads) sEta[i] = p.eta ? p.eta[(size_t)bh * N + i] : p.eta_scalar;
+    if (p.eta)
+        for (int i = tid; i < N; i += kDwThreads) sEta[i] = p.eta[(size_t)bh * N + i];
     // K and V landed (every thread observes the barrier) and the generic stores
     // above are visible; a timeout (never expected) is CTA-uniform after the vote
     if (!__syncthreads_and(mbar_wait(bar_kv, 0, p.status, kSiteStage))) {
@@ -193,36 +239,24 @@ __global__ void __launch_bounds__(kDwThreads) ttt_dwconv_kernel(const DwParams p
     }
 
     const bool active = tid < parts * npair;
+    // this thread's run of positions: an even share of the N in row-major order
+    const int p0 = (int)((long long)N * part / parts), p1 = (int)((long long)N * (part + 1) / parts);
+    // W -= upd * (summed partials): the dot loss's sign and a scalar eta
+    const float upd = (p.dot ? -1.f : 1.f) * (p.eta ? 1.f : p.eta_scalar);
     for (int ep = 0; ep < p.epochs; ++ep) {
-        float2 w[9], g[9];
-#pragma unroll
-        for (int o = 0; o < 9; ++o) {
-            w[o] = *reinterpret_cast<const float2 *>(sW + o * d + c);
-            g[o] = make_float2(0.f, 0.f);
-        }
         if (active) {
-            for (int y = part; y < hh; y += parts) {
-                walk_row(sK, y, ww, d, c, [&](int x, const float2(&a)[3], const float2(&b)[3], const float2(&n)[3]) {
-                    const int pos = y * ww + x;
-                    const float2 vv = ld2(sV + (size_t)pos * d + c);
-                    float2 e = make_float2(-vv.x, -vv.y);
-                    if (!p.dot) {
+            float2 w[9], g[9];
 #pragma unroll
-                        for (int r = 0; r < 3; ++r) {
-                            e = fma2(a[r], w[3 * r], e);
-                            e = fma2(b[r], w[3 * r + 1], e);
-                            e = fma2(n[r], w[3 * r + 2], e);
-                        }
-                    }
-                    const float et = sEta[pos];
-                    e = __fmul2_rn(e, make_float2(et, et));
-#pragma unroll
-                    for (int r = 0; r < 3; ++r) {
-                        g[3 * r] = fma2(e, a[r], g[3 * r]);
-                        g[3 * r + 1] = fma2(e, b[r], g[3 * r + 1]);
-                        g[3 * r + 2] = fma2(e, n[r], g[3 * r + 2]);
-                    }
-                });
+            for (int o = 0; o < 9; ++o) {
+                w[o] = *reinterpret_cast<const float2 *>(sW + o * d + c);
+                g[o] = make_float2(0.f, 0.f);
+            }
+            if (p.dot) {
+                if (p.eta) epoch_grad<TIO, true, true>(sK, sV, sEta, w, g, p0, p1, ww, d, c);
+                else epoch_grad<TIO, true, false>(sK, sV, sEta, w, g, p0, p1, ww, d, c);
+            } else {
+                if (p.eta) epoch_grad<TIO, false, true>(sK, sV, sEta, w, g, p0, p1, ww, d, c);
+                else epoch_grad<TIO, false, false>(sK, sV, sEta, w, g, p0, p1, ww, d, c);
             }
 #pragma unroll
             for (int o = 0; o < 9; ++o) *reinterpret_cast<float2 *>(sPart + ((size_t)part * 9 + o) * d + c) = g[o];
@@ -231,7 +265,7 @@ __global__ void __launch_bounds__(kDwThreads) ttt_dwconv_kernel(const DwParams p
         for (int i = tid; i < 9 * d; i += kDwThreads) {
             float s = 0.f;
             for (int r = 0; r < parts; ++r) s += sPart[(size_t)r * 9 * d + i];
-            sW[i] -= s;
+            sW[i] = fmaf(-upd, s, sW[i]);
         }
         __syncthreads();  // the epoch's taps visible
     }
@@ -243,18 +277,16 @@ __global__ void __launch_bounds__(kDwThreads) ttt_dwconv_kernel(const DwParams p
 #pragma unroll
         for (int o = 0; o < 9; ++o) w[o] = *reinterpret_cast<const float2 *>(sW + o * d + c);
         TIO *z = static_cast<TIO *>(p.z) + off;
-        for (int y = part; y < hh; y += parts) {
-            walk_row(sQ, y, ww, d, c, [&](int x, const float2(&a)[3], const float2(&b)[3], const float2(&n)[3]) {
-                float2 zz = make_float2(0.f, 0.f);
+        walk_run(sQ, p0, p1, ww, d, c, [&](int pos, const float2(&a)[3], const float2(&b)[3], const float2(&n)[3]) {
+            float2 zz = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int r = 0; r < 3; ++r) {
-                    zz = fma2(a[r], w[3 * r], zz);
-                    zz = fma2(b[r], w[3 * r + 1], zz);
-                    zz = fma2(n[r], w[3 * r + 2], zz);
-                }
-                st2(z + (size_t)(y * ww + x) * d + c, zz.x, zz.y);
-            });
-        }
+            for (int r = 0; r < 3; ++r) {
+                zz = fma2(a[r], w[3 * r], zz);
+                zz = fma2(b[r], w[3 * r + 1], zz);
+                zz = fma2(n[r], w[3 * r + 2], zz);
+            }
+            st2(z + (size_t)pos * d + c, zz.x, zz.y);
+        });
     }
     if (p.W_out)
         for (int i = tid; i < 9 * d; i += kDwThreads) p.W_out[(size_t)bh * 9 * d + i] = sW[i];
