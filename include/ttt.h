@@ -232,8 +232,9 @@ typedef struct {
  * sum_p eta_p l_p at the epoch's start taps and steps by it; z = f(q; W_final).
  *   q, k, v, z : [B,H,N,d] io_dtype; eta: [B,H,N] fp32 or NULL (eta_scalar)
  *   W0         : fp32 taps, see w0_batch_stride; W_out: [B,H,9,d] fp32 or NULL
- * The sequence is held on chip: 2 (height+2) (width+2) d sizeof(io) + N d sizeof(io)
- * + 4 (9 d + N + 9 * 512) bytes must fit in 227 KB (bf16, d = 64: up to 22 x 22
+ * The sequence is held on chip: two padded grids of (height+2) (width+2) d
+ * sizeof(io) bytes and V of N d sizeof(io) bytes, each rounded up to 128 bytes, plus
+ * 256 + 4 (9 d + N + 9 * 512) bytes must fit in 227 KB (bf16, d = 64: up to 22 x 22
  * tokens), else TTT_ERR_UNSUPPORTED.  Pointers: q, k,
  * v, z 16-byte aligned (TTT_ERR_ALIGN), fp32 arrays 4-byte aligned.
  */

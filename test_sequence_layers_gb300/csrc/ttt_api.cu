@@ -102,6 +102,20 @@ bool ttt::encode_token_map(CUtensorMap *m, const void *ptr, int BH, int T, int d
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool ttt::encode_grid_map(CUtensorMap *m, const void *ptr, bool bf16, int BH, int hh, int ww, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || d > 256 || ww + 2 > 256 || hh + 2 > 256) return false;
+    const cuuint64_t es = bf16 ? 2 : 4;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)ww, (cuuint64_t)hh, (cuuint64_t)BH};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * es, (cuuint64_t)ww * d * es, (cuuint64_t)hh * ww * d * es};
+    const cuuint32_t box[4] = {(cuuint32_t)d, (cuuint32_t)ww + 2, (cuuint32_t)hh + 2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(ptr),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -55,6 +55,12 @@ struct DwconvArgs {
 // entry point is unavailable or rejects it.
 bool encode_token_map(CUtensorMap *m, const void *ptr, int BH, int T, int d, int rows, int cols = 0);
 
+// Descriptor of a token tensor [BH][hh][ww][d] (bf16 or fp32) whose box is one
+// sequence's zero-bordered grid: d x (ww+2) x (hh+2) at coordinates (0, -1, -1, bh),
+// the border read as zeros (out of range).  False if d > 256, hh + 2 or ww + 2 > 256,
+// or the encoding fails.
+bool encode_grid_map(CUtensorMap *m, const void *ptr, bool bf16, int BH, int hh, int ww, int d);
+
 // q, k, v descriptors (zeroed, unused when T == 0); false on an encoding failure.
 inline bool encode_qkv(CUtensorMap *maps, const void *q, const void *k, const void *v, int BH, int T,
                        int d, int rows)

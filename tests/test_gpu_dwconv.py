@@ -59,6 +59,15 @@ def test_head_dims_and_epochs(d, epochs):
     _check(inp, 8, 10, epochs=epochs, per_batch=True)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_wide_head_row_copies(dtype):
+    """d = 512, past the 256-element box of a tensor map: one bulk copy per grid row
+    with the border zeroed in shared memory, a single buffer, runtime strides."""
+    inp = G.synth.make("dwconv", B=1, H=3, T=12, d=512, b=12, causal=False, dtype=dtype, eta="sigmoid",
+                       seed=1400)
+    _check(inp, 3, 4, loss="mse", epochs=2)
+
+
 def test_largest_grid_on_chip():
     """22 x 22 tokens at d = 64 in bf16: the largest square grid one CTA holds (the
     padded K and Q grids, V and the partial sums); 23 x 23 is rejected."""
