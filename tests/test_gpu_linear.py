@@ -82,7 +82,7 @@ def test_full_batch_noncausal_single_block():
     _check(inp)
 
 
-@pytest.mark.parametrize("T", [1, 17, 64, 100, 196, 256, 300])
+@pytest.mark.parametrize("T", [1, 17, 48, 64, 80, 100, 196, 240, 256, 300])
 def test_full_batch_lengths(T):
     """b >= T, non-causal (one inner GD step over the whole sequence, every query
     reads the updated weights): short, ragged, box-aligned and longest on-chip
