@@ -197,7 +197,9 @@ int launch_linear(const ttt::LinearArgs &a, ttt_dtype io)
     } else if (io == TTT_BF16) {
         rc = ttt::launch_linear_fb(a);  // full-batch mini-batch: no serial chain
         if (rc == TTT_ERR_UNSUPPORTED && a.epochs == 1)  // repeated epochs: the full-batch kernel only
-            rc = (a.b == 16 && a.d <= 64) ? ttt::launch_linear_b16(a) : ttt::launch_linear_bf16(a);
+            rc = a.b == 1                    ? ttt::launch_linear_b1(a)  // delta rule: column-parallel
+                 : (a.b == 16 && a.d <= 64) ? ttt::launch_linear_b16(a)
+                                            : ttt::launch_linear_bf16(a);
     } else
         rc = ttt::launch_linear_f32(a);
     return rc;

@@ -71,6 +71,17 @@ def test_b16_d64_odd_chain_counts(B, H):
     _check(inp)
 
 
+@pytest.mark.parametrize("d", [16, 32, 128])
+@pytest.mark.parametrize("T", [0, 1, 63, 64, 65, 129])
+def test_b1_delta_rule_lengths(d, T):
+    """b = 1 (the delta rule, column-parallel kernel): lengths around its 64-token
+    blocks, per-token eta, per-batch W0, both masks (a one-token mini-batch reads its
+    own write either way)."""
+    for causal in (True, False):
+        inp = G.synth.make("linear", B=3, H=1, T=T, d=d, b=1, causal=causal, eta="sigmoid", seed=900 + d + T)
+        _check(inp, per_batch_w0=True)
+
+
 def test_per_token_eta_and_per_batch_w0():
     inp = G.synth.make("linear", B=3, H=2, T=130, d=64, b=16, causal=True, eta="sigmoid", seed=11)
     _check(inp, per_batch_w0=True)
