@@ -111,6 +111,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *st
 
 // --------------------------------------------------------------- async copies
 
+// Starts fetching a TMA descriptor (kernel parameter) into the descriptor cache,
+// so the first copy that uses it does not wait for that fetch.
+__device__ __forceinline__ void prefetch_tmap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // TMA: 3-D tiled tensor load into shared memory, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar, int x,
                                             int y, int zc)

@@ -153,6 +153,9 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
     const uint32_t blk_full = base + C::BAR_OFF;      // block landed (producer -> warps)
     const uint32_t blk_empty = blk_full + 8 * NB;     // block released (warps -> producer)
     if (threadIdx.x == 0) {
+        if (QSIDE) prefetch_tmap(tq);
+        prefetch_tmap(tk);
+        prefetch_tmap(tv);
         for (int s = 0; s < NB; ++s) {
             mbar_init(blk_full + 8 * s, 1 + (has_eta ? 32 : 0));
             mbar_init(blk_empty + 8 * s, C::NCW);

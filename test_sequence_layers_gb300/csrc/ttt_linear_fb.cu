@@ -79,6 +79,9 @@ __global__ void __launch_bounds__(FbCfg::THREADS, 3)
     const bool has_eta = p.eta != nullptr;
 
     if (threadIdx.x == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
         for (int L = 0; L <= nblk; ++L) mbar_init(kv_bar + 8 * L, 1);
         fence_barrier_init();
     }
