@@ -56,7 +56,6 @@ struct B16Cfg {
     static constexpr int BAR_OFF = ETA_OFF + NB * 256;
     static constexpr int RED_OFF = BAR_OFF + 2 * NB * 8;  // inner-norm partial sums [3][NCW][16] float2
     static constexpr int SMEM = RED_OFF + 3 * NCW * 16 * 8 + 1024;
-    static constexpr uint32_t SWM = RB == 128 ? 7u : (RB == 64 ? 3u : 1u);
 };
 
 // Offset of element (r, c) inside a 64-token block written by TMA with the swizzle
@@ -65,8 +64,9 @@ struct B16Cfg {
 template <int D>
 __device__ __forceinline__ uint32_t boff(int r, int c)
 {
+    constexpr uint32_t SWM = 2 * D == 128 ? 7u : (2 * D == 64 ? 3u : 1u);  // swizzle key mask of the row length
     uint32_t a = static_cast<uint32_t>(r * B16Cfg<D>::RB + c * 2);
-    return a ^ (((a >> 7) & B16Cfg<D>::SWM) << 4);
+    return a ^ (((a >> 7) & SWM) << 4);
 }
 
 template <int D>
