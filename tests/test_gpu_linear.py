@@ -190,7 +190,8 @@ def _check_variant(inp, loss="mse", epochs=1, tol=None):
 
 
 @pytest.mark.parametrize("d,b,causal", [(16, 16, True), (64, 16, True), (64, 16, False), (32, 5, True),
-                                        (128, 16, True), (64, 1, True), (64, 196, False)])
+                                        (128, 16, True), (64, 1, True), (16, 1, False), (128, 1, True),
+                                        (64, 196, False)])
 def test_dot_loss_bf16(d, b, causal):
     """Negative dot-product loss (the ViT3 block's inner loss): residual -V; every
     bf16 kernel (b = 16, general, full batch)."""
