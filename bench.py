@@ -101,7 +101,7 @@ def kernel_name(inp):
         return "ttt_linear_f32_kernel" if inp.kind == "linear" else "ttt_mlp_f32_kernel"
     if inp.kind == "linear":
         if not inp.causal and inp.b >= inp.T and inp.d == 64 and inp.T <= 256:
-            return "ttt_linear_fb_kernel"
+            return "ttt_linear_fb_tc_kernel" if inp.options.get("epochs", 1) == 1 else "ttt_linear_fb_kernel"
         if inp.b == 1 and inp.options.get("epochs", 1) == 1 and not inp.options.get("ln"):
             return "ttt_linear_b1_kernel"
         return "ttt_linear_b16_kernel" if min(inp.b, inp.T) == 16 and inp.d <= 64 else "ttt_linear_bf16_kernel"

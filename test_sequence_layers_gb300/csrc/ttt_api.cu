@@ -195,7 +195,8 @@ int launch_linear(const ttt::LinearArgs &a, ttt_dtype io)
         const bool b16 = a.b == 16 || (a.b == a.T && a.T < 16);
         rc = (b16 && a.d <= 64) ? ttt::launch_linear_b16(a) : TTT_ERR_UNSUPPORTED;
     } else if (io == TTT_BF16) {
-        rc = ttt::launch_linear_fb(a);  // full-batch mini-batch: no serial chain
+        rc = ttt::launch_linear_fb_tc(a);  // full-batch mini-batch: no serial chain
+        if (rc == TTT_ERR_UNSUPPORTED) rc = ttt::launch_linear_fb(a);  // several epochs
         if (rc == TTT_ERR_UNSUPPORTED && a.epochs == 1)  // repeated epochs: the full-batch kernel only
             rc = a.b == 1                    ? ttt::launch_linear_b1(a)  // delta rule: column-parallel
                  : (a.b == 16 && a.d <= 64) ? ttt::launch_linear_b16(a)
