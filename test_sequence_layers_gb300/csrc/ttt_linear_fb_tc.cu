@@ -42,13 +42,9 @@ struct FbtCfg {
     static constexpr int TMEM_COLS = 128;                // E, then the update, then Z: 2 x 64 columns
 };
 
-// Offset of element (r, c) of a tile of rows of 64 bf16 (128 bytes) written with the
-// 128-byte swizzle (the tile 1024-byte aligned): 16-byte chunk c/8 of row r moves to
-// chunk (c/8) ^ (r % 8).
-__device__ __forceinline__ uint32_t sw128(int r, int c)
-{
-    return (uint32_t)r * 128u + (uint32_t)(((c >> 3) ^ (r & 7)) << 4) + (uint32_t)(c & 7) * 2u;
-}
+// Tiles are rows of 64 bf16 (128 bytes) with the 128-byte swizzle (tiles 1024-byte
+// aligned): the 16-byte chunk ch of row r sits at r * 128 + ((ch ^ (r % 8)) << 4), the
+// layout TMA writes and the tensor core reads.
 
 // Shared-memory matrix descriptor of a 128-byte-swizzled operand: start address, the
 // byte distance between 64-element atoms along M/N (read for MN-major operands only)
@@ -156,17 +152,20 @@ __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // W0^T as bf16 rows (row j: W0[0..63][j]), the B operand of E = K W0; the column of
-    // W0 that this thread completes after the update (see there) is read now
+    // Lanes 0..15 of warp q own column j = 16 q + lane of W: they read W0's column j
+    // (kept for the update's epilogue) and write it as row j of the bf16 W0^T tile, the
+    // B operand of E = K W0
     const float *W0 = p.W0 + (size_t)(bh / p.H) * p.w0_bstride + (size_t)(bh % p.H) * D * D;
     const int j = 16 * warp + (lane & 15);
     float w0c[D];
 #pragma unroll
     for (int i = 0; i < D; ++i) w0c[i] = W0[(size_t)i * D + j];
-    for (int e = tid; e < D * D; e += C::THREADS) {
-        const int i = e >> 6, j = e & 63;  // coalesced reads of W0[i][j]
-        *reinterpret_cast<__nv_bfloat16 *>(gb + C::W_OFF + sw128(j, i)) = __float2bfloat16_rn(W0[e]);
-    }
+    if (lane < 16)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4 *>(gb + C::W_OFF + j * 128 + (((uint32_t)ch ^ (uint32_t)(j & 7)) << 4)) =
+                make_uint4(pack_bf16(w0c[8 * ch], w0c[8 * ch + 1]), pack_bf16(w0c[8 * ch + 2], w0c[8 * ch + 3]),
+                           pack_bf16(w0c[8 * ch + 4], w0c[8 * ch + 5]), pack_bf16(w0c[8 * ch + 6], w0c[8 * ch + 7]));
     fence_proxy_async();  // the generic-proxy writes of W0^T before the tensor core reads them
     tc_fence_before();
     __syncthreads();
