@@ -93,6 +93,27 @@ def test_full_batch_noncausal_single_block():
     _check(inp)
 
 
+def test_full_batch_weights_not_16_byte_aligned():
+    """Initial and final weights that are only 4-byte aligned (views at an odd float
+    offset), which the boundary accepts: the full-batch kernel reads and writes them
+    as single floats."""
+    inp = G.synth.make("linear", B=2, H=2, T=196, d=64, b=196, causal=False, eta="sigmoid", seed=450)
+    dev = torch.device("cuda")
+    from test_sequence_layers_gb300 import abi
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    W0 = inp.params["W0"]
+    buf = torch.zeros(W0.numel() + 1, device=dev)
+    buf[1:] = W0.reshape(-1).to(dev)
+    W0u = buf[1:].view(W0.shape)
+    obuf = torch.zeros(2 * 2 * 64 * 64 + 1, device=dev)
+    Wout = obuf[1:].view(2, 2, 64, 64)
+    z, W = abi.ttt_linear_fwd(q, k, v, W0u, inp.b, False, eta=inp.eta.to(dev), W_out=Wout)
+    abi.ttt_sync_status()
+    zr, Wr = G.oracle_linear(inp)
+    ez, eW = G.rel_err(z.double().cpu(), zr), G.rel_err(Wout.double().cpu(), Wr)
+    assert ez <= G.TOL_BF16 and eW <= G.TOL_BF16, (ez, eW)
+
+
 @pytest.mark.parametrize("T", [1, 17, 48, 64, 80, 100, 196, 240, 256, 300])
 def test_full_batch_lengths(T):
     """b >= T, non-causal (one inner GD step over the whole sequence, every query
