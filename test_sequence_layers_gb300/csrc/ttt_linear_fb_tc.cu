@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
     // Et rows: -eta_t (E - V) over this thread's rows of V (zero past T)
     if (ok) {
         for (int m = 0; m < ntile; ++m) {
+            if (128 * m + 32 * warp >= 16 * nk) break;  // rows the update does not read (warp-uniform)
             const int t = 128 * m + 32 * warp + lane;
             const float et = t < T ? (p.eta ? p.eta[(size_t)bh * T + t] : p.eta_scalar) : 0.f;
             uint8_t *vrow = gb + C::V_OFF + t * 128;
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
     tc_fence_after();
     if (ok) {
         for (int m = 0; m < ntile; ++m) {
+            if (128 * m + 32 * warp >= T) break;  // no token of this warp's rows (warp-uniform)
             const int t = 128 * m + 32 * warp + lane;
             __nv_bfloat16 *zr = p.z + ((size_t)bh * T + t) * D;
             float zz[64];
