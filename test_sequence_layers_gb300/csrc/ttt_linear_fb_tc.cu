@@ -28,6 +28,7 @@
 
 #include "ttt_device.cuh"
 #include "ttt_internal.h"
+#include "ttt_tcgen05.cuh"
 
 namespace ttt {
 namespace {
@@ -41,67 +42,6 @@ struct FbtCfg {
     static constexpr int SMEM = BAR_OFF + 32 + 1024;
     static constexpr int TMEM_COLS = 128;                // E, then the update, then Z: 2 x 64 columns
 };
-
-// Tiles are rows of 64 bf16 (128 bytes) with the 128-byte swizzle (tiles 1024-byte
-// aligned): the 16-byte chunk ch of row r sits at r * 128 + ((ch ^ (r % 8)) << 4), the
-// layout TMA writes and the tensor core reads.
-
-// Shared-memory matrix descriptor of a 128-byte-swizzled operand: start address, the
-// byte distance between 64-element atoms along M/N (read for MN-major operands only)
-// and between 8-row atoms (1024 bytes).  K-major operands step along K by 32 bytes
-// per 16-element slice inside the swizzled row; MN-major ones by two 8-row atoms.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t mn_atom_stride)
-{
-    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((mn_atom_stride >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)(1024u >> 4) << 32;
-    d |= (uint64_t)1 << 46;  // descriptor version
-    d |= (uint64_t)2 << 61;  // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor of a bf16 x bf16 -> fp32 product of shape M x N (x K16);
-// mn_a / mn_b: the operand is MN-major (M or N contiguous) rather than K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool mn_a, bool mn_b)
-{
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((mn_a ? 1u : 0u) << 15) | ((mn_b ? 1u : 0u) << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t dtmem, uint64_t da, uint64_t db, uint32_t idesc, bool acc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
-        "l"(da), "l"(db), "r"(idesc), "r"((uint32_t)acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 64 consecutive fp32 columns of this thread's TMEM lane (four loads, one wait)
-__device__ __forceinline__ void tc_ld64(uint32_t taddr, float (&v)[64])
-{
-    uint32_t r[64];
-#pragma unroll
-    for (int c = 0; c < 64; c += 16)
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-            : "=r"(r[c + 0]), "=r"(r[c + 1]), "=r"(r[c + 2]), "=r"(r[c + 3]), "=r"(r[c + 4]), "=r"(r[c + 5]),
-              "=r"(r[c + 6]), "=r"(r[c + 7]), "=r"(r[c + 8]), "=r"(r[c + 9]), "=r"(r[c + 10]), "=r"(r[c + 11]),
-              "=r"(r[c + 12]), "=r"(r[c + 13]), "=r"(r[c + 14]), "=r"(r[c + 15])
-            : "r"(taddr + c));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 struct FbtParams {
     int H, T, dot;
@@ -146,12 +86,7 @@ __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
             tma_load_3d(sV + L * 8192, &tv, bar_kv, 0, 64 * L, bh);
         }
     }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + C::BAR_OFF + 24),
-                     "r"(C::TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 0) tc_alloc(base + C::BAR_OFF + 24, C::TMEM_COLS);
     // Lanes 0..15 of warp q own column j = 16 q + lane of W: they read W0's column j
     // (kept for the update's epilogue) and write it as row j of the bf16 W0^T tile, the
     // B operand of E = K W0
@@ -298,8 +233,7 @@ __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+    if (warp == 0) tc_dealloc(tmem, C::TMEM_COLS);
 }
 
 }  // namespace

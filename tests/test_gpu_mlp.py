@@ -63,7 +63,7 @@ def test_bf16_small(d, b, causal):
     _check(inp)
 
 
-@pytest.mark.parametrize("T", [1, 16, 17, 75, 196])
+@pytest.mark.parametrize("T", [1, 16, 17, 75, 129, 196, 256])
 def test_bf16_full_batch(T):
     """b >= T, non-causal: one inner GD step over the whole sequence, every query
     reads the updated weights (short, chunk-aligned and ragged lengths, biases,
