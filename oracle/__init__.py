@@ -47,6 +47,8 @@ def _load():
         lib.ttt_oracle_mlp.restype = i
         lib.ttt_oracle_dwconv.argtypes = [i, i, i, i, i, i, i, dp, dp, dp, dp, d, dp, ll, dp, dp, i]
         lib.ttt_oracle_dwconv.restype = i
+        lib.ttt_oracle_eta_gate.argtypes = [i, i, i, i, dp, dp, d, dp]
+        lib.ttt_oracle_eta_gate.restype = i
         _lib = lib
     return _lib
 
@@ -155,3 +157,18 @@ def dwconv(q, k, v, W0, height, width, eta=None, eta_scalar=1.0, loss="mse", epo
     if rc != 0:
         raise ValueError("ttt_oracle_dwconv rejected its arguments")
     return z, Wf
+
+
+def eta_gate(x, theta, eta_base=1.0):
+    """Input-dependent inner learning rate, fp64: eta[b,h,t] = eta_base *
+    sigma(theta[h] . x[b,t]).  x: [B,T,dm] (the layer's input tokens); theta: [H,dm]
+    (one learnable vector per head).  Returns eta [B,H,T] as a float64 numpy array."""
+    x, theta = _f64(x), _f64(theta)
+    B, T, dm = x.shape
+    H = theta.shape[0]
+    assert theta.shape == (H, dm)
+    eta = np.zeros((B, H, T))
+    rc = _load().ttt_oracle_eta_gate(B, T, H, dm, _ptr(x), _ptr(theta), float(eta_base), _ptr(eta))
+    if rc != 0:
+        raise ValueError("ttt_oracle_eta_gate rejected its arguments")
+    return eta

@@ -488,3 +488,27 @@ int ttt_oracle_dwconv(int B, int H, int hh, int ww, int d, int loss, int epochs,
     pthread_mutex_destroy(&J.lock);
     return 0;
 }
+
+/*
+ * Input-dependent inner learning rate ("Learning to (Learn at Test Time)"
+ * walkthrough, section 2.2.3, the learnable rate): eta(x) = eta_base * sigma(theta_lr . x)
+ * with theta_lr a learnable vector of the outer loop, sigma the logistic function
+ * 1 / (1 + e^-a) and eta_base the base rate (1 for TTT-Linear, 0.1 for TTT-MLP).
+ * x is the layer's input token; each head carries its own vector (the passage names
+ * one vector; a multi-head layer gates each head's rate).
+ *   x: [B,T,dm], theta: [H,dm], eta: [B,H,T] (the layout the TTT layer reads).
+ */
+int ttt_oracle_eta_gate(int B, int T, int H, int dm, const double *x, const double *theta,
+                        double eta_base, double *eta)
+{
+    if (B < 0 || T < 0 || H < 1 || dm < 1 || !x || !theta || !eta) return -1;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int t = 0; t < T; ++t) {
+                const double *xt = x + ((size_t)b * T + t) * dm, *th = theta + (size_t)h * dm;
+                double a = 0.0;
+                for (int i = 0; i < dm; ++i) a += th[i] * xt[i];
+                eta[((size_t)b * H + h) * T + t] = eta_base / (1.0 + exp(-a));
+            }
+    return 0;
+}

@@ -448,3 +448,53 @@ def test_linear_layer_norm_needs_mse():
     with pytest.raises(ValueError):
         oracle.linear(q, k, v, np.zeros((1, 4, 4)), 2, loss="dot", ln_gamma=np.ones((1, 4)),
                       ln_beta=np.zeros((1, 4)))
+
+
+# ------------------------------------------------- input-dependent learning rate
+
+def _logit(eta, eta_base):
+    p = eta / eta_base
+    return np.log(p) - np.log1p(-p)
+
+
+def test_eta_gate_zero_vector_is_half_the_base_rate():
+    """theta = 0: sigma(0) = 1/2 for every token, exactly."""
+    x = rng.standard_normal((2, 7, 24))
+    eta = oracle.eta_gate(x, np.zeros((3, 24)), eta_base=0.1)
+    assert eta.shape == (2, 3, 7)
+    assert np.all(eta == 0.05)
+
+
+def test_eta_gate_one_hot_vectors_read_one_feature_per_head():
+    """theta[h] = c_h e_{j_h}: the logit of eta[b,h,t] / eta_base is c_h x[b,t,j_h]
+    (pins which axis of x is the feature axis and which row of theta each head uses)."""
+    B, T, dm, H = 3, 11, 40, 4
+    x = rng.standard_normal((B, T, dm))
+    js, cs = [3, 17, 0, 39], [0.5, -1.25, 2.0, 0.75]
+    theta = np.zeros((H, dm))
+    for h in range(H):
+        theta[h, js[h]] = cs[h]
+    eta = oracle.eta_gate(x, theta, eta_base=1.0)
+    for h in range(H):
+        np.testing.assert_allclose(_logit(eta[:, h, :], 1.0), cs[h] * x[:, :, js[h]], rtol=1e-10, atol=1e-12)
+
+
+def test_eta_gate_logit_is_linear_in_the_vector():
+    """logit(eta(theta1 + theta2)) = logit(eta(theta1)) + logit(eta(theta2)): the gate's
+    argument is a full dot product (no dropped or repeated feature)."""
+    B, T, dm, H = 2, 9, 72, 3
+    x = rng.standard_normal((B, T, dm))
+    t1, t2 = 0.05 * rng.standard_normal((H, dm)), 0.05 * rng.standard_normal((H, dm))
+    e1, e2, e12 = (oracle.eta_gate(x, t, 1.0) for t in (t1, t2, t1 + t2))
+    np.testing.assert_allclose(_logit(e12, 1.0), _logit(e1, 1.0) + _logit(e2, 1.0), rtol=1e-9, atol=1e-12)
+
+
+def test_eta_gate_symmetry_and_saturation():
+    """sigma(a) + sigma(-a) = 1, so eta(theta) + eta(-theta) = eta_base; a large
+    argument gives the base rate (sigma(40) rounds to 1 in double precision)."""
+    x = rng.standard_normal((2, 6, 16))
+    th = rng.standard_normal((5, 16))
+    np.testing.assert_allclose(oracle.eta_gate(x, th, 0.1) + oracle.eta_gate(x, -th, 0.1), 0.1, rtol=1e-14)
+    ones = np.ones((1, 3, 4))
+    assert np.all(oracle.eta_gate(ones, np.full((1, 4), 10.0), 1.0) == 1.0)
+    assert np.all(oracle.eta_gate(ones, np.full((1, 4), -10.0), 1.0) < 1e-17)
