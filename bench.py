@@ -62,6 +62,9 @@ def flops_per_token_head(inp):
         # FMAs; output 9 FMAs
         per_epoch = 18 * d + (18 * d if o.get("loss", "mse") == "mse" else 0)
         return o.get("epochs", 1) * per_epoch + 18 * d
+    if inp.kind == "linear" and o.get("gate"):
+        # the rate gate: theta_h . x_t over the model width H d (2 H d), then the layer
+        return 2 * inp.H * d + 6 * d * d + (2 * (b + 1) * d if inp.causal else 0)
     if inp.kind == "linear" and o.get("ln"):
         # plus the inner norm: statistics, normalisation and its backward on k W (about
         # 12 d) and on q W (about 6 d)
@@ -90,6 +93,9 @@ def bytes_per_launch(inp):
         n += BH * T * 4
     nparam = sum(p.numel() for p in inp.params.values()) // inp.H  # one head's set
     n += inp.H * nparam * 4 + BH * nparam * 4
+    if inp.gate_x is not None:
+        # the gate reads x and its vectors once and writes the rates, which the layer reads
+        n += inp.gate_x.numel() * 2 + inp.gate_theta.numel() * 2 + 2 * BH * T * 4
     return n
 
 
@@ -210,7 +216,11 @@ def run_ours(args, rank, world, inp, peaks):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
-    eta = inp.eta.to(dev) if inp.eta is not None else None
+    # the per-token input of the rate: eta itself, or the layer input x of the gate
+    gate = inp.gate_x is not None
+    eta_src = inp.gate_x if gate else inp.eta
+    eta = eta_src.to(dev) if eta_src is not None else None
+    theta = inp.gate_theta.to(dev) if gate else None
     params = {n: p.to(dev) for n, p in inp.params.items()}
     z = torch.empty_like(q)
     B, H, d = inp.B, inp.H, inp.d
@@ -230,6 +240,8 @@ def run_ours(args, rank, world, inp, peaks):
             return [torch.empty((B, H, d, d), device=dev)]
 
         def step(qq=q, kk=k, vv=v, ee=eta, zz=z, oo=(outs,), wsp=ws):
+            if gate:  # ee holds x: the rates come from the gate, every step
+                ee = abi.ttt_eta_gate(ee, theta, inp.eta_scalar)
             if wsp is not None:
                 abi.ttt_linear_fwd_seqpar(qq, kk, vv, params["W0"], inp.b, inp.causal, eta=ee,
                                           eta_scalar=inp.eta_scalar, z=zz, W_out=oo[0], workspace=wsp)
@@ -324,7 +336,7 @@ def run_ours(args, rank, world, inp, peaks):
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
-        he = inp.eta.pin_memory() if inp.eta is not None else None
+        he = eta_src.pin_memory() if eta_src is not None else None
         lanes = []
         for _ in range(E2E_STREAMS):
             ln = {"s": torch.cuda.Stream(device=dev), "q": torch.empty_like(q), "k": torch.empty_like(k),
@@ -357,7 +369,7 @@ def run_ours(args, rank, world, inp, peaks):
         if world > 1:
             e2e_ms = allreduce_max(e2e_ms, dev)
         h2d = sum(x.numel() * x.element_size() for x in (inp.q, inp.k, inp.v))
-        h2d += inp.eta.numel() * 4 if inp.eta is not None else 0
+        h2d += eta_src.numel() * eta_src.element_size() if eta_src is not None else 0
         d2h = sum(t.numel() * t.element_size() for t in out_bytes)
         e2e = {"value": world * inp.token_heads / (e2e_ms / 1e3), "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
@@ -372,6 +384,7 @@ def run_ours(args, rank, world, inp, peaks):
 def oracle_sample(inp, budget_s):
     """Times the fp64 oracle on whole (batch, head) chains of the workload, adding
     chains until about budget_s of CPU work; returns (token-heads/s, threads, desc)."""
+    import numpy as np
     import oracle
     oracle.build()
     threads = os.cpu_count() or 1
@@ -386,6 +399,10 @@ def oracle_sample(inp, budget_s):
         eta = flat(inp.eta) if inp.eta is not None else None
         t0 = time.perf_counter()
         o = inp.options
+        if inp.gate_x is not None:  # the rates of the sampled chains from the gate
+            eta = torch.from_numpy(np.stack([oracle.eta_gate(inp.gate_x[c // inp.H:c // inp.H + 1],
+                                                             inp.gate_theta[c % inp.H:c % inp.H + 1],
+                                                             inp.eta_scalar)[0, 0] for c in sel]))[None]
         if inp.kind == "linear":
             W0 = torch.stack([inp.params["W0"][c % inp.H] for c in sel]).unsqueeze(0)
             ln = {}
@@ -449,7 +466,9 @@ def main():
     flops = flops_per_token_head(inp) * inp.token_heads
     config = {"workload": args.workload, "kind": inp.kind, "B": inp.B, "H": inp.H, "T": inp.T,
               "d": inp.d, "m": inp.m or None, "mini_batch": inp.b, "causal": inp.causal,
-              "eta": "per-token sigmoid(g)" if inp.eta is not None else inp.eta_scalar,
+              "eta": ("per-token sigmoid(g)" if inp.eta is not None else
+                      f"per-token {inp.eta_scalar} sigmoid(theta_h . x_t), x of width {inp.H * inp.d} (ttt_eta_gate)"
+                      if inp.gate_x is not None else inp.eta_scalar),
               "io_dtype": str(inp.q.dtype).replace("torch.", ""),
               "state_dtype": "float32", "l2": "flushed before every timed step (256 MiB write + 256 MiB read)",
               "parallelism": f"weak: every rank runs its own {inp.B}x{inp.H} chains"}

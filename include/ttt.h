@@ -243,6 +243,30 @@ ttt_status ttt_dwconv_fwd(const ttt_dwconv_desc *desc,
                           const float *eta, float eta_scalar,
                           const float *W0, void *z, float *W_out, void *stream);
 
+/* Input-dependent inner learning rate problem description. */
+typedef struct {
+    int B, T;                  /* batch, tokens per sequence                            */
+    int H;                     /* heads, 1 .. 64 (TTT_ERR_UNSUPPORTED above)            */
+    int dm;                    /* width of the layer's input tokens, a multiple of 8
+                                  (TTT_ERR_UNSUPPORTED otherwise)                       */
+} ttt_gate_desc;
+
+/*
+ * The inner learning rate as a function of the input token ("Learning to (Learn at
+ * Test Time)" walkthrough, section 2.2.3): a learnable vector of the outer loop per
+ * head, a sigmoid, and a base rate (1 for TTT-Linear, 0.1 for TTT-MLP):
+ *     eta[b,h,t] = eta_base * sigma(theta[h] . x[b,t]),  sigma(a) = 1 / (1 + e^-a)
+ *   x     : [B,T,dm] bf16, the layer's input tokens, 16-byte aligned
+ *   theta : [H,dm] bf16, one vector per head, 16-byte aligned
+ *   eta   : [B,H,T] fp32 (written), 4-byte aligned: the per-token rates that
+ *           ttt_linear_fwd, ttt_linear_fwd_seqpar and ttt_mlp_fwd read
+ * The dot products accumulate in fp32 from the bf16 operands.  All pointers are
+ * device memory owned by the caller; eta must not overlap x or theta (TTT_ERR_ARG).
+ * B = 0 or T = 0 queues nothing.  Misaligned pointers: TTT_ERR_ALIGN.
+ */
+ttt_status ttt_eta_gate(const ttt_gate_desc *desc, const void *x, const void *theta, float eta_base,
+                        float *eta, void *stream);
+
 /* Waits for `stream`, then reports (and clears) a kernel wait timeout recorded on
  * the current device, or a CUDA error seen while waiting. */
 ttt_status ttt_sync_status(void *stream);

@@ -21,7 +21,7 @@ STATUS = {0: "TTT_OK", -1: "TTT_ERR_ARG", -2: "TTT_ERR_UNSUPPORTED", -3: "TTT_ER
 
 # every symbol include/ttt.h declares
 EXPORTS = ("ttt_linear_fwd", "ttt_linear_seqpar_workspace", "ttt_linear_fwd_seqpar",
-           "ttt_linear_fwd_seqpar_noalloc", "ttt_dwconv_fwd",
+           "ttt_linear_fwd_seqpar_noalloc", "ttt_dwconv_fwd", "ttt_eta_gate",
            "ttt_mlp_fwd", "ttt_sync_status", "ttt_status_str", "ttt_launch_count")
 
 
@@ -49,6 +49,10 @@ class MlpDesc(ctypes.Structure):
                 ("params_per_batch", ctypes.c_int), ("activation", ctypes.c_int)]
 
 ACTIVATIONS = {"silu": 0, "gelu": 1}
+
+
+class GateDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int), ("dm", ctypes.c_int)]
 
 
 class TTTError(RuntimeError):
@@ -84,6 +88,8 @@ def lib():
         L.ttt_mlp_fwd.argtypes = [ctypes.POINTER(MlpDesc), vp, vp, vp, fp, f, fp, fp, fp, fp,
                                   vp, fp, fp, fp, fp, vp]
         L.ttt_mlp_fwd.restype = ctypes.c_int
+        L.ttt_eta_gate.argtypes = [ctypes.POINTER(GateDesc), vp, vp, f, fp, vp]
+        L.ttt_eta_gate.restype = ctypes.c_int
         L.ttt_sync_status.argtypes = [vp]
         L.ttt_sync_status.restype = ctypes.c_int
         L.ttt_status_str.argtypes = [ctypes.c_int]
@@ -287,6 +293,31 @@ def ttt_mlp_fwd(q, k, v, W1, c1, W2, c2, mini_batch, causal=True, eta=None, eta_
     if rc != 0:
         raise TTTError("ttt_mlp_fwd", rc)
     return z, outs
+
+
+def ttt_eta_gate(x, theta, eta_base=1.0, eta=None, stream=None):
+    """Input-dependent inner learning rate eta[b,h,t] = eta_base * sigmoid(theta[h] .
+    x[b,t]).  x: bf16 [B,T,dm] (the layer's input tokens); theta: bf16 [H,dm] (one
+    vector per head).  Returns eta, fp32 [B,H,T] (the layout the TTT entry points
+    read)."""
+    for name, t in (("x", x), ("theta", theta)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor (no CPU path)")
+    if x.dim() != 3 or theta.dim() != 2 or theta.shape[1] != x.shape[2]:
+        raise ValueError("x must be [B,T,dm] and theta [H,dm]")
+    B, T, dm = x.shape
+    H = theta.shape[0]
+    if eta is None:
+        eta = torch.empty((B, H, T), device=x.device, dtype=torch.float32)
+    eta = _f32(eta, "eta")
+    if eta.shape != (B, H, T):
+        raise ValueError("eta must be [B,H,T]")
+    desc = GateDesc(B, T, H, dm)
+    rc = lib().ttt_eta_gate(ctypes.byref(desc), _ptr(x), _ptr(theta), float(eta_base), _ptr(eta),
+                            _stream(stream))
+    if rc != 0:
+        raise TTTError("ttt_eta_gate", rc)
+    return eta
 
 
 def ttt_sync_status(stream=None):

@@ -407,6 +407,35 @@ ttt_status ttt_dwconv_fwd(const ttt_dwconv_desc *desc, const void *q, const void
     return code(rc);
 }
 
+ttt_status ttt_eta_gate(const ttt_gate_desc *desc, const void *x, const void *theta, float eta_base,
+                        float *eta, void *stream)
+{
+    if (!desc) return TTT_ERR_ARG;
+    const ttt_gate_desc D = *desc;
+    if (D.B < 0 || D.T < 0 || D.H < 1 || D.dm < 1) return TTT_ERR_ARG;
+    if (D.B == 0 || D.T == 0) return TTT_OK;
+    if (!x || !theta || !eta) return TTT_ERR_ARG;
+    if (D.H > 64 || D.dm % 8 != 0 || D.B > 65535) return TTT_ERR_UNSUPPORTED;
+    if (!aligned(x, 16) || !aligned(theta, 16) || !aligned(eta, 4)) return TTT_ERR_ALIGN;
+    const size_t nx = (size_t)D.B * D.T * D.dm * 2, nth = (size_t)D.H * D.dm * 2, ne = (size_t)D.B * D.H * D.T * 4;
+    if (overlaps(eta, ne, x, nx) || overlaps(eta, ne, theta, nth)) return TTT_ERR_ARG;
+    ttt::GateArgs a;
+    a.B = D.B;
+    a.T = D.T;
+    a.H = D.H;
+    a.dm = D.dm;
+    a.x = x;
+    a.theta = theta;
+    a.eta_base = eta_base;
+    a.eta = eta;
+    a.status = status_word();
+    a.stream = static_cast<cudaStream_t>(stream);
+    if (!a.status) return TTT_ERR_LAUNCH;
+    const int rc = ttt::launch_eta_gate(a);
+    if (rc == 0) g_launches.fetch_add(1, std::memory_order_relaxed);
+    return code(rc);
+}
+
 ttt_status ttt_sync_status(void *stream)
 {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTT_ERR_LAUNCH;

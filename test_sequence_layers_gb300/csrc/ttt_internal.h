@@ -49,6 +49,15 @@ struct DwconvArgs {
     cudaStream_t stream;
 };
 
+struct GateArgs {
+    int B, T, H, dm;
+    const void *x, *theta;  // bf16 [B][T][dm], [H][dm]
+    float eta_base;
+    float *eta;             // fp32 [B][H][T]
+    int *status;            // device status word (timeouts)
+    cudaStream_t stream;
+};
+
 // TMA descriptor of a bf16 token tensor viewed as [BH][T][d]: boxes of `rows`
 // tokens x `cols` features (0: min(d, 64)), swizzled to the box row length, rows
 // past T zero-filled on loads and dropped on stores.  Returns false if the driver
@@ -109,6 +118,7 @@ int launch_linear_seqpar_serial(const LinearArgs &a, const SeqparPlan &pl, void 
 // one CTA and the launch.
 size_t dwconv_smem(int hh, int ww, int d, int es);
 int launch_dwconv(const DwconvArgs &a);
+int launch_eta_gate(const GateArgs &a);  // H <= 64; -2 otherwise
 
 // Largest d*m the fp32 MLP path holds on chip.
 bool mlp_f32_fits(int d, int m);

@@ -14,6 +14,9 @@ sets -- Pile, Books3, ImageNet -- are not used):
     sigmoid(g_t) with g_t ~ N(0, 1) (the input-dependent learning rate of the
     "Learning to (Learn at Test Time)" walkthrough, section 2.2.3, with the gate's
     projection replaced by a random draw).
+  * gate inputs (``gate_inputs``): layer input tokens x ~ N(0, 1) of the model
+    width, bf16, and one gate vector per head ~ N(0, 1/width), bf16, so that the
+    gate's argument theta . x is O(1) (the sigmoid's working range).
   * inner weights ~ N(0, 0.02^2), biases zero, one set per head shared over the
     batch (the learnable initial weights are shared across sequences, same
     walkthrough, section 2.2.2).
@@ -45,6 +48,9 @@ WORKLOADS = {
     "mlp_125m_gelu": ("mlp", 8, 12, 2048, 64, 256, 16, True, torch.bfloat16, 0.1, 10),
     "vision_dwconv": ("dwconv", 256, 6, 196, 64, 0, 196, False, torch.bfloat16, 1.0, 7),
     "linear_125m_ln": ("linear", 8, 12, 2048, 64, 0, 16, True, torch.bfloat16, 1.0, 11),
+    # the long gated context with the rate computed from the layer input (model width
+    # H d = 2048) by the gate, every step
+    "linear_long_gate_x": ("linear", 2, 32, 32768, 64, 0, 16, True, torch.bfloat16, 1.0, 12),
 }
 
 # options beyond the base layer: inner loss ("dot"), inner epochs, MLP activation,
@@ -55,6 +61,7 @@ OPTIONS = {
     "mlp_125m_gelu": {"activation": "gelu"},                # the walkthrough's TTT-MLP
     "vision_dwconv": {"height": 14, "width": 14, "loss": "dot"},  # ViT3: depthwise conv, dot loss
     "linear_125m_ln": {"ln": True},                         # x + LN(x W): the walkthrough's TTT-Linear
+    "linear_long_gate_x": {"gate": True},                   # eta = eta_base sigma(theta_lr . x)
 }
 
 
@@ -75,6 +82,8 @@ class Inputs:
     eta_scalar: float
     params: dict = field(default_factory=dict)   # fp32 CPU tensors: W0 | W1,c1,W2,c2
     options: dict = field(default_factory=dict)  # loss, epochs, activation, height, width
+    gate_x: torch.Tensor | None = None      # [B,T,H d] bf16 layer input of the rate gate
+    gate_theta: torch.Tensor | None = None  # [H,H d] bf16 gate vectors (eta_base = eta_scalar)
 
     @property
     def token_heads(self) -> int:
@@ -136,4 +145,15 @@ def workload(name, **override):
     kw.setdefault("ln", bool(OPTIONS.get(name, {}).get("ln", False)))
     inp = make(**kw)
     inp.options = dict(OPTIONS.get(name, {}))
+    if inp.options.get("gate"):  # drawn after the layer's inputs, from a seed of its own
+        inp.gate_x, inp.gate_theta = gate_inputs(inp.B, inp.T, inp.H, inp.H * inp.d, seed=kw["seed"] + 1000)
     return inp
+
+
+def gate_inputs(B, T, H, dm, seed=0):
+    """Layer input tokens x [B,T,dm] and per-head gate vectors theta [H,dm], both bf16
+    on the CPU (x drawn first)."""
+    g = torch.Generator().manual_seed(seed)
+    x = _normal((B, T, dm), g).to(torch.bfloat16)
+    theta = (torch.randn((H, dm), generator=g) / dm ** 0.5).to(torch.bfloat16)
+    return x, theta

@@ -148,3 +148,26 @@ def test_dwconv_rejects_bad_arguments(L):
     assert call(w0_batch_stride=5) == -1
     assert call(d=12) == -2                      # channels must be a multiple of 8
     assert call(height=64, width=64) == -2       # the sequence does not fit on chip
+
+
+def test_eta_gate_rejects_bad_arguments(L):
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+
+    def call(x=FAKE, theta=FAKE, eta=FAKE + (1 << 26), **kw):
+        d = dict(B=2, T=100, H=32, dm=2048)
+        d.update(kw)
+        desc = abi.GateDesc(**d)
+        return L.ttt_eta_gate(ctypes.byref(desc), vp(x), vp(theta), 1.0, vp(eta), None)
+
+    assert L.ttt_eta_gate(None, None, None, 1.0, None, None) == -1
+    assert call(B=-1) == -1
+    assert call(H=0) == -1
+    assert call(dm=0) == -1
+    assert call(B=0) == 0 and call(T=0, x=None) == 0   # nothing to queue
+    assert call(x=None) == -1
+    assert call(H=65) == -2                             # heads past 64
+    assert call(dm=100) == -2                           # width not a multiple of 8
+    assert call(x=FAKE + 8) == -3
+    assert call(theta=FAKE + 2) == -3
+    assert call(eta=FAKE + (1 << 26) + 2) == -3
+    assert call(eta=FAKE + 64) == -1                    # eta overlaps x
