@@ -43,7 +43,7 @@ def _load():
                                           dp, dp, d]
         lib.ttt_oracle_linear.restype = i
         lib.ttt_oracle_mlp.argtypes = [i, i, i, i, i, i, i, dp, dp, dp, dp, d,
-                                       dp, dp, dp, dp, i, dp, dp, dp, dp, dp, i, i]
+                                       dp, dp, dp, dp, i, dp, dp, dp, dp, dp, i, i, dp, dp, d]
         lib.ttt_oracle_mlp.restype = i
         lib.ttt_oracle_dwconv.argtypes = [i, i, i, i, i, i, i, dp, dp, dp, dp, d, dp, ll, dp, dp, i]
         lib.ttt_oracle_dwconv.restype = i
@@ -105,11 +105,11 @@ def linear(q, k, v, W0, b, causal=True, eta=None, eta_scalar=1.0, loss="mse",
 
 
 def mlp(q, k, v, W1, c1, W2, c2, b, causal=True, eta=None, eta_scalar=0.1, threads=None,
-        activation="silu"):
+        activation="silu", ln_gamma=None, ln_beta=None, ln_eps=1e-6):
     """TTT-MLP forward, fp64, f(x) = act(x W1 + c1) W2 + c2, act "silu" or "gelu"
-    (erf form).  Parameters are given per head ([H,...], shared over the batch) or
-    per (batch, head) ([B,H,...]).  Returns (z, W1_final, c1_final, W2_final,
-    c2_final)."""
+    (erf form); with ln_gamma, ln_beta [H,d]: f(x) = x + LN(act(x W1 + c1) W2 + c2).
+    Parameters are given per head ([H,...], shared over the batch) or per (batch,
+    head) ([B,H,...]).  Returns (z, W1_final, c1_final, W2_final, c2_final)."""
     q, k, v, eta = _f64(q), _f64(k), _f64(v), _f64(eta)
     W1, c1, W2, c2 = _f64(W1), _f64(c1), _f64(W2), _f64(c2)
     B, H, T, d = q.shape
@@ -120,6 +120,9 @@ def mlp(q, k, v, W1, c1, W2, c2, b, causal=True, eta=None, eta_scalar=0.1, threa
     assert W2.shape == lead + (m, d) and c2.shape == lead + (d,)
     if eta is not None:
         assert eta.shape == (B, H, T)
+    gam, bet = _f64(ln_gamma), _f64(ln_beta)
+    if gam is not None:
+        assert gam.shape == (H, d) and bet.shape == (H, d)
     z = np.zeros((B, H, T, d))
     W1o, c1o = np.zeros((B, H, d, m)), np.zeros((B, H, m))
     W2o, c2o = np.zeros((B, H, m, d)), np.zeros((B, H, d))
@@ -127,7 +130,8 @@ def mlp(q, k, v, W1, c1, W2, c2, b, causal=True, eta=None, eta_scalar=0.1, threa
                                 _ptr(q), _ptr(k), _ptr(v), _ptr(eta), float(eta_scalar),
                                 _ptr(W1), _ptr(c1), _ptr(W2), _ptr(c2), per_batch,
                                 _ptr(z), _ptr(W1o), _ptr(c1o), _ptr(W2o), _ptr(c2o),
-                                threads or default_threads(), {"silu": 0, "gelu": 1}[activation])
+                                threads or default_threads(), {"silu": 0, "gelu": 1}[activation],
+                                _ptr(gam), _ptr(bet), float(ln_eps))
     if rc != 0:
         raise ValueError("ttt_oracle_mlp rejected its arguments")
     return z, W1o, c1o, W2o, c2o

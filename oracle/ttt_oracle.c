@@ -39,6 +39,9 @@
  *
  * Inner models (walkthrough section 2.2.1; ViT3 article observation 4):
  *   linear: f(x; W) = x W, W in R^{d x d} (row convention, x is a 1 x d row).
+ *   norm (mlp): f(x) = x + LN(act(x W1 + c1) W2 + c2) with the same LN and gradient
+ *   rule (the walkthrough's TTT-MLP carries the norm and residual too); the MLP's
+ *   backward then starts from dy instead of e.
  *   mlp   : f(x) = act(x W1 + c1) W2 + c2, W1 d x m, c1 1 x m, W2 m x d, c2 1 x d,
  *           act = SiLU, SiLU(h) = h * sigma(h) (ViT3 article, observation 4), or
  *           act = GELU, GELU(h) = h * Phi(h) with Phi the standard normal CDF
@@ -252,9 +255,50 @@ typedef struct {
     const double *W1, *c1, *W2, *c2;
     int per_batch;
     double *z, *W1o, *c1o, *W2o, *c2o;
+    const double *ln_gamma, *ln_beta;  /* [H][d] inner norm x + LN(mlp(x)), or NULL */
+    double ln_eps;
     int next;
     pthread_mutex_t lock;
 } mlp_job;
+
+/* With the inner norm, f(x) = x + LN(y), y = the MLP's output row (length d):
+ * replaces the residual row r = y - v by dL/dy for l = 1/2 ||x + LN(y) - v||^2, in
+ * place (the same formula as the linear model's norm: g = gamma e,
+ * dy = (g - mean(g) - yh mean(g yh)) / s with e = x + LN(y) - v); yh is scratch. */
+static void mlp_ln_grad(int d, const double *gm, const double *bt, double eps, const double *x,
+                        const double *vt, double *r, double *yh)
+{
+    double mu = 0.0, var = 0.0;
+    for (int j = 0; j < d; ++j) r[j] += vt[j];  /* back to y */
+    for (int j = 0; j < d; ++j) mu += r[j];
+    mu /= d;
+    for (int j = 0; j < d; ++j) var += (r[j] - mu) * (r[j] - mu);
+    var /= d;
+    const double sd = sqrt(var + eps);
+    double mg = 0.0, mgy = 0.0;
+    for (int j = 0; j < d; ++j) {
+        yh[j] = (r[j] - mu) / sd;
+        const double e = x[j] + gm[j] * yh[j] + bt[j] - vt[j];
+        r[j] = gm[j] * e;
+        mg += r[j];
+        mgy += r[j] * yh[j];
+    }
+    mg /= d;
+    mgy /= d;
+    for (int j = 0; j < d; ++j) r[j] = (r[j] - mg - yh[j] * mgy) / sd;
+}
+
+/* z = x + LN(y) in place of the MLP output row y */
+static void mlp_ln_out(int d, const double *gm, const double *bt, double eps, const double *x, double *y)
+{
+    double mu = 0.0, var = 0.0;
+    for (int j = 0; j < d; ++j) mu += y[j];
+    mu /= d;
+    for (int j = 0; j < d; ++j) var += (y[j] - mu) * (y[j] - mu);
+    var /= d;
+    const double sd = sqrt(var + eps);
+    for (int j = 0; j < d; ++j) y[j] = x[j] + gm[j] * (y[j] - mu) / sd + bt[j];
+}
 
 /* z = act(x W1 + c1) W2 + c2 with scratch h (length m) */
 static void mlp_forward(int act, int d, int m, const double *x, const double *W1, const double *c1,
@@ -289,6 +333,9 @@ static void mlp_chain(const mlp_job *J, int bh)
     double *c2 = malloc(sizeof(double) * d), *c2s = malloc(sizeof(double) * d);
     double *h = malloc(sizeof(double) * m), *a = malloc(sizeof(double) * m);
     double *g = malloc(sizeof(double) * m), *e = malloc(sizeof(double) * d);
+    double *yh = malloc(sizeof(double) * d);
+    const double *gm = J->ln_gamma ? J->ln_gamma + (size_t)hi * d : NULL;
+    const double *bt = J->ln_beta ? J->ln_beta + (size_t)hi * d : NULL;
     memcpy(W1, J->W1 + hp * d * m, sizeof(double) * d * m);
     memcpy(c1, J->c1 + hp * m, sizeof(double) * m);
     memcpy(W2, J->W2 + hp * m * d, sizeof(double) * m * d);
@@ -315,6 +362,7 @@ static void mlp_chain(const mlp_job *J, int bh)
                 for (int i = 0; i < m; ++i) s += a[i] * W2s[i * d + j];
                 e[j] = s - vt[j];
             }
+            if (gm) mlp_ln_grad(d, gm, bt, J->ln_eps, kt, vt, e, yh);  /* e := dL/dy */
             /* backward: g = (e W2s^T) * act'(h) */
             for (int i = 0; i < m; ++i) {
                 double s = 0.0;
@@ -333,19 +381,23 @@ static void mlp_chain(const mlp_job *J, int bh)
             for (int i = 0; i < d; ++i)
                 for (int j = 0; j < m; ++j) W1[i * m + j] -= et * kt[i] * g[j];
             for (int j = 0; j < m; ++j) c1[j] -= et * g[j];
-            if (J->causal)
+            if (J->causal) {
                 mlp_forward(J->act, d, m, q + (size_t)t * d, W1, c1, W2, c2, h, z + (size_t)t * d);
+                if (gm) mlp_ln_out(d, gm, bt, J->ln_eps, q + (size_t)t * d, z + (size_t)t * d);
+            }
         }
         if (!J->causal)
-            for (int t = n0; t < n1; ++t)
+            for (int t = n0; t < n1; ++t) {
                 mlp_forward(J->act, d, m, q + (size_t)t * d, W1, c1, W2, c2, h, z + (size_t)t * d);
+                if (gm) mlp_ln_out(d, gm, bt, J->ln_eps, q + (size_t)t * d, z + (size_t)t * d);
+            }
     }
     if (J->W1o) memcpy(J->W1o + (size_t)bh * d * m, W1, sizeof(double) * d * m);
     if (J->c1o) memcpy(J->c1o + (size_t)bh * m, c1, sizeof(double) * m);
     if (J->W2o) memcpy(J->W2o + (size_t)bh * m * d, W2, sizeof(double) * m * d);
     if (J->c2o) memcpy(J->c2o + (size_t)bh * d, c2, sizeof(double) * d);
     free(W1); free(W1s); free(W2); free(W2s); free(c1); free(c1s); free(c2); free(c2s);
-    free(h); free(a); free(g); free(e);
+    free(h); free(a); free(g); free(e); free(yh);
 }
 
 static void *mlp_worker(void *arg)
@@ -367,13 +419,13 @@ int ttt_oracle_mlp(int B, int H, int T, int d, int m, int b, int causal,
                    const double *W1, const double *c1, const double *W2, const double *c2,
                    int per_batch,
                    double *z, double *W1o, double *c1o, double *W2o, double *c2o,
-                   int nthreads, int act)
+                   int nthreads, int act, const double *ln_gamma, const double *ln_beta, double ln_eps)
 {
     if (B < 0 || H < 0 || T < 0 || d <= 0 || m <= 0 || b <= 0 || !W1 || !c1 || !W2 || !c2 ||
-        (T > 0 && (!q || !k || !v || !z)) || (act != 0 && act != 1))
+        (T > 0 && (!q || !k || !v || !z)) || (act != 0 && act != 1) || (!ln_gamma != !ln_beta))
         return -1;
     mlp_job J = {B, H, T, d, m, b, causal ? 1 : 0, act, q, k, v, eta, eta_scalar,
-                 W1, c1, W2, c2, per_batch ? 1 : 0, z, W1o, c1o, W2o, c2o, 0};
+                 W1, c1, W2, c2, per_batch ? 1 : 0, z, W1o, c1o, W2o, c2o, ln_gamma, ln_beta, ln_eps, 0};
     pthread_mutex_init(&J.lock, NULL);
     if (nthreads < 1) nthreads = 1;
     pthread_t *th = malloc(sizeof(pthread_t) * nthreads);

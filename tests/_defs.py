@@ -30,6 +30,17 @@ def make_f_linear_ln(gamma, beta, eps=1e-6):
     return f
 
 
+def make_f_mlp_ln(gamma, beta, activation="silu", eps=1e-6):
+    """f(x) = x + LN(act(x W1 + c1) W2 + c2) with fixed scale / shift (torch's layer_norm)."""
+    act = silu_t if activation == "silu" else torch.nn.functional.gelu
+
+    def f(x, P):
+        W1, c1, W2, c2 = P
+        y = act(x @ W1 + c1) @ W2 + c2
+        return x + torch.nn.functional.layer_norm(y, (y.shape[-1],), gamma, beta, eps)
+    return f
+
+
 def f_mlp_gelu(x, P):
     W1, c1, W2, c2 = P
     return torch.nn.functional.gelu(x @ W1 + c1) @ W2 + c2

@@ -498,3 +498,31 @@ def test_eta_gate_symmetry_and_saturation():
     ones = np.ones((1, 3, 4))
     assert np.all(oracle.eta_gate(ones, np.full((1, 4), 10.0), 1.0) == 1.0)
     assert np.all(oracle.eta_gate(ones, np.full((1, 4), -10.0), 1.0) < 1e-17)
+
+
+# ------------------------------------------------ inner layer norm + residual (MLP)
+
+
+@pytest.mark.parametrize("activation", ["silu", "gelu"])
+@pytest.mark.parametrize("T,b,causal", [(11, 1, True), (11, 4, True), (12, 4, False), (9, 9, False),
+                                        (10, 16, True)])
+def test_mlp_layer_norm_residual_matches_definition_autograd(T, b, causal, activation):
+    """f(x) = x + LN(act(x W1 + c1) W2 + c2) (the walkthrough's TTT-MLP, section 2.2.1):
+    the oracle's hand LN backward, fed into the MLP's backward, equals the layer's
+    definition with torch's layer_norm and autograd, every mini-batch size, both masks."""
+    B, H, d, m = 1, 2, 6, 16
+    q, k, v = _qkv(B, H, T, d)
+    W1, c1, W2, c2 = _mlp_params(H, d, m)
+    eta = rng.uniform(0.1, 1.0, (B, H, T))
+    gam = rng.uniform(0.5, 1.5, (H, d))
+    bet = rng.standard_normal((H, d)) * 0.1
+    out = oracle.mlp(q, k, v, W1, c1, W2, c2, b=b, causal=causal, eta=eta, activation=activation,
+                     ln_gamma=gam, ln_beta=bet)
+    t = lambda a: torch.tensor(a)
+    for h in range(H):
+        f = _defs.make_f_mlp_ln(t(gam[h]), t(bet[h]), activation)
+        zr, Pr = _defs.definition_autograd(f, [t(W1[h]), t(c1[h]), t(W2[h]), t(c2[h])], t(q[0, h]),
+                                           t(k[0, h]), t(v[0, h]), t(eta[0, h]), b, causal)
+        np.testing.assert_allclose(out[0][0, h], zr.numpy(), rtol=1e-10, atol=1e-11)
+        for got, ref in zip(out[1:], Pr):
+            np.testing.assert_allclose(got[0, h], ref.numpy(), rtol=1e-10, atol=1e-11)
