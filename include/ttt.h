@@ -196,10 +196,19 @@ typedef struct {
     int params_per_batch;      /* 0: W1,c1,W2,c2 are [H,...] shared over the batch;
                                   1: they are [B,H,...]                                */
     int activation;            /* ttt_activation (0 = TTT_ACT_SILU)                    */
+    const float *ln_gamma;     /* inner layer norm + residual: f(x) = x + LN(act(x W1 +
+                                  c1) W2 + c2), LN over the d outputs as in
+                                  ttt_linear_desc ("Learning to (Learn at Test Time)"
+                                  walkthrough, section 2.2.1); [H,d] fp32 device arrays,
+                                  fixed, or both NULL for the plain MLP.  fp32 I/O only
+                                  (bf16: TTT_ERR_UNSUPPORTED)                           */
+    const float *ln_beta;
+    float ln_eps;              /* > 0 when the norm is used                             */
 } ttt_mlp_desc;
 
 /*
- * TTT-MLP forward, f(x) = act(x W1 + c1) W2 + c2, act = SiLU or GELU (desc->activation).
+ * TTT-MLP forward, f(x) = act(x W1 + c1) W2 + c2, act = SiLU or GELU (desc->activation),
+ * or x + LN(f(x)) with the inner norm (desc->ln_gamma, ln_beta, ln_eps).
  *   W1 [..,d,m], c1 [..,m], W2 [..,m,d], c2 [..,d] fp32 initial inner weights;
  *   the *_out arrays are [B,H,...] fp32 final weights (each may be NULL).
  * Other arguments as for ttt_linear_fwd.

@@ -46,7 +46,8 @@ class MlpDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
                 ("d", ctypes.c_int), ("m", ctypes.c_int), ("mini_batch", ctypes.c_int),
                 ("causal", ctypes.c_int), ("io_dtype", ctypes.c_int),
-                ("params_per_batch", ctypes.c_int), ("activation", ctypes.c_int)]
+                ("params_per_batch", ctypes.c_int), ("activation", ctypes.c_int),
+                ("ln_gamma", ctypes.c_void_p), ("ln_beta", ctypes.c_void_p), ("ln_eps", ctypes.c_float)]
 
 ACTIVATIONS = {"silu": 0, "gelu": 1}
 
@@ -264,8 +265,10 @@ def ttt_dwconv_fwd(q, k, v, W0, height, width, eta=None, eta_scalar=1.0, loss="m
 
 
 def ttt_mlp_fwd(q, k, v, W1, c1, W2, c2, mini_batch, causal=True, eta=None, eta_scalar=0.1,
-                z=None, outs=None, want_W=True, stream=None, activation="silu"):
-    """TTT-MLP forward, f(x) = act(x W1 + c1) W2 + c2, activation "silu" or "gelu".
+                z=None, outs=None, want_W=True, stream=None, activation="silu", ln_gamma=None,
+                ln_beta=None, ln_eps=1e-6):
+    """TTT-MLP forward, f(x) = act(x W1 + c1) W2 + c2, activation "silu" or "gelu"; with
+    ln_gamma, ln_beta (fp32 [H,d], fp32 I/O only): f(x) = x + LN(act(x W1 + c1) W2 + c2).
     Parameters fp32, per head ([H,...]) or per (batch, head) ([B,H,...]).  Returns
     (z, (W1,c1,W2,c2) final or None)."""
     io = _check_tokens(q, k, v)
@@ -285,8 +288,10 @@ def ttt_mlp_fwd(q, k, v, W1, c1, W2, c2, mini_batch, causal=True, eta=None, eta_
         outs = (torch.empty((B, H, d, m), device=dev), torch.empty((B, H, m), device=dev),
                 torch.empty((B, H, m, d), device=dev), torch.empty((B, H, d), device=dev))
     o = outs if outs is not None else (None, None, None, None)
+    ln_gamma, ln_beta = _f32(ln_gamma, "ln_gamma"), _f32(ln_beta, "ln_beta")
     desc = MlpDesc(B, H, T, d, m, int(mini_batch), 1 if causal else 0, io, per_batch,
-                   ACTIVATIONS[activation])
+                   ACTIVATIONS[activation], None if ln_gamma is None else ln_gamma.data_ptr(),
+                   None if ln_beta is None else ln_beta.data_ptr(), float(ln_eps))
     rc = lib().ttt_mlp_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(eta),
                            float(eta_scalar), _ptr(W1), _ptr(c1), _ptr(W2), _ptr(c2), _ptr(z),
                            *(_ptr(t) for t in o), _stream(stream))

@@ -285,8 +285,12 @@ ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc, const void *q, const void *k, c
     if (D.activation != TTT_ACT_SILU && D.activation != TTT_ACT_GELU) return TTT_ERR_ARG;
     if (D.io_dtype != TTT_F32 && D.io_dtype != TTT_BF16) return TTT_ERR_ARG;
     if (D.T > 0 && (!q || !k || !v || !z)) return TTT_ERR_ARG;
+    const bool ln = D.ln_gamma || D.ln_beta;
+    if (ln && (!D.ln_gamma || !D.ln_beta || !(D.ln_eps > 0.f))) return TTT_ERR_ARG;
     if (D.d != 16 && D.d != 32 && D.d != 64) return TTT_ERR_UNSUPPORTED;
     if (D.m % 16 != 0) return TTT_ERR_UNSUPPORTED;
+    if (ln && D.io_dtype != TTT_F32) return TTT_ERR_UNSUPPORTED;
+    if (ln && (!aligned(D.ln_gamma, 4) || !aligned(D.ln_beta, 4))) return TTT_ERR_ALIGN;
     if ((long long)D.B * D.H > 0x7fffffffLL) return TTT_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16)) return TTT_ERR_ALIGN;
     const void *f32p[] = {eta, W1, c1, W2, c2, W1_out, c1_out, W2_out, c2_out};
@@ -311,6 +315,9 @@ ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc, const void *q, const void *k, c
     a.causal = D.causal;
     a.per_batch = D.params_per_batch;
     a.act = D.activation;
+    a.ln_gamma = ln ? D.ln_gamma : nullptr;
+    a.ln_beta = ln ? D.ln_beta : nullptr;
+    a.ln_eps = D.ln_eps;
     a.q = q;
     a.k = k;
     a.v = v;

@@ -26,6 +26,8 @@ struct LinearArgs {
 struct MlpArgs {
     int B, H, T, d, m, b, causal, per_batch;
     int act = 0;  // inner activation: 0 SiLU, 1 GELU
+    const float *ln_gamma = nullptr, *ln_beta = nullptr;  // inner norm [H][d] (null: plain MLP)
+    float ln_eps = 1e-6f;
     const void *q, *k, *v;
     const float *eta;
     float eta_scalar;

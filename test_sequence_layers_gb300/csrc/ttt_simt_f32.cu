@@ -180,6 +180,8 @@ namespace {
 
 struct MlpF32Params {
     int H, T, d, m, b, causal, per_batch, act;  // act: 0 SiLU, 1 GELU (h Phi(h), erf form)
+    const float *ln_gamma, *ln_beta;             // inner norm x + LN(mlp(x)), [H][d] (or null)
+    float ln_eps;
     const float *q, *k, *v, *eta;
     float eta_scalar;
     const float *W1, *c1, *W2, *c2;
@@ -207,12 +209,23 @@ __device__ __forceinline__ float act_d_f32(int act, float h)
 // floats of shared memory used by the fp32 MLP kernel
 __host__ __device__ inline size_t mlp_f32_floats(int d, int m)
 {
-    return 2 * ((size_t)d * m + m + (size_t)m * d + d) + 4 * (size_t)m + 4 * (size_t)d;
+    return 2 * ((size_t)d * m + m + (size_t)m * d + d) + 4 * (size_t)m + 5 * (size_t)d;
 }
 
-// z = act(x W1 + c1) W2 + c2 for the query in xq; hbuf (m) is scratch
+// mean and 1 / sqrt(var + eps) of the n values x (every calling thread reads all)
+__device__ __forceinline__ void row_stats_f32(const float *x, int n, float eps, float &mu, float &rs)
+{
+    float s = 0.f, s2 = 0.f;
+    for (int i = 0; i < n; ++i) s += x[i];
+    mu = s / n;
+    for (int i = 0; i < n; ++i) s2 += (x[i] - mu) * (x[i] - mu);
+    rs = rsqrtf(s2 / n + eps);
+}
+
+// z = act(x W1 + c1) W2 + c2 for the query in xq, or x + LN(that) with the inner
+// norm; hbuf (m) and ybuf (d) are scratch
 __device__ void mlp_query(const MlpF32Params &p, const float *xq, const float *W1, const float *c1,
-                          const float *W2, const float *c2, float *hbuf, float *zrow)
+                          const float *W2, const float *c2, float *hbuf, float *ybuf, float *zrow)
 {
     const int d = p.d, m = p.m, tid = threadIdx.x;
     for (int j = tid; j < m; j += blockDim.x) {
@@ -221,11 +234,25 @@ __device__ void mlp_query(const MlpF32Params &p, const float *xq, const float *W
         hbuf[j] = act_f32(p.act, s);
     }
     __syncthreads();
+    if (!p.ln_gamma) {
+        for (int j = tid; j < d; j += blockDim.x) {
+            float s = c2[j];
+            for (int i = 0; i < m; ++i) s = fmaf(hbuf[i], W2[i * d + j], s);
+            zrow[j] = s;
+        }
+        return;
+    }
+    // z = x + LN(y): y into ybuf, then every thread reads the row's statistics
     for (int j = tid; j < d; j += blockDim.x) {
         float s = c2[j];
         for (int i = 0; i < m; ++i) s = fmaf(hbuf[i], W2[i * d + j], s);
-        zrow[j] = s;
+        ybuf[j] = s;
     }
+    __syncthreads();
+    float mu, rs;
+    row_stats_f32(ybuf, d, p.ln_eps, mu, rs);
+    const float *gm = p.ln_gamma + (size_t)(blockIdx.x % p.H) * d, *bt = p.ln_beta + (size_t)(blockIdx.x % p.H) * d;
+    for (int j = tid; j < d; j += blockDim.x) zrow[j] = xq[j] + fmaf(gm[j], (ybuf[j] - mu) * rs, bt[j]);
 }
 
 __global__ void __launch_bounds__(kThreads) ttt_mlp_f32_kernel(const MlpF32Params p)
@@ -235,8 +262,11 @@ __global__ void __launch_bounds__(kThreads) ttt_mlp_f32_kernel(const MlpF32Param
     float *W1 = sm, *c1 = W1 + d * m, *W2 = c1 + m, *c2 = W2 + m * d;
     float *W1s = c2 + d, *c1s = W1s + d * m, *W2s = c1s + m, *c2s = W2s + m * d;
     float *hh = c2s + d, *aa = hh + m, *gg = aa + m, *hq = gg + m;
-    float *kk = hq + m, *vv = kk + d, *qq = vv + d, *ee = qq + d;
+    float *kk = hq + m, *vv = kk + d, *qq = vv + d, *ee = qq + d, *yh = ee + d;
     const int bh = blockIdx.x;
+    const bool ln = p.ln_gamma != nullptr;
+    const float *gm = ln ? p.ln_gamma + (size_t)(bh % p.H) * d : nullptr;
+    const float *bt = ln ? p.ln_beta + (size_t)(bh % p.H) * d : nullptr;
     const size_t ps = p.per_batch ? (size_t)bh : (size_t)(bh % p.H);
     for (int i = tid; i < d * m; i += nt) {
         W1[i] = p.W1[ps * d * m + i];
@@ -275,7 +305,25 @@ __global__ void __launch_bounds__(kThreads) ttt_mlp_f32_kernel(const MlpF32Param
             for (int j = tid; j < d; j += nt) {
                 float s = c2s[j];
                 for (int i = 0; i < m; ++i) s = fmaf(aa[i], W2s[i * d + j], s);
-                ee[j] = s - vv[j];
+                ee[j] = ln ? s : s - vv[j];
+            }
+            if (ln) {  // e := dL/dy through x + LN(y): dy = (g - mean g - yh mean(g yh)) / s, g = gamma e
+                __syncthreads();
+                float mu, rs;
+                row_stats_f32(ee, d, p.ln_eps, mu, rs);
+                __syncthreads();  // every thread has read y
+                for (int j = tid; j < d; j += nt) {
+                    yh[j] = (ee[j] - mu) * rs;
+                    ee[j] = gm[j] * (kk[j] + fmaf(gm[j], yh[j], bt[j]) - vv[j]);
+                }
+                __syncthreads();
+                float mg = 0.f, mgy = 0.f;
+                for (int j = 0; j < d; ++j) {
+                    mg += ee[j];
+                    mgy += ee[j] * yh[j];
+                }
+                __syncthreads();  // every thread has read g
+                for (int j = tid; j < d; j += nt) ee[j] = (ee[j] - mg / d - yh[j] * (mgy / d)) * rs;
             }
             __syncthreads();
             for (int i = tid; i < m; i += nt) {  // g = (e W2s^T) * act'(h)
@@ -291,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) ttt_mlp_f32_kernel(const MlpF32Param
             for (int i = tid; i < m; i += nt) c1[i] = fmaf(-et, gg[i], c1[i]);
             if (p.causal) {
                 __syncthreads();
-                mlp_query(p, qq, W1, c1, W2, c2, hq, z + (size_t)t * d);
+                mlp_query(p, qq, W1, c1, W2, c2, hq, yh, z + (size_t)t * d);
             }
         }
         if (!p.causal) {
@@ -299,7 +347,7 @@ __global__ void __launch_bounds__(kThreads) ttt_mlp_f32_kernel(const MlpF32Param
                 __syncthreads();
                 for (int i = tid; i < d; i += nt) qq[i] = q[(size_t)t * d + i];
                 __syncthreads();
-                mlp_query(p, qq, W1, c1, W2, c2, hq, z + (size_t)t * d);
+                mlp_query(p, qq, W1, c1, W2, c2, hq, yh, z + (size_t)t * d);
             }
         }
     }
@@ -330,6 +378,9 @@ int launch_mlp_f32(const MlpArgs &a)
     p.causal = a.causal;
     p.per_batch = a.per_batch;
     p.act = a.act;
+    p.ln_gamma = a.ln_gamma;
+    p.ln_beta = a.ln_beta;
+    p.ln_eps = a.ln_eps;
     p.q = static_cast<const float *>(a.q);
     p.k = static_cast<const float *>(a.k);
     p.v = static_cast<const float *>(a.v);

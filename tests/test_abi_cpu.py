@@ -106,6 +106,11 @@ def test_mlp_rejects_bad_arguments(L):
     assert _call_mlp(L, _mlp(), q=FAKE + 4) == -3
     assert _call_mlp(L, _mlp(), W2=FAKE + 1) == -3
     assert _call_mlp(L, _mlp(B=2), W1=FAKE, W1o=FAKE) == -1
+    g = FAKE + (1 << 24)
+    assert _call_mlp(L, _mlp(ln_gamma=g, ln_eps=1e-6)) == -1               # beta missing
+    assert _call_mlp(L, _mlp(io_dtype=abi.TTT_F32, ln_gamma=g, ln_beta=g, ln_eps=0.0)) == -1
+    assert _call_mlp(L, _mlp(ln_gamma=g, ln_beta=g, ln_eps=1e-6)) == -2    # inner norm: fp32 only
+    assert _call_mlp(L, _mlp(io_dtype=abi.TTT_F32, ln_gamma=g + 2, ln_beta=g, ln_eps=1e-6)) == -3
 
 
 def test_binding_refuses_cpu_tensors():

@@ -167,3 +167,38 @@ def test_gelu_inner_model(d, b, causal, T, dtype):
     errs = [G.rel_err(z.double().cpu().numpy(), zr)]
     errs += [G.rel_err(o.double().cpu().numpy(), r) for o, r in zip(outs, Wr) if np.abs(r).max() > 0]
     assert max(errs) <= G.tol_for(inp), errs
+
+
+@pytest.mark.parametrize("activation", ["silu", "gelu"])
+@pytest.mark.parametrize("d,b,causal,T", [(16, 16, True, 40), (16, 5, True, 37), (32, 16, True, 50),
+                                          (32, 8, False, 33), (16, 40, False, 40)])
+def test_fp32_inner_norm(d, b, causal, T, activation):
+    """f(x) = x + LN(act(x W1 + c1) W2 + c2) on the fp32 path against the oracle's
+    hand-derived norm backward, final weights included."""
+    import oracle
+    inp = _mlp_inputs(2, 2, T, d, b, causal, dtype=torch.float32, eta=0.05, seed=90 + d + b, bias=0.1)
+    g = torch.Generator().manual_seed(91 + d)
+    gam = 1.0 + 0.1 * torch.randn((2, d), generator=g)
+    bet = 0.1 * torch.randn((2, d), generator=g)
+    dev = torch.device("cuda")
+    P = [inp.params[n] for n in ("W1", "c1", "W2", "c2")]
+    z, outs = abi.ttt_mlp_fwd(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), *(p.to(dev) for p in P), b, causal,
+                              eta_scalar=inp.eta_scalar, activation=activation, ln_gamma=gam.to(dev),
+                              ln_beta=bet.to(dev))
+    abi.ttt_sync_status()
+    zr, *Wr = oracle.mlp(inp.q, inp.k, inp.v, *P, b, causal, eta_scalar=inp.eta_scalar, activation=activation,
+                         ln_gamma=gam, ln_beta=bet)
+    errs = [G.rel_err(z.double().cpu().numpy(), zr)]
+    errs += [G.rel_err(o.double().cpu().numpy(), r) for o, r in zip(outs, Wr)]
+    assert max(errs) <= G.TOL_F32, errs
+
+
+def test_inner_norm_needs_fp32():
+    inp = _mlp_inputs(1, 1, 32, 16, 16, True, seed=95)
+    dev = torch.device("cuda")
+    P = [inp.params[n].to(dev) for n in ("W1", "c1", "W2", "c2")]
+    one = torch.ones((1, 16), device=dev)
+    with pytest.raises(abi.TTTError) as ei:
+        abi.ttt_mlp_fwd(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), *P, 16, True, ln_gamma=one,
+                        ln_beta=one * 0)
+    assert ei.value.code == -2
