@@ -57,6 +57,8 @@ def flops_per_token_head(inp):
     (b+1)/2 visible pairs per token in a causal block of b)."""
     d, m, b = inp.d, inp.m, inp.b
     o = inp.options
+    if inp.kind == "gate":  # theta_h . x_t over the layer width H d, then the sigmoid
+        return 2 * inp.H * d
     if inp.kind == "dwconv":
         # per channel and epoch: residual 9 FMAs (none for the dot loss), gradient 9
         # FMAs; output 9 FMAs
@@ -88,6 +90,8 @@ def bytes_per_launch(inp):
     per-token eta read, initial weights read once per head, final weights written."""
     es = inp.q.element_size()
     BH, T, d = inp.B * inp.H, inp.T, inp.d
+    if inp.kind == "gate":  # x read once, the gate vectors, the rates written
+        return inp.q.numel() * es + inp.gate_theta.numel() * 2 + BH * T * 4
     n = BH * T * d * es * 4
     if inp.eta is not None:
         n += BH * T * 4
@@ -101,6 +105,8 @@ def bytes_per_launch(inp):
 
 def kernel_name(inp):
     """The kernel the library dispatches this workload to (mirrors the C ABI's choice)."""
+    if inp.kind == "gate":
+        return "ttt_eta_gate_kernel"
     if inp.kind == "dwconv":
         return "ttt_dwconv_kernel"
     if inp.q.element_size() == 4:
@@ -215,14 +221,14 @@ def run_ours(args, rank, world, inp, peaks):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    q, k, v = (x.to(dev) if x is not None else None for x in (inp.q, inp.k, inp.v))
     # the per-token input of the rate: eta itself, or the layer input x of the gate
     gate = inp.gate_x is not None
     eta_src = inp.gate_x if gate else inp.eta
     eta = eta_src.to(dev) if eta_src is not None else None
-    theta = inp.gate_theta.to(dev) if gate else None
+    theta = inp.gate_theta.to(dev) if inp.gate_theta is not None else None
     params = {n: p.to(dev) for n, p in inp.params.items()}
-    z = torch.empty_like(q)
+    z = torch.empty_like(q) if inp.kind != "gate" else None
     B, H, d = inp.B, inp.H, inp.d
     if inp.kind == "linear":
         outs = torch.empty((B, H, d, d), device=dev)
@@ -251,6 +257,16 @@ def run_ours(args, rank, world, inp, peaks):
                                    epochs=epochs, ln_gamma=params.get("ln_gamma"),
                                    ln_beta=params.get("ln_beta"))
         out_bytes = [z, outs]
+    elif inp.kind == "gate":  # the rates alone, from x (held in q)
+        outs = torch.empty((B, H, inp.T), device=dev)
+        ws = None
+
+        def new_outs():
+            return [torch.empty((B, H, inp.T), device=dev)]
+
+        def step(qq=q, kk=None, vv=None, ee=None, zz=None, oo=(outs,), wsp=None):
+            abi.ttt_eta_gate(qq, theta, inp.eta_scalar, eta=oo[0])
+        out_bytes = [outs]
     elif inp.kind == "dwconv":
         outs = torch.empty((B, H, 9, d), device=dev)
         o = inp.options
@@ -335,27 +351,29 @@ def run_ours(args, rank, world, inp, peaks):
     # every step still moves its own inputs and outputs.
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
+        hq, hk, hv = (x.pin_memory() if x is not None else None for x in (inp.q, inp.k, inp.v))
         he = eta_src.pin_memory() if eta_src is not None else None
         lanes = []
         for _ in range(E2E_STREAMS):
-            ln = {"s": torch.cuda.Stream(device=dev), "q": torch.empty_like(q), "k": torch.empty_like(k),
-                  "v": torch.empty_like(v), "e": torch.empty_like(eta) if eta is not None else None,
-                  "z": torch.empty_like(z), "o": new_outs(),
+            like = lambda t: torch.empty_like(t) if t is not None else None
+            ln = {"s": torch.cuda.Stream(device=dev), "q": like(q), "k": like(k),
+                  "v": like(v), "e": like(eta),
+                  "z": like(z), "o": new_outs(),
                   "ws": torch.empty_like(ws) if ws is not None else None}
-            ln["h"] = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in [ln["z"], *ln["o"]]]
+            ln["h"] = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in [ln["z"], *ln["o"]]
+                       if t is not None]
             lanes.append(ln)
 
         def e2e_step(i):
             ln = lanes[i % E2E_STREAMS]
             with torch.cuda.stream(ln["s"]):
-                ln["q"].copy_(hq, non_blocking=True)
-                ln["k"].copy_(hk, non_blocking=True)
-                ln["v"].copy_(hv, non_blocking=True)
+                for dst, src in ((ln["q"], hq), (ln["k"], hk), (ln["v"], hv)):
+                    if dst is not None:
+                        dst.copy_(src, non_blocking=True)
                 if ln["e"] is not None:
                     ln["e"].copy_(he, non_blocking=True)
                 step(ln["q"], ln["k"], ln["v"], ln["e"], ln["z"], ln["o"], ln["ws"])
-                for h, t in zip(ln["h"], [ln["z"], *ln["o"]]):
+                for h, t in zip(ln["h"], [t for t in [ln["z"], *ln["o"]] if t is not None]):
                     h.copy_(t, non_blocking=True)
         for i in range(E2E_STREAMS):
             e2e_step(i)
@@ -368,7 +386,7 @@ def run_ours(args, rank, world, inp, peaks):
         e2e_ms = (time.perf_counter() - t0) * 1e3 / ne
         if world > 1:
             e2e_ms = allreduce_max(e2e_ms, dev)
-        h2d = sum(x.numel() * x.element_size() for x in (inp.q, inp.k, inp.v))
+        h2d = sum(x.numel() * x.element_size() for x in (inp.q, inp.k, inp.v) if x is not None)
         h2d += eta_src.numel() * eta_src.element_size() if eta_src is not None else 0
         d2h = sum(t.numel() * t.element_size() for t in out_bytes)
         e2e = {"value": world * inp.token_heads / (e2e_ms / 1e3), "unit": UNIT,
@@ -388,6 +406,16 @@ def oracle_sample(inp, budget_s):
     import oracle
     oracle.build()
     threads = os.cpu_count() or 1
+    if inp.kind == "gate":  # slices of 1024 tokens of the layer input, every head
+        done, elapsed, S = 0, 0.0, 1024
+        while elapsed < budget_s and done < inp.B * inp.T:
+            b, t = divmod(done, inp.T)
+            t0 = time.perf_counter()
+            oracle.eta_gate(inp.q[b:b + 1, t:t + S], inp.gate_theta, inp.eta_scalar)
+            elapsed += time.perf_counter() - t0
+            done += min(S, inp.T - t)
+        return done * inp.H / elapsed, 1, f"{done} of {inp.B * inp.T} tokens x {inp.H} heads, " \
+                                           f"{elapsed:.1f} s of oracle time (one thread)"
     BH = inp.B * inp.H
     n = min(BH, threads)
     done, elapsed = 0, 0.0
@@ -499,7 +527,7 @@ def main():
     tflops = flops / (ms * 1e-3) / 1e12
     nbytes = bytes_per_launch(inp)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    if inp.kind in ("linear", "dwconv"):  # arithmetic intensity below the ridge
+    if inp.kind in ("linear", "dwconv", "gate"):  # arithmetic intensity below the ridge
         roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": gbs / peaks["hbm_gbs"]}
     else:

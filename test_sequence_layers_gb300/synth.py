@@ -51,6 +51,8 @@ WORKLOADS = {
     # the long gated context with the rate computed from the layer input (model width
     # H d = 2048) by the gate, every step
     "linear_long_gate_x": ("linear", 2, 32, 32768, 64, 0, 16, True, torch.bfloat16, 1.0, 12),
+    # the rate gate alone at that shape (H heads of d: layer width H d = 2048; eta_base 1)
+    "eta_gate_long": ("gate", 2, 32, 32768, 64, 0, 0, False, torch.bfloat16, 1.0, 13),
 }
 
 # options beyond the base layer: inner loss ("dot"), inner epochs, MLP activation,
@@ -67,7 +69,7 @@ OPTIONS = {
 
 @dataclass
 class Inputs:
-    kind: str            # "linear" or "mlp"
+    kind: str            # "linear", "mlp", "dwconv" or "gate"
     B: int
     H: int
     T: int
@@ -108,6 +110,10 @@ def make(kind, B, H, T, d, b, causal, dtype=torch.bfloat16, eta=1.0, seed=0, m=0
     """Draw one input set.  ``eta`` is a float (constant) or "sigmoid"; ``ln`` adds
     the inner layer norm's scale ~ 1 + N(0, 0.1^2) and shift ~ N(0, 0.1^2) per head
     (drawn after the weights, so the other draws do not change)."""
+    if kind == "gate":  # the rate gate alone: q holds the layer input x [B,T,H d]
+        x, theta = gate_inputs(B, T, H, H * d, seed)
+        return Inputs(kind, B, H, T, d, 0, b, False, x, None, None, None, float(eta), {},
+                      gate_theta=theta)
     g = torch.Generator().manual_seed(seed)
     shape = (B, H, T, d)
     q = _unit_rows(_normal(shape, g)).to(dtype)

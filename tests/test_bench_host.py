@@ -35,6 +35,17 @@ def test_mlp_and_gate_work_models():
     assert bench.flops_per_token_head(g) == 2 * dm + 6 * g.d * g.d + 2 * (g.b + 1) * g.d
 
 
+def test_gate_alone_work_model_and_reference_sample():
+    g = synth.workload("eta_gate_long", T=96, B=1, H=4)
+    dm = g.H * g.d
+    assert g.kind == "gate" and g.q.shape == (1, 96, dm) and g.k is None
+    assert bench.bytes_per_launch(g) == 96 * dm * 2 + 4 * dm * 2 + 4 * 96 * 4
+    assert bench.flops_per_token_head(g) == 2 * dm
+    assert bench.kernel_name(g) == "ttt_eta_gate_kernel"
+    v, cores, desc = bench.oracle_sample(g, 0.05)
+    assert v > 0 and cores == 1 and "tokens" in desc
+
+
 @pytest.mark.parametrize("name,kernel", [
     ("linear_125m", "ttt_linear_b16_kernel"), ("linear_125m_b1", "ttt_linear_b1_kernel"),
     ("vision_linear", "ttt_linear_fb_tc_kernel"), ("vision_linear_dot", "ttt_linear_fb_tc_kernel"),
