@@ -94,6 +94,37 @@ def dual_linear(q, k, v, W0, eta, b, causal):
     return z, W
 
 
+def block_form_linear(q, k, v, W0, eta, b, nb):
+    """Causal TTT-Linear over blocks of nb mini-batches of b tokens each, numpy fp64, one
+    chain (q,k,v [T,d], eta [T]); the state moves once per block by a dense affine map.
+
+    With U_i = -diag(eta_i) (K_i W_i - V_i) the step of mini-batch i and W_i = W + sum_{j<i}
+    K_j^T U_j (W the block's start state), the steps of a block solve the block-unit-
+    lower-triangular system (I + L) U = -diag(eta) (K W - V), L_ij = diag(eta_i) K_i K_j^T
+    for j < i.  With T = (I + L)^-1:  U = P W + C, P = -T diag(eta) K, C = T diag(eta) V,
+        W_next = (I + K^T P) W + K^T C                   (the only serial product)
+        Z      = (Q + M.(Q K^T) P) W + M.(Q K^T) C       (M: key s <= query t)
+    so everything but one d x d product per block is independent of the state."""
+    T, d = q.shape
+    W = W0.copy()
+    z = np.zeros((T, d))
+    L = b * nb
+    for s0 in range(0, T, L):
+        s1 = min(s0 + L, T)
+        n = s1 - s0
+        Q, K, V, et = q[s0:s1], k[s0:s1], v[s0:s1], eta[s0:s1]
+        mb = np.arange(n) // b                           # mini-batch of each token
+        Lm = (mb[:, None] > mb[None, :]) * (et[:, None] * (K @ K.T))
+        Tinv = np.linalg.solve(np.eye(n) + Lm, np.eye(n))
+        P = -Tinv @ (et[:, None] * K)
+        C = Tinv @ (et[:, None] * V)
+        M = np.tril(np.ones((n, n)))
+        S = M * (Q @ K.T)
+        z[s0:s1] = (Q + S @ P) @ W + S @ C
+        W = (np.eye(d) + K.T @ P) @ W + K.T @ C
+    return z, W
+
+
 def dual_mlp(q, k, v, W1, c1, W2, c2, eta, b, causal, activation="silu"):
     """TTT-MLP mini-batch step in matrix form (numpy fp64, one chain).  The "+1"
     terms carry the bias writes: c_t = c - sum_{s<=t} eta_s * grad_c l_s."""

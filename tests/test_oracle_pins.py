@@ -526,3 +526,22 @@ def test_mlp_layer_norm_residual_matches_definition_autograd(T, b, causal, activ
         np.testing.assert_allclose(out[0][0, h], zr.numpy(), rtol=1e-10, atol=1e-11)
         for got, ref in zip(out[1:], Pr):
             np.testing.assert_allclose(got[0, h], ref.numpy(), rtol=1e-10, atol=1e-11)
+
+
+# ------------------------------------------- block (several mini-batches) form
+
+
+@pytest.mark.parametrize("T,b,nb", [(64, 16, 4), (70, 16, 4), (45, 4, 3), (33, 8, 1), (50, 5, 10)])
+def test_linear_block_form_equals_token_loop(T, b, nb):
+    """Causal TTT-Linear rewritten per block of nb mini-batches as one affine state map
+    (a block-unit-triangular solve for the steps, then W <- (I + K^T P) W + K^T C): equal
+    to the oracle's token loop to fp64 rounding, ragged tails included."""
+    B, H, d = 1, 2, 8
+    q, k, v = _qkv(B, H, T, d)
+    eta = rng.uniform(0.1, 1.0, (B, H, T))
+    W0 = rng.standard_normal((H, d, d)) * 0.3
+    z, Wf = oracle.linear(q, k, v, W0, b, causal=True, eta=eta)
+    for h in range(H):
+        zb, Wb = _defs.block_form_linear(q[0, h], k[0, h], v[0, h], W0[h], eta[0, h], b, nb)
+        np.testing.assert_allclose(zb, z[0, h], rtol=1e-9, atol=1e-10)
+        np.testing.assert_allclose(Wb, Wf[0, h], rtol=1e-9, atol=1e-10)
