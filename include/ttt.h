@@ -20,9 +20,13 @@
  *                the ViT3 article, observation 2).
  * b = 1 is the delta rule ("Fast weights 与 TTT layers", section 1).
  *
- * Inner models (walkthrough section 2.2.1; ViT3 article, observation 4):
+ * Inner models (walkthrough section 2.2.1; ViT3 article, observations 4 and 6):
  *   ttt_linear_fwd:  f(x; W) = x W,                      W in R^{d x d}
- *   ttt_mlp_fwd:     f(x) = SiLU(x W1 + c1) W2 + c2,      W1 d x m, W2 m x d
+ *   ttt_mlp_fwd:     f(x) = act(x W1 + c1) W2 + c2,       W1 d x m, W2 m x d
+ *   ttt_dwconv_fwd:  a depthwise 3 x 3 convolution over a token grid
+ *   (optionally x + LN(f(x)) for the first two: the inner norm and residual).
+ * ttt_eta_gate computes the per-token rates eta = eta_base * sigma(theta_lr . x)
+ * from the layer input (walkthrough section 2.2.3) in the layout the others read.
  * Row convention throughout: a token x is a 1 x d row vector.
  *
  * Conventions shared by every entry point
