@@ -545,3 +545,20 @@ def test_linear_block_form_equals_token_loop(T, b, nb):
         zb, Wb = _defs.block_form_linear(q[0, h], k[0, h], v[0, h], W0[h], eta[0, h], b, nb)
         np.testing.assert_allclose(zb, z[0, h], rtol=1e-9, atol=1e-10)
         np.testing.assert_allclose(Wb, Wf[0, h], rtol=1e-9, atol=1e-10)
+
+
+@pytest.mark.parametrize("nb", [1, 2, 4])
+def test_block_form_triangular_factor_is_a_finite_series(nb):
+    """L is block-strictly-lower over nb mini-batches, so L^nb = 0 and (I + L)^-1 is the
+    finite series I - L + L^2 - ... (Horner: I - L(I - L(...))): no solve on chip."""
+    b, d = 16, 8
+    n = b * nb
+    K = _unit(rng.standard_normal((n, d)))
+    et = rng.uniform(0.1, 1.0, n)
+    mb = np.arange(n) // b
+    L = (mb[:, None] > mb[None, :]) * (et[:, None] * (K @ K.T))
+    assert np.abs(np.linalg.matrix_power(L, nb)).max() == 0.0
+    T = np.eye(n)
+    for _ in range(nb - 1):
+        T = np.eye(n) - L @ T
+    np.testing.assert_allclose(T, np.linalg.inv(np.eye(n) + L), rtol=1e-12, atol=1e-13)
