@@ -176,3 +176,15 @@ def test_eta_gate_rejects_bad_arguments(L):
     assert call(theta=FAKE + 2) == -3
     assert call(eta=FAKE + (1 << 26) + 2) == -3
     assert call(eta=FAKE + 64) == -1                    # eta overlaps x
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built library the binding raises; there is no CPU fallback."""
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "from test_sequence_layers_gb300 import abi\n"
+            "abi.LIB_PATH = %r\n"
+            "try:\n    abi.lib()\nexcept RuntimeError as e:\n    print('raised', e)\n" % (ROOT, str(tmp_path / "libttt.so")))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.startswith("raised"), (r.stdout, r.stderr)
