@@ -103,6 +103,22 @@ def bytes_per_launch(inp):
     return n
 
 
+def roofline_bound(flops, nbytes, ms, peaks):
+    """The attainable bound min(tensor peak, AI x HBM bandwidth): the launch is
+    HBM-bound when its algorithmic bytes take longer at the copy bandwidth than its
+    algorithmic FLOPs at the bf16 tensor peak, else tensor-bound.  The fraction is
+    achieved / peak of that resource."""
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "bound_ms": t_hbm * 1e3}
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": tf / peaks["bf16_tflops"], "bound_ms": t_tc * 1e3}
+
+
 def kernel_name(inp):
     """The kernel the library dispatches this workload to (mirrors the C ABI's choice)."""
     if inp.kind == "gate":
@@ -183,10 +199,18 @@ class ClockSampler:
         except ValueError:
             return None
 
-    def summary(self, t0, t1):
+    def summary(self, t0, t1, spin0=None):
+        """Clocks over the timed region [t0, t1]; when the region is too short for the
+        sampler to land in it, over the untimed spin [spin0, t0) that ran the same
+        step back to back just before it (labelled in "source")."""
         rows = [r for r in csv.reader(io.StringIO(self.out)) if len(r) >= 9]
-        inside = [r for r in rows if (lambda t: t is not None and t0 <= t <= t1)(self._ts(r[0]))]
-        use = inside or rows
+        within = lambda a, b: [r for r in rows if (lambda t: t is not None and a <= t <= b)(self._ts(r[0]))]
+        inside = within(t0, t1)
+        spin = within(spin0, t0) if spin0 is not None else []
+        use = inside or spin or rows
+        source = ("timed region" if inside else
+                  "same-load spin just before the timed region (the region is shorter than the "
+                  "sampling interval)" if spin else "whole run")
         if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -198,7 +222,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "power_w_max": max(pw) if pw else None,
-                "samples": len(use), "samples_in_timed_region": len(inside)}
+                "samples": len(use), "samples_in_timed_region": len(inside), "source": source}
 
 
 # ------------------------------------------------------------------ our arm
@@ -315,7 +339,9 @@ def run_ours(args, rank, world, inp, peaks):
     clk = ClockSampler(dev.index)
     if not args.quick:
         clk.start()
-    # keep the GPU busy (untimed) while the sampler starts up
+    # keep the GPU busy (untimed) while the sampler starts up; its samples stand in
+    # for a timed region shorter than the sampling interval
+    spin_wall0 = time.time()
     t_spin = time.perf_counter()
     while not args.quick and time.perf_counter() - t_spin < 0.6:
         l2_flush()
@@ -392,7 +418,7 @@ def run_ours(args, rank, world, inp, peaks):
         e2e = {"value": world * inp.token_heads / (e2e_ms / 1e3), "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    clocks = clk.summary(w0, w1)
+    clocks = clk.summary(w0, w1, spin_wall0)
     return ms, times, launches, e2e, clocks
 
 
@@ -527,12 +553,7 @@ def main():
     tflops = flops / (ms * 1e-3) / 1e12
     nbytes = bytes_per_launch(inp)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    if inp.kind in ("linear", "dwconv", "gate"):  # arithmetic intensity below the ridge
-        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / peaks["hbm_gbs"]}
-    else:
-        roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"]}
+    roof = roofline_bound(flops, nbytes, ms, peaks)
     roof.update({"traffic": recorded_traffic(args.workload), "peak_source": peaks["source"],
                  "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
                  "kernel": kernel_name(inp),

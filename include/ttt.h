@@ -31,7 +31,10 @@
  *
  * Conventions shared by every entry point
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
- *     allocates no device memory; it keeps one small status word per device.
+ *     allocates no device memory.  Its device state is one small status word per
+ *     device and the fixed 4 MiB scratch array of ttt_linear_fwd_seqpar_noalloc
+ *     (a static device array, held on every device that loads the library until
+ *     the process exits).
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the
  *     legacy default stream) and runs asynchronously.  The return value reports
  *     argument validation and launch errors synchronously.  A kernel-side wait that

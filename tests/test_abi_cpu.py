@@ -188,3 +188,117 @@ def test_missing_library_fails_loudly(tmp_path):
             "try:\n    abi.lib()\nexcept RuntimeError as e:\n    print('raised', e)\n" % (ROOT, str(tmp_path / "libttt.so")))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.startswith("raised"), (r.stdout, r.stderr)
+
+
+class _Dev:
+    """Stand-in for a CUDA tensor (this machine has none): the attributes the binding
+    reads before it touches the library or the device."""
+
+    def __init__(self, shape, dtype=None, index=0, cuda=True):
+        import torch
+        self.shape = torch.Size(shape)
+        self.dtype = torch.float32 if dtype is None else dtype
+        self.device = torch.device("cuda", index) if cuda else torch.device("cpu")
+        self.is_cuda = cuda
+
+    def dim(self):
+        return len(self.shape)
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        raise AssertionError("the binding reached the library with a bad argument")
+
+
+def _lin_args(B=2, H=3, T=40, d=64, **over):
+    import torch
+    bf = torch.bfloat16
+    a = dict(q=_Dev((B, H, T, d), bf), k=_Dev((B, H, T, d), bf), v=_Dev((B, H, T, d), bf),
+             W0=_Dev((H, d, d)), eta=_Dev((B, H, T)), z=_Dev((B, H, T, d), bf), W_out=_Dev((B, H, d, d)))
+    a.update(over)
+    return a
+
+
+@pytest.mark.parametrize("bad", [
+    dict(z=_Dev((2, 3, 40, 64), None, cuda=False)),            # CPU output
+    dict(z=_Dev((2, 3, 39, 64))),                              # wrong shape (and dtype)
+    dict(W_out=_Dev((2, 3, 64, 32))),                          # undersized final weights
+    dict(W_out=_Dev((3, 64, 64))),                             # final weights must be [B,H,d,d]
+    dict(eta=_Dev((2, 3, 39))),                                # undersized per-token rates
+    dict(eta=_Dev((3, 40))),
+    dict(W0=_Dev((3, 64, 64), index=1)),                       # another device
+    dict(z=_Dev((2, 3, 40, 64), None, index=1)),
+    dict(eta=_Dev((2, 3, 40), index=1)),
+    dict(k=_Dev((2, 3, 40, 64), None, index=1)),
+])
+def test_linear_wrappers_reject_bad_tensors_before_any_launch(bad):
+    a = _lin_args(**bad)
+    for fn in (abi.ttt_linear_fwd, abi.ttt_linear_fwd_seqpar):
+        with pytest.raises(ValueError):
+            fn(a["q"], a["k"], a["v"], a["W0"], 16, eta=a["eta"], z=a["z"], W_out=a["W_out"])
+    with pytest.raises(ValueError):
+        abi.ttt_linear_fwd_seqpar_noalloc(a["q"], a["k"], a["v"], a["W0"], a["z"], a["W_out"], 16,
+                                          eta=a["eta"])
+
+
+def test_linear_wrapper_rejects_inner_norm_of_wrong_shape():
+    a = _lin_args()
+    with pytest.raises(ValueError):
+        abi.ttt_linear_fwd(a["q"], a["k"], a["v"], a["W0"], 16, z=a["z"], W_out=a["W_out"],
+                           ln_gamma=_Dev((3, 32)), ln_beta=_Dev((3, 64)))
+
+
+def _mlp_args(B=2, H=3, T=40, d=64, m=256):
+    import torch
+    bf = torch.bfloat16
+    return dict(q=_Dev((B, H, T, d), bf), W1=_Dev((H, d, m)), c1=_Dev((H, m)), W2=_Dev((H, m, d)),
+                c2=_Dev((H, d)), z=_Dev((B, H, T, d), bf),
+                outs=(_Dev((B, H, d, m)), _Dev((B, H, m)), _Dev((B, H, m, d)), _Dev((B, H, d))))
+
+
+@pytest.mark.parametrize("which", ["W1_out_shape", "c2_out_shape", "W2_device", "z_shape", "eta_shape",
+                                   "outs_cpu"])
+def test_mlp_wrapper_rejects_bad_tensors_before_any_launch(which):
+    a = _mlp_args()
+    outs, eta, z, W2 = list(a["outs"]), None, a["z"], a["W2"]
+    if which == "W1_out_shape":
+        outs[0] = _Dev((2, 3, 64, 128))
+    elif which == "c2_out_shape":
+        outs[3] = _Dev((3, 64))
+    elif which == "W2_device":
+        W2 = _Dev((3, 256, 64), index=1)
+    elif which == "z_shape":
+        z = _Dev((2, 3, 40, 32))
+    elif which == "eta_shape":
+        eta = _Dev((2, 3, 41))
+    elif which == "outs_cpu":
+        outs[1] = _Dev((2, 3, 256), cuda=False)
+    q = a["q"]
+    with pytest.raises(ValueError):
+        abi.ttt_mlp_fwd(q, q, q, a["W1"], a["c1"], W2, a["c2"], 16, eta=eta, z=z, outs=tuple(outs))
+
+
+def test_gate_and_dwconv_wrappers_reject_bad_tensors():
+    import torch
+    x, th = _Dev((2, 50, 256), torch.bfloat16), _Dev((4, 256), torch.bfloat16)
+    with pytest.raises(ValueError):
+        abi.ttt_eta_gate(x, th, eta=_Dev((2, 4, 49)))
+    with pytest.raises(ValueError):
+        abi.ttt_eta_gate(x, _Dev((4, 256), torch.bfloat16, index=1))
+    q = _Dev((1, 2, 196, 64), torch.bfloat16)
+    with pytest.raises(ValueError):
+        abi.ttt_dwconv_fwd(q, q, q, _Dev((2, 9, 64)), 14, 14, z=q, W_out=_Dev((1, 2, 9, 32)))
+    with pytest.raises(ValueError):
+        abi.ttt_dwconv_fwd(q, q, q, _Dev((2, 9, 64), index=2), 14, 14, z=q, W_out=_Dev((1, 2, 9, 64)))
+
+
+def test_stream_on_another_device_is_rejected():
+    import torch
+
+    class _S:
+        device = torch.device("cuda", 1)
+    a = _lin_args()
+    with pytest.raises(ValueError):
+        abi.ttt_linear_fwd(a["q"], a["k"], a["v"], a["W0"], 16, eta=a["eta"], z=a["z"], W_out=a["W_out"],
+                           stream=_S())

@@ -79,3 +79,29 @@ def test_warmup_below_three_is_refused():
                         "linear_tiny_f32", "--warmup", "2"], capture_output=True, text=True, timeout=300,
                        cwd=ROOT)
     assert r.returncode != 0
+
+
+def _peaks():
+    return {"hbm_gbs": 6771.5, "bf16_tflops": 1922.2, "bf16_tflops_sustained": 1710.2, "source": "measured"}
+
+
+def test_roofline_bound_is_the_attainable_minimum():
+    """The bound is min(tensor peak, AI x bandwidth) per workload, not per kind: the
+    full-batch MLP's required final weights (about 203 MB) make it HBM-bound, the
+    causal MLP stays tensor-bound, TTT-Linear is HBM-bound."""
+    pk = _peaks()
+    vm = synth.workload("vision_mlp")
+    flops = bench.flops_per_token_head(vm) * vm.token_heads
+    nbytes = bench.bytes_per_launch(vm)
+    assert 3.4e8 < nbytes < 3.7e8 and 6.5e10 < flops < 7.2e10
+    r = bench.roofline_bound(flops, nbytes, 0.5, pk)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["frac"] - nbytes / 0.5e-3 / 1e9 / pk["hbm_gbs"]) < 1e-12
+    assert abs(r["bound_ms"] - nbytes / (pk["hbm_gbs"] * 1e9) * 1e3) < 1e-12
+    m = synth.workload("mlp_125m", T=2048)
+    r = bench.roofline_bound(bench.flops_per_token_head(m) * m.token_heads, bench.bytes_per_launch(m), 0.4, pk)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    lin = synth.workload("linear_125m")
+    r = bench.roofline_bound(bench.flops_per_token_head(lin) * lin.token_heads, bench.bytes_per_launch(lin),
+                             0.0374, pk)
+    assert r["bound"] == "hbm" and abs(r["frac"] - 0.4045) < 2e-3

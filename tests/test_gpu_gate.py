@@ -56,15 +56,16 @@ def test_gate_empty_and_in_place_output():
     np.testing.assert_allclose(out.double().cpu().numpy(), oracle.eta_gate(x, theta, 1.0), atol=TOL)
 
 
-def test_gate_full_size_sampled_tokens():
+def test_gate_full_size_every_token():
     """The gated long workload's width (32 heads x 64 = 2048) over 2 x 32768 tokens,
-    in the launch the benchmark times; sampled tokens against the oracle."""
+    in the launch the benchmark times; every token against the oracle."""
     B, T, H, dm = 2, 32768, 32, 2048
     x, theta = synth.gate_inputs(B, T, H, dm, seed=77)
     got = _gpu(x, theta, 1.0)
-    ts = np.sort(np.random.default_rng(0).choice(T, 512, replace=False))
-    ref = oracle.eta_gate(x[:, ts], theta, 1.0)
-    assert np.abs(got[:, :, ts] - ref).max() <= TOL
+    ref = oracle.eta_gate(x, theta, 1.0)
+    err = np.abs(got - ref).max()
+    print(f"eta_gate full size max abs err {err:.3e}")
+    assert err <= TOL
 
 
 @pytest.mark.parametrize("causal", [True, False])

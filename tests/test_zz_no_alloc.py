@@ -72,7 +72,13 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point():
 
 def test_split_beyond_the_fixed_scratch_is_rejected():
     """16 chains of d = 64 over 4096 tokens split eight ways: maps and start weights
-    take more than 4 MiB, so the call returns TTT_ERR_SCRATCH and queues nothing."""
+    take more than 4 MiB, so the call returns TTT_ERR_SCRATCH and queues nothing.
+    The planner gives each chain at most (SMs / chains) segments, so eight segments
+    (about 4.75 MiB of scratch) need at least 128 SMs; on a smaller GPU the split is
+    coarser and fits, which says nothing about this entry point."""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    if nsm < 128:
+        pytest.skip(f"{nsm} SMs: the planner splits 16 chains fewer than eight ways")
     inp = G.synth.make("linear", B=1, H=16, T=4096, d=64, b=16, causal=True, seed=702)
     q, k, v, eta, W0 = _dev(inp)
     z = torch.empty_like(q)
