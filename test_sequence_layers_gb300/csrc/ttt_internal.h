@@ -88,7 +88,6 @@ int launch_linear_bf16(const LinearArgs &a);
 int launch_linear_b16(const LinearArgs &a);  // b = 16 specialisation (d <= 64)
 int launch_linear_b1(const LinearArgs &a);   // b = 1 (delta rule), column-parallel
 int launch_linear_fb_tc(const LinearArgs &a);  // full batch, one epoch, on tcgen05
-int launch_linear_blk_tc(const LinearArgs &a);  // causal b = 16, d = 64: block form on tcgen05
 // b = 16, d <= 64 kernel over segments of each chain (segment 0 = tokens [0, len0),
 // segment s >= 1 = [len0 + (s-1) seg_len, len0 + s seg_len)).  prep = false: output
 // units for segments seg0 .. seg0+nseg-1 of every chain, from start weights W0
