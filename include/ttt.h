@@ -294,6 +294,19 @@ const char *ttt_status_str(ttt_status s);
  * (all devices); used to count this library's launches inside a timed region. */
 unsigned long long ttt_launch_count(void);
 
+/*
+ * Test hook of the timeout path (never needed in normal use; the pages have no
+ * counterpart).  With ns > 0, every later TTT-Linear launch of the b = 16 kernel
+ * (causal or not, mini_batch 16, d <= 64) and of the full-batch kernel (bf16, d = 64,
+ * mini_batch >= T <= 256, one epoch) makes its first consumer-side wait on a barrier
+ * that nothing arrives at, bounded by ns nanoseconds: the wait runs out, the kernel
+ * records TTT_ERR_TIMEOUT in the device status word, skips its products (outputs
+ * undefined), still waits for its own copies in flight and frees its tensor memory,
+ * and ttt_sync_status() reports the timeout.  ns = 0 restores normal operation.  The
+ * setting is process-wide (read at each launch); other kernels ignore it.
+ */
+void ttt_debug_wait_limit(unsigned long long ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,8 @@ STATUS = {0: "TTT_OK", -1: "TTT_ERR_ARG", -2: "TTT_ERR_UNSUPPORTED", -3: "TTT_ER
 # every symbol include/ttt.h declares
 EXPORTS = ("ttt_linear_fwd", "ttt_linear_seqpar_workspace", "ttt_linear_fwd_seqpar",
            "ttt_linear_fwd_seqpar_noalloc", "ttt_dwconv_fwd", "ttt_eta_gate",
-           "ttt_mlp_fwd", "ttt_sync_status", "ttt_status_str", "ttt_launch_count")
+           "ttt_mlp_fwd", "ttt_sync_status", "ttt_status_str", "ttt_launch_count",
+           "ttt_debug_wait_limit")
 
 
 class LinearDesc(ctypes.Structure):
@@ -97,6 +98,8 @@ def lib():
         L.ttt_status_str.restype = ctypes.c_char_p
         L.ttt_launch_count.argtypes = []
         L.ttt_launch_count.restype = ctypes.c_ulonglong
+        L.ttt_debug_wait_limit.argtypes = [ctypes.c_ulonglong]
+        L.ttt_debug_wait_limit.restype = None
         _lib = L
     return _lib
 
@@ -381,3 +384,10 @@ def ttt_sync_status(stream=None):
 
 def ttt_launch_count() -> int:
     return int(lib().ttt_launch_count())
+
+
+def ttt_debug_wait_limit(ns: int) -> None:
+    """Test hook of the timeout path: ns > 0 makes the first consumer wait of the
+    b = 16 and full-batch TTT-Linear kernels run out after ns nanoseconds (see
+    include/ttt.h); 0 restores normal operation."""
+    lib().ttt_debug_wait_limit(int(ns))

@@ -25,6 +25,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 namespace {
 
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<unsigned long long> g_test_stall_ns{0};  // ttt_debug_wait_limit
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -183,6 +184,7 @@ ttt_status linear_args(const ttt_linear_desc *desc, const void *q, const void *k
     a.W_out = W_out;
     a.status = status_word();
     a.stream = static_cast<cudaStream_t>(stream);
+    a.test_stall_ns = g_test_stall_ns.load(std::memory_order_relaxed);
     if (!a.status) return TTT_ERR_LAUNCH;
     return TTT_OK;
 }
@@ -471,5 +473,7 @@ const char *ttt_status_str(ttt_status s)
 }
 
 unsigned long long ttt_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void ttt_debug_wait_limit(unsigned long long ns) { g_test_stall_ns.store(ns, std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -95,14 +95,16 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
 }
 
 // Waits for the phase with the given parity to complete.  Returns false after
-// kWaitLimitNs, having recorded `site` in *status (first error wins).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status, int site)
+// limit_ns (kWaitLimitNs by default), having recorded `site` in *status (first error
+// wins).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status, int site,
+                                          unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0u && globaltimer() - t0 > kWaitLimitNs) {
+        if ((it & 63u) == 0u && globaltimer() - t0 > limit_ns) {
             atomicCAS(status, 0, site);
             return false;
         }

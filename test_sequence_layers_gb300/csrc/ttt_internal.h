@@ -21,6 +21,9 @@ struct LinearArgs {
     float *W_out;
     int *status;         // device status word (timeouts)
     cudaStream_t stream;
+    // test hook (ttt_debug_wait_limit): > 0 makes the first consumer wait of the b = 16
+    // and full-batch kernels wait this long on a barrier nothing arrives at
+    unsigned long long test_stall_ns = 0;
 };
 
 struct MlpArgs {

@@ -54,7 +54,9 @@ struct B16Cfg {
     static constexpr int SLOT = ((3 * BLK + 1023) / 1024) * 1024;  // Q, K, V of one block
     static constexpr int ETA_OFF = NB * SLOT;        // 64 fp32 per block
     static constexpr int BAR_OFF = ETA_OFF + NB * 256;
-    static constexpr int RED_OFF = BAR_OFF + 2 * NB * 8;  // inner-norm partial sums [3][NCW][16] float2
+    // full / empty barriers per block slot, then one barrier nothing arrives at (the
+    // timeout test of ttt_debug_wait_limit), then the inner-norm partial sums
+    static constexpr int RED_OFF = BAR_OFF + (2 * NB + 1) * 8;  // [3][NCW][16] float2
     static constexpr int SMEM = RED_OFF + 3 * NCW * 16 * 8 + 1024;
 };
 
@@ -99,6 +101,7 @@ struct B16Params {
     float *maps;  // [BH][nsplit-2][2][d][d] affine maps A, B of segments 1 .. nsplit-2
     const float *ln_gamma, *ln_beta;  // [H][d] inner norm scale / shift (VAR 2)
     float ln_eps;
+    unsigned long long test_stall_ns;  // > 0: the timeout test (first wait on a dead barrier)
 };
 
 // Named barrier of the compute warps (the producer warp does not take part).
@@ -152,6 +155,7 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
 
     const uint32_t blk_full = base + C::BAR_OFF;      // block landed (producer -> warps)
     const uint32_t blk_empty = blk_full + 8 * NB;     // block released (warps -> producer)
+    const uint32_t dead = blk_empty + 8 * NB;          // nothing arrives here (timeout test)
     if (threadIdx.x == 0) {
         if (QSIDE) prefetch_tmap(tq);
         prefetch_tmap(tk);
@@ -160,6 +164,7 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
             mbar_init(blk_full + 8 * s, 1 + (has_eta ? 32 : 0));
             mbar_init(blk_empty + 8 * s, C::NCW);
         }
+        mbar_init(dead, 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -175,7 +180,9 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
         // ------------------------------------------------------------ producer
         for (int L = 0; L < nblk; ++L) {
             const int s = L & (NB - 1);
-            if (L >= NB && !mbar_wait(blk_empty + 8 * s, ((L / NB) & 1) ^ 1, p.status, kSiteProducerEmpty))
+            // (in the timeout test the warps release nothing: give up after the test's limit)
+            if (L >= NB && !mbar_wait(blk_empty + 8 * s, ((L / NB) & 1) ^ 1, p.status, kSiteProducerEmpty,
+                                      p.test_stall_ns ? p.test_stall_ns : kWaitLimitNs))
                 break;
             const uint32_t full = blk_full + 8 * s, st = base + s * C::SLOT;
             if (has_eta) {
@@ -559,7 +566,8 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
                chunk(I3{}, fullc, FB, FA, L);
     };
 
-    bool first = nblk > 0 && mbar_wait(blk_full, 0, p.status, kSiteConsumerFull);
+    bool first = nblk > 0 && (p.test_stall_ns ? mbar_wait(dead, 0, p.status, kSiteConsumerFull, p.test_stall_ns)
+                                                : mbar_wait(blk_full, 0, p.status, kSiteConsumerFull));
     if constexpr (LN)  // the chunks meet at named barriers: every compute warp starts, or none
         if (nblk > 0) first = bar_compute_and(C::NCW * 32, first);
     if (first) {
@@ -651,6 +659,7 @@ B16Params b16_params(const LinearArgs &a)
     p.ln_gamma = a.ln_gamma;
     p.ln_beta = a.ln_beta;
     p.ln_eps = a.ln_eps;
+    p.test_stall_ns = a.test_stall_ns;
     return p;
 }
 

@@ -38,8 +38,9 @@ struct FbtCfg {
     static constexpr int TILE = 128 * 128;               // 128 token rows of 128 bytes
     static constexpr int K_OFF = 0, V_OFF = 2 * TILE;    // 2 tiles each; Q replaces K
     static constexpr int W_OFF = 4 * TILE;               // W0^T, then W1^T: 64 rows of 128 bytes
-    static constexpr int BAR_OFF = W_OFF + 64 * 128;     // kv, q, mma barriers + TMEM address
-    static constexpr int SMEM = BAR_OFF + 32 + 1024;
+    static constexpr int BAR_OFF = W_OFF + 64 * 128;     // kv, q, mma barriers, one barrier nothing
+                                                         // arrives at (timeout test), TMEM address
+    static constexpr int SMEM = BAR_OFF + 40 + 1024;
     static constexpr int TMEM_COLS = 128;                // E, then the update, then Z: 2 x 64 columns
 };
 
@@ -52,6 +53,7 @@ struct FbtParams {
     __nv_bfloat16 *z;
     float *W_out;
     int *status;
+    unsigned long long test_stall_ns;  // > 0: the timeout test (first wait on a dead barrier)
 };
 
 __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
@@ -68,8 +70,8 @@ __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
     const int bh = blockIdx.x, T = p.T;
     const int ntile = T > 128 ? 2 : 1, nbox = 2 * ntile, nk = (T + 15) >> 4;
     const uint32_t sK = base + C::K_OFF, sV = base + C::V_OFF, sQ = sK, sW = base + C::W_OFF;
-    const uint32_t bar_kv = base + C::BAR_OFF, bar_q = bar_kv + 8, bar_mma = bar_kv + 16;
-    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gb + C::BAR_OFF + 24);
+    const uint32_t bar_kv = base + C::BAR_OFF, bar_q = bar_kv + 8, bar_mma = bar_kv + 16, dead = bar_kv + 24;
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gb + C::BAR_OFF + 32);
 
     if (tid == 0) {
         prefetch_tmap(&tq);
@@ -78,6 +80,7 @@ __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
         mbar_init(bar_kv, 1);
         mbar_init(bar_q, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(dead, 1);
         fence_barrier_init();
         // every box of the tiles in use (rows past T arrive as zeros)
         mbar_arrive_expect_tx(bar_kv, 2 * nbox * 8192);
@@ -86,7 +89,7 @@ __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
             tma_load_3d(sV + L * 8192, &tv, bar_kv, 0, 64 * L, bh);
         }
     }
-    if (warp == 0) tc_alloc(base + C::BAR_OFF + 24, C::TMEM_COLS);
+    if (warp == 0) tc_alloc(base + C::BAR_OFF + 32, C::TMEM_COLS);
     // Lanes 0..15 of warp q own column j = 16 q + lane of W: they read W0's column j
     // (kept for the update's epilogue) and write it as row j of the bf16 W0^T tile, the
     // B operand of E = K W0
@@ -109,8 +112,11 @@ __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
     bool ok = true;
 
     // ---------------------------------------------------------------- E = K W0
+    // the timeout test: the first wait is on a barrier nothing arrives at, and every
+    // thread then leaves the products (the copies are still drained below)
+    const bool stalled = p.test_stall_ns != 0 && !mbar_wait(dead, 0, p.status, kSiteConsumerFull, p.test_stall_ns);
     if (tid == 0) {
-        if (!p.dot && mbar_wait(bar_kv, 0, p.status, kSiteConsumerFull)) {
+        if (!p.dot && !stalled && mbar_wait(bar_kv, 0, p.status, kSiteConsumerFull)) {
             constexpr uint32_t id = idesc_bf16(128, 64, false, false);
             for (int m = 0; m < ntile; ++m)
                 for (int kk = 0; kk < 4; ++kk)
@@ -118,7 +124,8 @@ __global__ void __launch_bounds__(FbtCfg::THREADS, 3)
         }
         tc_commit(bar_mma);  // (arrives at once when no product was issued)
     }
-    ok = mbar_wait(bar_kv, 0, p.status, kSiteConsumerFull) && mbar_wait(bar_mma, 0, p.status, kSiteConsumerReady);
+    ok = !stalled && mbar_wait(bar_kv, 0, p.status, kSiteConsumerFull) &&
+         mbar_wait(bar_mma, 0, p.status, kSiteConsumerReady);
     tc_fence_after();
 
     // Et rows: -eta_t (E - V) over this thread's rows of V (zero past T)
@@ -260,6 +267,7 @@ int launch_linear_fb_tc(const LinearArgs &a)
     p.z = static_cast<__nv_bfloat16 *>(a.z);
     p.W_out = a.W_out;
     p.status = a.status;
+    p.test_stall_ns = a.test_stall_ns;
     ttt_linear_fb_tc_kernel<<<a.B * a.H, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
