@@ -80,8 +80,9 @@ def flops_per_token_head(inp):
         # with Et over (b+1)/2 visible pairs (2d each); non-causal: Z = Q W_end
         return 6 * d * d + (2 * (b + 1) * d if inp.causal else 0)
     # MLP: 7 products of 2dm (K W1, A W2, E W2^T, two updates, Q W1, A_q W2) + masked terms
+    # (+ about 18 d for the inner norm: statistics, normalisation and its backward)
     if inp.causal:
-        return 14 * d * m + 2 * (b + 1) * (d + m)
+        return 14 * d * m + 2 * (b + 1) * (d + m) + (18 * d if o.get("ln") else 0)
     return 14 * d * m + 2 * (d + m)
 
 
@@ -316,7 +317,8 @@ def run_ours(args, rank, world, inp, peaks):
         def step(qq=q, kk=k, vv=v, ee=eta, zz=z, oo=outs, wsp=None):
             abi.ttt_mlp_fwd(qq, kk, vv, params["W1"], params["c1"], params["W2"], params["c2"],
                             inp.b, inp.causal, eta=ee, eta_scalar=inp.eta_scalar, z=zz, outs=tuple(oo),
-                            activation=inp.options.get("activation", "silu"))
+                            activation=inp.options.get("activation", "silu"),
+                            ln_gamma=params.get("ln_gamma"), ln_beta=params.get("ln_beta"))
         out_bytes = [z, *outs]
 
     flush_w = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -472,8 +474,12 @@ def oracle_sample(inp, budget_s):
         else:
             P = [torch.stack([inp.params[nm][c % inp.H] for c in sel]).unsqueeze(0)
                  for nm in ("W1", "c1", "W2", "c2")]
+            ln = {}
+            if "ln_gamma" in inp.params:
+                ln = {"ln_gamma": torch.stack([inp.params["ln_gamma"][c % inp.H] for c in sel]),
+                      "ln_beta": torch.stack([inp.params["ln_beta"][c % inp.H] for c in sel])}
             oracle.mlp(q, k, v, *P, inp.b, inp.causal, eta=eta, eta_scalar=inp.eta_scalar,
-                       threads=threads, activation=o.get("activation", "silu"))
+                       threads=threads, activation=o.get("activation", "silu"), **ln)
         elapsed += time.perf_counter() - t0
         done += take
         n = min(2 * n, BH)

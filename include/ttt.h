@@ -207,8 +207,9 @@ typedef struct {
                                   c1) W2 + c2), LN over the d outputs as in
                                   ttt_linear_desc ("Learning to (Learn at Test Time)"
                                   walkthrough, section 2.2.1); [H,d] fp32 device arrays,
-                                  fixed, or both NULL for the plain MLP.  fp32 I/O only
-                                  (bf16: TTT_ERR_UNSUPPORTED)                           */
+                                  fixed, or both NULL for the plain MLP.  bf16 I/O needs
+                                  d = 64, m = 256, mini_batch <= 16 (the eight-warp
+                                  tensor-core kernel; TTT_ERR_UNSUPPORTED otherwise)     */
     const float *ln_beta;
     float ln_eps;              /* > 0 when the norm is used                             */
 } ttt_mlp_desc;

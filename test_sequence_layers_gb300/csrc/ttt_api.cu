@@ -291,7 +291,9 @@ ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc, const void *q, const void *k, c
     if (ln && (!D.ln_gamma || !D.ln_beta || !(D.ln_eps > 0.f))) return TTT_ERR_ARG;
     if (D.d != 16 && D.d != 32 && D.d != 64) return TTT_ERR_UNSUPPORTED;
     if (D.m % 16 != 0) return TTT_ERR_UNSUPPORTED;
-    if (ln && D.io_dtype != TTT_F32) return TTT_ERR_UNSUPPORTED;
+    if (ln && D.io_dtype == TTT_BF16 &&  // the bf16 inner norm: the eight-warp kernel's shapes
+        (D.d != 64 || D.m != 256 || (D.T > 0 && D.mini_batch > D.T ? D.T : D.mini_batch) > 16))
+        return TTT_ERR_UNSUPPORTED;
     if (ln && (!aligned(D.ln_gamma, 4) || !aligned(D.ln_beta, 4))) return TTT_ERR_ALIGN;
     if ((long long)D.B * D.H > 0x7fffffffLL) return TTT_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16)) return TTT_ERR_ALIGN;

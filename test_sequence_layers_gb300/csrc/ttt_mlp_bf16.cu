@@ -137,6 +137,11 @@ struct MlpParams {
     __nv_bfloat16 *z;
     float *W1o, *c1o, *W2o, *c2o;
     int *status;
+    // inner norm + residual (eight-warp kernel, LN = true): [H][d] scale and shift, the
+    // queries (the residual of z, read from global memory)
+    const float *ln_gamma = nullptr, *ln_beta = nullptr;
+    float ln_eps = 1e-6f;
+    const __nv_bfloat16 *q = nullptr;
 };
 
 // MULTI: causal with mini-batches longer than one 16-token chunk, so the chunk's
@@ -698,13 +703,18 @@ struct W8Cfg {
     static constexpr int S2P_OFF = SP_OFF + 16 * 48;            // bf16 S2' = M .* (A_q A_k^T + 1) [16][48 B]
     static constexpr int S2F_OFF = S2P_OFF + 16 * 48;           // fp32 [NW][16][S2R] partial A_q A_k^T
     static constexpr int C2S_OFF = S2F_OFF + NW * 16 * S2R * 4; // fp32 [2][D] c2 at a chunk's start
-    static constexpr int BAR_OFF = C2S_OFF + 2 * D * 4;         // full[NS], abort flag
+    static constexpr int LNR_OFF = C2S_OFF + 2 * D * 4;         // inner norm: float2 [3][4 warps][16 rows]
+    static constexpr int BAR_OFF = LNR_OFF + 3 * 4 * 16 * 8;    // full[NS], abort flag
     static constexpr int SMEM = BAR_OFF + NS * 8 + 16 + 1024;
 };
 static_assert(MlpCfg<64>::RB == 128, "tile rows of 128 bytes");
 static_assert(W8Cfg::SMEM <= 227 * 1024, "shared memory");
 
-template <int ACT>
+// LN: the inner model is x + LN(act(x W1 + c1) W2 + c2) (walkthrough section 2.2.1): the
+// residual of a key is the layer-norm backward of f(k) - v, and z = q + LN(y_q), with
+// each token's statistics over its 64 outputs summed across the four warps that hold
+// them (a shuffle over the quad, then a shared-memory exchange at a named barrier).
+template <int ACT, bool LN>
 __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
     ttt_mlp_w8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const MlpParams p)
@@ -835,6 +845,45 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
     // [16][AR] bf16; cc = 16 (w mod 4)); the fragments of the next 32 hidden units
     // load while the current ones multiply
     const int cc = 16 * (w & 3);
+    // inner norm: scale / shift of columns cc + 8 nt + 2 t4 + i
+    float lg[2][2] = {}, lb[2][2] = {};
+    if constexpr (LN) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                lg[nt][i] = p.ln_gamma[(size_t)(bh % p.H) * D + cc + 8 * nt + 2 * t4 + i];
+                lb[nt][i] = p.ln_beta[(size_t)(bh % p.H) * D + cc + 8 * nt + 2 * t4 + i];
+            }
+    }
+    // per-token sums (a, b) over the 64 outputs for token rows g and g + 8: this warp's 16
+    // columns (quad shuffle), then the four warps of the group (buffer buf, named barrier
+    // barid of the group's 128 threads)
+    auto row_sums = [&](float (&a)[2], float (&b)[2], int buf, int barid) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            a[r] += __shfl_xor_sync(0xffffffffu, a[r], 1);
+            a[r] += __shfl_xor_sync(0xffffffffu, a[r], 2);
+            b[r] += __shfl_xor_sync(0xffffffffu, b[r], 1);
+            b[r] += __shfl_xor_sync(0xffffffffu, b[r], 2);
+        }
+        float2 *red = reinterpret_cast<float2 *>(gbase + C::LNR_OFF) + buf * 64;
+        if (t4 == 0) {
+            red[(w & 3) * 16 + g] = make_float2(a[0], b[0]);
+            red[(w & 3) * 16 + g + 8] = make_float2(a[1], b[1]);
+        }
+        asm volatile("bar.sync %0, 128;" ::"r"(barid) : "memory");
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            a[r] = b[r] = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 x = red[u * 16 + g + 8 * r];
+                a[r] += x.x;
+                b[r] += x.y;
+            }
+        }
+    };
     auto col_product16 = [&](uint32_t W, uint32_t X, float (&acc)[2][2][4]) {
         uint32_t fb[2][2][4], fa[2][8];
         auto ld = [&](int kp, int sl) {
@@ -874,16 +923,61 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
         uint32_t sa[4], b0, b1, b2, b3;
         ldsm_x4(base + C::S2P_OFF + rowA * 48 + colA * 2, sa[0], sa[1], sa[2], sa[3]);
         ldsm_x4_t(NEBc + (uint32_t)(lane & 15) * C::ER + (cc + 8 * (lane >> 4)) * 2, b0, b1, b2, b3);
+        if constexpr (!LN) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                float zz[4] = {pz[nt][0][0] + pz[nt][1][0], pz[nt][0][1] + pz[nt][1][1], pz[nt][0][2] + pz[nt][1][2],
+                               pz[nt][0][3] + pz[nt][1][3]};
+                mma_bf16(zz, sa[0], sa[1], sa[2], sa[3], nt ? b2 : b0, nt ? b3 : b1);
+                const int col = cc + 8 * nt + 2 * t4;
+                const float x = c2s[col], y = c2s[col + 1];
+                __nv_bfloat16 *zb = p.z + ((size_t)bh * T + t0) * D + col;
+                if (g < c) *reinterpret_cast<uint32_t *>(zb + (size_t)g * D) = pack_bf16(zz[0] + x, zz[1] + y);
+                if (g + 8 < c) *reinterpret_cast<uint32_t *>(zb + (size_t)(g + 8) * D) = pack_bf16(zz[2] + x, zz[3] + y);
+            }
+            return;
+        }
+        float zz[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            float zz[4] = {pz[nt][0][0] + pz[nt][1][0], pz[nt][0][1] + pz[nt][1][1], pz[nt][0][2] + pz[nt][1][2],
-                           pz[nt][0][3] + pz[nt][1][3]};
-            mma_bf16(zz, sa[0], sa[1], sa[2], sa[3], nt ? b2 : b0, nt ? b3 : b1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) zz[nt][i] = pz[nt][0][i] + pz[nt][1][i];
+            mma_bf16(zz[nt], sa[0], sa[1], sa[2], sa[3], nt ? b2 : b0, nt ? b3 : b1);
             const int col = cc + 8 * nt + 2 * t4;
-            const float x = c2s[col], y = c2s[col + 1];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) zz[nt][i] += c2s[col + (i & 1)];
+        }
+        {  // z = q + LN(y_q), statistics over the 64 outputs of each query
+            float s1[2] = {}, s2[2] = {};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    s1[i >> 1] += zz[nt][i];
+                    s2[i >> 1] += zz[nt][i] * zz[nt][i];
+                }
+            row_sums(s1, s2, 2, 2);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const float mu = s1[r] * (1.f / D);
+                const float rs = rsqrtf(fmaxf(s2[r] * (1.f / D) - mu * mu, 0.f) + p.ln_eps);
+                const int tok = g + 8 * r;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = cc + 8 * nt + 2 * t4;
+                    uint32_t qw = 0;
+                    if (tok < c) qw = *reinterpret_cast<const uint32_t *>(p.q + ((size_t)bh * T + t0 + tok) * D + col);
+                    zz[nt][2 * r] = bf16_lo(qw) + lg[nt][0] * (zz[nt][2 * r] - mu) * rs + lb[nt][0];
+                    zz[nt][2 * r + 1] = bf16_hi(qw) + lg[nt][1] * (zz[nt][2 * r + 1] - mu) * rs + lb[nt][1];
+                }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int col = cc + 8 * nt + 2 * t4;
             __nv_bfloat16 *zb = p.z + ((size_t)bh * T + t0) * D + col;
-            if (g < c) *reinterpret_cast<uint32_t *>(zb + (size_t)g * D) = pack_bf16(zz[0] + x, zz[1] + y);
-            if (g + 8 < c) *reinterpret_cast<uint32_t *>(zb + (size_t)(g + 8) * D) = pack_bf16(zz[2] + x, zz[3] + y);
+            if (g < c) *reinterpret_cast<uint32_t *>(zb + (size_t)g * D) = pack_bf16(zz[nt][0], zz[nt][1]);
+            if (g + 8 < c) *reinterpret_cast<uint32_t *>(zb + (size_t)(g + 8) * D) = pack_bf16(zz[nt][2], zz[nt][3]);
         }
     };
     int prev_t0 = 0, prev_c = 0;   // the previous chunk, whose outputs are finished one chunk later
@@ -970,6 +1064,52 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
             float e[2][2][4] = {};
             col_product16(W2B, AK, e);
             float *c2snap = reinterpret_cast<float *>(gbase + C::C2S_OFF) + (jb & 1) * D;
+            // LN: the residual of key t is the layer-norm backward of f(k_t) - v_t,
+            // (gamma / sigma) (g - mean(g) - xhat mean(g xhat)), g = gamma (k + LN(y) - v)
+            float lnr[2][2][2] = {};  // [nt][row][i]
+            if constexpr (LN) {
+                float y[2][2][2], s1[2] = {}, s2[2] = {};
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            y[nt][r][i] = e[nt][0][2 * r + i] + e[nt][1][2 * r + i] + c2r[nt][i];
+                            s1[r] += y[nt][r][i];
+                            s2[r] += y[nt][r][i] * y[nt][r][i];
+                        }
+                row_sums(s1, s2, 0, 1);
+                float rs[2], g1[2] = {}, g2[2] = {}, gv[2][2][2], xh[2][2][2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float mu = s1[r] * (1.f / D);
+                    rs[r] = rsqrtf(fmaxf(s2[r] * (1.f / D) - mu * mu, 0.f) + p.ln_eps);
+                    const int tok = g + 8 * r;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int col = cc + 8 * nt + 2 * t4;
+                        const uint32_t kw = *reinterpret_cast<const uint32_t *>(gbase + (tK - base) + mtoff<D>(tok, col));
+                        const uint32_t vw = *reinterpret_cast<const uint32_t *>(gbase + (tV - base) + mtoff<D>(tok, col));
+                        const float kv[2] = {bf16_lo(kw), bf16_hi(kw)}, vv[2] = {bf16_lo(vw), bf16_hi(vw)};
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            xh[nt][r][i] = (y[nt][r][i] - mu) * rs[r];
+                            gv[nt][r][i] = lg[nt][i] * (kv[i] + lg[nt][i] * xh[nt][r][i] + lb[nt][i] - vv[i]);
+                            g1[r] += gv[nt][r][i];
+                            g2[r] += gv[nt][r][i] * xh[nt][r][i];
+                        }
+                    }
+                }
+                row_sums(g1, g2, 1, 1);
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int i = 0; i < 2; ++i)
+                            lnr[nt][r][i] = rs[r] * (gv[nt][r][i] - g1[r] * (1.f / D) - xh[nt][r][i] * g2[r] * (1.f / D));
+            }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int col = cc + 8 * nt + 2 * t4;
@@ -981,8 +1121,8 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
                 for (int r = 0; r < 2; ++r) {  // token rows g, g + 8
                     const int tok = g + 8 * r;
                     const uint32_t vw = *reinterpret_cast<const uint32_t *>(gbase + (tV - base) + mtoff<D>(tok, col));
-                    const float ex = e[nt][0][2 * r] + e[nt][1][2 * r] + c2r[nt][0] - bf16_lo(vw);
-                    const float ey = e[nt][0][2 * r + 1] + e[nt][1][2 * r + 1] + c2r[nt][1] - bf16_hi(vw);
+                    const float ex = LN ? lnr[nt][r][0] : e[nt][0][2 * r] + e[nt][1][2 * r] + c2r[nt][0] - bf16_lo(vw);
+                    const float ey = LN ? lnr[nt][r][1] : e[nt][0][2 * r + 1] + e[nt][1][2 * r + 1] + c2r[nt][1] - bf16_hi(vw);
                     const bool ok = tok < J.c;
                     const float et = -eta_of(tok);
                     const float nx = ok ? et * ex : 0.f, ny = ok ? et * ey : 0.f;
@@ -1191,7 +1331,8 @@ __global__ void __launch_bounds__(W8Cfg::THREADS, 1)
 static int launch_mlp_w8(const MlpArgs &a, const CUtensorMap *maps)
 {
     using C = W8Cfg;
-    auto kern = a.act ? ttt_mlp_w8_kernel<1> : ttt_mlp_w8_kernel<0>;
+    auto kern = a.ln_gamma ? (a.act ? ttt_mlp_w8_kernel<1, true> : ttt_mlp_w8_kernel<0, true>)
+                           : (a.act ? ttt_mlp_w8_kernel<1, false> : ttt_mlp_w8_kernel<0, false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return -4;
     MlpParams p;
@@ -1212,6 +1353,10 @@ static int launch_mlp_w8(const MlpArgs &a, const CUtensorMap *maps)
     p.W2o = a.W2o;
     p.c2o = a.c2o;
     p.status = a.status;
+    p.ln_gamma = a.ln_gamma;
+    p.ln_beta = a.ln_beta;
+    p.ln_eps = a.ln_eps;
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
     kern<<<a.B * a.H, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
@@ -1642,6 +1787,8 @@ int launch_mlp_bf16(const MlpArgs &a)
     if (a.m != 4 * a.d) return -2;
     CUtensorMap maps[3];
     if (!encode_qkv(maps, a.q, a.k, a.v, a.B * a.H, a.T, a.d, 16)) return -4;
+    if (a.ln_gamma)  // inner norm + residual: the eight-warp kernel (d = 64, mini-batches <= 16)
+        return a.d == 64 && a.b <= 16 ? launch_mlp_w8(a, maps) : -2;
     switch (a.d) {
     case 16: return launch_mlp_t<16>(a, maps);
     case 32: return launch_mlp_t<32>(a, maps);

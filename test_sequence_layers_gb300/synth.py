@@ -53,6 +53,10 @@ WORKLOADS = {
     "linear_long_gate_x": ("linear", 2, 32, 32768, 64, 0, 16, True, torch.bfloat16, 1.0, 12),
     # the rate gate alone at that shape (H heads of d: layer width H d = 2048; eta_base 1)
     "eta_gate_long": ("gate", 2, 32, 32768, 64, 0, 0, False, torch.bfloat16, 1.0, 13),
+    # TTT-MLP with the inner norm and residual (the walkthrough's TTT-MLP) at the 125M shape
+    "mlp_125m_ln": ("mlp", 8, 12, 2048, 64, 256, 16, True, torch.bfloat16, 0.1, 14),
+    # the 125M TTT-MLP shape at eta = 0.01, whose plain inner GD stays finite
+    "mlp_125m_eta001": ("mlp", 8, 12, 2048, 64, 256, 16, True, torch.bfloat16, 0.01, 15),
 }
 
 # options beyond the base layer: inner loss ("dot"), inner epochs, MLP activation,
@@ -64,6 +68,7 @@ OPTIONS = {
     "vision_dwconv": {"height": 14, "width": 14, "loss": "dot"},  # ViT3: depthwise conv, dot loss
     "linear_125m_ln": {"ln": True},                         # x + LN(x W): the walkthrough's TTT-Linear
     "linear_long_gate_x": {"gate": True},                   # eta = eta_base sigma(theta_lr . x)
+    "mlp_125m_ln": {"ln": True},                            # x + LN(act(x W1 + c1) W2 + c2)
 }
 
 

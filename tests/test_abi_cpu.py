@@ -109,7 +109,7 @@ def test_mlp_rejects_bad_arguments(L):
     g = FAKE + (1 << 24)
     assert _call_mlp(L, _mlp(ln_gamma=g, ln_eps=1e-6)) == -1               # beta missing
     assert _call_mlp(L, _mlp(io_dtype=abi.TTT_F32, ln_gamma=g, ln_beta=g, ln_eps=0.0)) == -1
-    assert _call_mlp(L, _mlp(ln_gamma=g, ln_beta=g, ln_eps=1e-6)) == -2    # inner norm: fp32 only
+    assert _call_mlp(L, _mlp(d=32, ln_gamma=g, ln_beta=g, ln_eps=1e-6)) == -2  # bf16 inner norm: d = 64 only
     assert _call_mlp(L, _mlp(io_dtype=abi.TTT_F32, ln_gamma=g + 2, ln_beta=g, ln_eps=1e-6)) == -3
 
 
