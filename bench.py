@@ -136,7 +136,9 @@ def kernel_name(inp):
         return "ttt_linear_b16_kernel" if min(inp.b, inp.T) == 16 and inp.d <= 64 else "ttt_linear_bf16_kernel"
     if inp.d == 64 and not inp.causal and inp.b >= inp.T:
         return "ttt_mlp_fb_kernel"
-    return "ttt_mlp_w8_kernel" if inp.d == 64 and min(inp.b, inp.T) <= 16 else "ttt_mlp_bf16_kernel"
+    if inp.d == 64 and min(inp.b, inp.T) <= 16:
+        return "ttt_mlp_w8_ln_kernel" if inp.options.get("ln") else "ttt_mlp_w8_kernel"
+    return "ttt_mlp_bf16_kernel"
 
 
 def recorded_traffic(workload):
