@@ -135,7 +135,7 @@ def kernel_name(inp):
             return "ttt_linear_b1_kernel"
         return "ttt_linear_b16_kernel" if min(inp.b, inp.T) == 16 and inp.d <= 64 else "ttt_linear_bf16_kernel"
     if inp.d == 64 and not inp.causal and inp.b >= inp.T:
-        return "ttt_mlp_fb_kernel"
+        return "ttt_mlp_fb_tc_kernel"
     if inp.d == 64 and min(inp.b, inp.T) <= 16:
         return "ttt_mlp_w8_ln_kernel" if inp.options.get("ln") else "ttt_mlp_w8_kernel"
     return "ttt_mlp_bf16_kernel"

@@ -103,6 +103,8 @@ int launch_linear_fb(const LinearArgs &a);   // one full-batch mini-batch (b = T
 int launch_linear_f32(const LinearArgs &a);
 int launch_mlp_f32(const MlpArgs &a);
 int launch_mlp_bf16(const MlpArgs &a);
+// one full-batch mini-batch (b >= T, non-causal), d = 64, m = 256, on tcgen05; -2 otherwise
+int launch_mlp_fb_tc(const MlpArgs &a);
 // Sequence-parallel TTT-Linear (ttt_linear_seqpar.cu): the segment plan for a
 // problem (false: the problem is not split, run the one-unit-per-chain path).
 struct SeqparPlan {

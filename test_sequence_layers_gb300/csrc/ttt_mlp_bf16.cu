@@ -808,426 +808,6 @@ static int launch_mlp_w8(const MlpArgs &a, const CUtensorMap *maps)
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
-// ---------------------------------------------------------------------------
-// Full-batch kernel for d = 64 (m = 256): one non-causal mini-batch covering the
-// whole sequence (b >= T; the ViT3 setting of one inner GD step over all tokens,
-// every query reading the updated weights).  Every residual is taken at the start
-// weights, so there is no dual-form correction and no dependency between chunks
-// except the accumulation of the weight writes:
-//  * update pass over 16-token chunks: H_k = K W1 + c1 (W1 from a bf16 snapshot of
-//    the start weights), E = A_k W2 + c2 - V (W2's start copy), Delta, and the
-//    writes accumulate into the W1^T / W2 rows each warp holds in registers (the
-//    same split as the eight-warp kernel above);
-//  * output pass over the chunks: H_q = Q W1' + c1', A_q, z = A_q W2' + c2'.
-struct FbmCfg {
-    static constexpr int D = 64, M = 256, NW = 8, THREADS = NW * 32;
-    static constexpr int NK = D / 16, NKM = M / 16, NJ = D / 8, NS = 4;
-    static constexpr int TILE = 16 * D * 2;
-    static constexpr int STAGE = ((3 * TILE + 64 + 1023) / 1024) * 1024;  // Q, K, V, eta
-    static constexpr int W2R = 2 * D + 16, AR = 2 * M + 16, ER = 2 * D + 16;
-    static constexpr int W1S_OFF = NS * STAGE;                  // bf16 W1^T [M][W2R] at the start
-    static constexpr int W2B_OFF = W1S_OFF + M * W2R;           // bf16 W2 [M][W2R]: start, then end copy
-    static constexpr int AK_OFF = W2B_OFF + 2 * M * W2R;        // bf16 A_k or A_q [16][AR]
-    static constexpr int EB_OFF = AK_OFF + 16 * AR;             // bf16 E [16][ER]
-    static constexpr int NEB_OFF = EB_OFF + 16 * ER;            // bf16 -Et [16][ER]
-    static constexpr int BAR_OFF = NEB_OFF + 16 * ER;           // full[NS], abort flag
-    static constexpr int SMEM = BAR_OFF + NS * 8 + 16 + 1024;
-};
-static_assert(FbmCfg::SMEM <= 227 * 1024, "shared memory");
-
-template <int ACT>
-__global__ void __launch_bounds__(FbmCfg::THREADS, 1)
-    ttt_mlp_fb_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const MlpParams p)
-{
-    using C = FbmCfg;
-    constexpr int D = C::D, M = C::M, NK = C::NK, NKM = C::NKM, NJ = C::NJ, NS = C::NS;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *gbase = smem_raw + (base - raw);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x, T = p.T;
-    const int g = lane >> 2, t4 = lane & 3;
-    const int rowA = (lane & 7) + 8 * ((lane >> 3) & 1), colA = 8 * (lane >> 4);
-    const int rowB = (lane & 7) + 8 * (lane >> 4), colB = 8 * ((lane >> 3) & 1);
-    const bool has_eta = p.eta != nullptr;
-    const uint32_t bar_full = base + C::BAR_OFF;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + C::BAR_OFF + NS * 8);
-    const uint32_t W1S = base + C::W1S_OFF, W2S = base + C::W2B_OFF, W2E = W2S + M * C::W2R;
-    const uint32_t AX = base + C::AK_OFF, EB = base + C::EB_OFF, NEB = base + C::NEB_OFF;
-    const int nch = (T + 15) >> 4, njobs = 2 * nch;  // update pass, then output pass
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(bar_full + 8 * s, 1 + (has_eta ? 32 : 0));
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    // ---------------------------------------------------------- initial state
-    const int w = warp, c0 = 8 * w;
-    const size_t ps = p.per_batch ? (size_t)bh : (size_t)(bh % p.H);
-    const float *W1g = p.W1 + ps * D * M, *c1g = p.c1 + ps * M;
-    const float *W2g = p.W2 + ps * M * D, *c2g = p.c2 + ps * D;
-    float w1[2][NJ][4];      // W1^T rows (32w + 16hg + g (+8)) x columns 8j + 2t4 ..
-    float w2[2][NK][2][4];   // W2[32w + 16hg + 8nt + 2t4 .. +1][16mt + g (+8)]
-    float c1r[2][2][2], c1s[2][2][2];  // c1 of hidden 32w + 16hg + 8nt + 2t4 + i (running, start)
-#pragma unroll
-    for (int hg = 0; hg < 2; ++hg) {
-        const int h0 = 32 * w + 16 * hg;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            const int r = 8 * j + 2 * t4;
-            w1[hg][j][0] = W1g[(size_t)r * M + h0 + g];
-            w1[hg][j][1] = W1g[(size_t)(r + 1) * M + h0 + g];
-            w1[hg][j][2] = W1g[(size_t)r * M + h0 + g + 8];
-            w1[hg][j][3] = W1g[(size_t)(r + 1) * M + h0 + g + 8];
-        }
-#pragma unroll
-        for (int mt = 0; mt < NK; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int hr = h0 + 8 * nt + 2 * t4, dc = 16 * mt + g;
-                w2[hg][mt][nt][0] = W2g[(size_t)hr * D + dc];
-                w2[hg][mt][nt][1] = W2g[(size_t)(hr + 1) * D + dc];
-                w2[hg][mt][nt][2] = W2g[(size_t)hr * D + dc + 8];
-                w2[hg][mt][nt][3] = W2g[(size_t)(hr + 1) * D + dc + 8];
-            }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int i = 0; i < 2; ++i) c1r[hg][nt][i] = c1s[hg][nt][i] = c1g[h0 + 8 * nt + 2 * t4 + i];
-    }
-    float c2r[2] = {c2g[c0 + 2 * t4], c2g[c0 + 2 * t4 + 1]};  // c2 of columns c0 + 2t4 + i (running)
-    const float c2s[2] = {c2r[0], c2r[1]};                    // ... at the start
-    auto put_w2 = [&](uint32_t buf) {  // bf16 W2 rows of this warp into buf ([hidden][d])
-        const int blk = lane >> 3, rr = lane & 7;
-#pragma unroll
-        for (int hg = 0; hg < 2; ++hg)
-#pragma unroll
-            for (int mt = 0; mt < NK; ++mt)
-                stsm_x4_t(buf + (uint32_t)(32 * w + 16 * hg + 8 * (blk >> 1) + rr) * C::W2R +
-                              (uint32_t)(16 * mt + 8 * (blk & 1)) * 2,
-                          pack_bf16(w2[hg][mt][0][0], w2[hg][mt][0][1]),
-                          pack_bf16(w2[hg][mt][0][2], w2[hg][mt][0][3]),
-                          pack_bf16(w2[hg][mt][1][0], w2[hg][mt][1][1]),
-                          pack_bf16(w2[hg][mt][1][2], w2[hg][mt][1][3]));
-    };
-    auto w1_b = [&](int hg, int kk, uint32_t (&b)[4]) {  // bf16 W1 (current) as a B operand
-        b[0] = pack_bf16(w1[hg][2 * kk][0], w1[hg][2 * kk][1]);
-        b[1] = pack_bf16(w1[hg][2 * kk + 1][0], w1[hg][2 * kk + 1][1]);
-        b[2] = pack_bf16(w1[hg][2 * kk][2], w1[hg][2 * kk][3]);
-        b[3] = pack_bf16(w1[hg][2 * kk + 1][2], w1[hg][2 * kk + 1][3]);
-    };
-    // start copies: W2 [hidden][d] and W1^T [hidden][d] (stmatrix of the A-fragment
-    // layout of the W1^T accumulators: rows = hidden, columns = d)
-    put_w2(W2S);
-#pragma unroll
-    for (int hg = 0; hg < 2; ++hg)
-#pragma unroll
-        for (int kk = 0; kk < NK; ++kk)
-            stsm_x4(W1S + (uint32_t)(32 * w + 16 * hg + rowA) * C::W2R + (16 * kk + colA) * 2,
-                    pack_bf16(w1[hg][2 * kk][0], w1[hg][2 * kk][1]), pack_bf16(w1[hg][2 * kk][2], w1[hg][2 * kk][3]),
-                    pack_bf16(w1[hg][2 * kk + 1][0], w1[hg][2 * kk + 1][1]),
-                    pack_bf16(w1[hg][2 * kk + 1][2], w1[hg][2 * kk + 1][3]));
-
-    // ------------------------------------------------ token tiles (warp 0 issues)
-    int issued = 0;
-    auto issue_next = [&]() {  // job j: chunk j of the update pass (K, V, eta), then of the output pass (Q)
-        if (issued >= njobs) return;
-        const int j = issued, s = j % NS;
-        const bool updj = j < nch;
-        const int t0 = 16 * (updj ? j : j - nch), c = min(16, T - t0);
-        const uint32_t st = base + s * C::STAGE, full = bar_full + 8 * s;
-        if (has_eta) {
-            if (updj && lane < c) cp_async_4(st + 3 * C::TILE + 4 * lane, p.eta + (size_t)bh * T + t0 + lane);
-            cp_async_arrive_noinc(full);
-        }
-        if (lane == 0) {
-            mbar_arrive_expect_tx(full, (updj ? 2 : 1) * C::TILE);
-            if (updj) {
-                tma_load_3d(st + C::TILE, &tk, full, 0, t0, bh);
-                tma_load_3d(st + 2 * C::TILE, &tv, full, 0, t0, bh);
-            } else {
-                tma_load_3d(st, &tq, full, 0, t0, bh);
-            }
-        }
-        __syncwarp();
-        ++issued;
-    };
-    if (warp == 0) {
-        if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tq)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
-        }
-        for (int i = 0; i < NS - 1; ++i) issue_next();
-    }
-    __syncthreads();
-
-    // acc += X W[:, c0 .. c0+7] over all hidden units (X = A_k or A_q, [16][AR] bf16)
-    auto col_product = [&](uint32_t W, uint32_t X, float (&acc)[2][4]) {
-        uint32_t fb[2][4], fa[2][8];
-        auto ld = [&](int kp, int sl) {
-            ldsm_x4_t(W + (uint32_t)(32 * kp + lane) * C::W2R + c0 * 2, fb[sl][0], fb[sl][1], fb[sl][2], fb[sl][3]);
-            ldsm_x4(X + rowA * C::AR + (32 * kp + colA) * 2, fa[sl][0], fa[sl][1], fa[sl][2], fa[sl][3]);
-            ldsm_x4(X + rowA * C::AR + (32 * kp + 16 + colA) * 2, fa[sl][4], fa[sl][5], fa[sl][6], fa[sl][7]);
-        };
-        ld(0, 0);
-#pragma unroll
-        for (int kp = 0; kp < NKM / 2; ++kp) {
-            if (kp + 1 < NKM / 2) ld(kp + 1, (kp + 1) & 1);
-            const int sl = kp & 1;
-            mma_bf16(acc[0], fa[sl][0], fa[sl][1], fa[sl][2], fa[sl][3], fb[sl][0], fb[sl][1]);
-            mma_bf16(acc[1], fa[sl][4], fa[sl][5], fa[sl][6], fa[sl][7], fb[sl][2], fb[sl][3]);
-        }
-    };
-
-    for (int jb = 0; jb < njobs; ++jb) {
-        if (warp == 0) issue_next();
-        const int s = jb % NS;
-        const bool upd = jb < nch;
-        const int t0 = 16 * (upd ? jb : jb - nch), c = min(16, T - t0);
-        const uint32_t tQ = base + s * C::STAGE, tK = tQ + C::TILE, tV = tQ + 2 * C::TILE;
-        const float *eta_s = reinterpret_cast<const float *>(gbase + s * C::STAGE + 3 * C::TILE);
-        auto eta_of = [&](int tok) -> float { return has_eta ? eta_s[tok] : p.eta_scalar; };
-        if (!mbar_wait(bar_full + 8 * s, (jb / NS) & 1, p.status, kSiteConsumerFull)) *abort_flag = 1;
-
-        if (upd) {
-            // ---------------------------------------------------- update pass
-            // phase 1: H_k = K W1 + c1 at the start weights, A_k, SiLU'(H_k)
-            uint32_t kf[NK][4];
-#pragma unroll
-            for (int kk = 0; kk < NK; ++kk) ldsm_x4(tK + mtoff<D>(rowA, 16 * kk + colA), kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3]);
-            float sp[2][2][4];
-            uint32_t akp[2][4];
-#pragma unroll
-            for (int hg = 0; hg < 2; ++hg) {
-                float hk[2][4] = {};
-#pragma unroll
-                for (int kk = 0; kk < NK; ++kk) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(W1S + (uint32_t)(32 * w + 16 * hg + rowB) * C::W2R + (16 * kk + colB) * 2, b0, b1, b2, b3);
-                    mma_bf16(hk[0], kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3], b0, b1);
-                    mma_bf16(hk[1], kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3], b2, b3);
-                }
-                float ak[2][4];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        act_d<ACT>(hk[nt][i] + c1s[hg][nt][i & 1], ak[nt][i], sp[hg][nt][i]);
-                    }
-                akp[hg][0] = pack_bf16(ak[0][0], ak[0][1]);
-                akp[hg][1] = pack_bf16(ak[0][2], ak[0][3]);
-                akp[hg][2] = pack_bf16(ak[1][0], ak[1][1]);
-                akp[hg][3] = pack_bf16(ak[1][2], ak[1][3]);
-                stsm_x4(AX + rowA * C::AR + (32 * w + 16 * hg + colA) * 2, akp[hg][0], akp[hg][1], akp[hg][2],
-                        akp[hg][3]);
-            }
-            __syncthreads();  // A_k visible
-            if (*abort_flag) break;
-
-            // phase 2: E = A_k W2 + c2 - V (start weights) on columns c0 .. c0+7; -Et
-            {
-                float e[2][4] = {};
-                col_product(W2S, AX, e);
-                float cs2[2] = {0.f, 0.f};
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const int tok = g + 8 * r;
-                    const uint32_t vw =
-                        *reinterpret_cast<const uint32_t *>(gbase + (tV - base) + mtoff<D>(tok, c0 + 2 * t4));
-                    const float ex = e[0][2 * r] + e[1][2 * r] + c2s[0] - bf16_lo(vw);
-                    const float ey = e[0][2 * r + 1] + e[1][2 * r + 1] + c2s[1] - bf16_hi(vw);
-                    const bool ok = tok < c;
-                    const float et = -eta_of(tok);
-                    const float nx = ok ? et * ex : 0.f, ny = ok ? et * ey : 0.f;
-                    cs2[0] += nx;
-                    cs2[1] += ny;
-                    *reinterpret_cast<uint32_t *>(gbase + C::EB_OFF + tok * C::ER + (c0 + 2 * t4) * 2) = pack_bf16(ex, ey);
-                    *reinterpret_cast<uint32_t *>(gbase + C::NEB_OFF + tok * C::ER + (c0 + 2 * t4) * 2) =
-                        pack_bf16(nx, ny);
-                }
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    cs2[i] += __shfl_xor_sync(0xffffffffu, cs2[i], 4);
-                    cs2[i] += __shfl_xor_sync(0xffffffffu, cs2[i], 8);
-                    cs2[i] += __shfl_xor_sync(0xffffffffu, cs2[i], 16);
-                    c2r[i] += cs2[i];
-                }
-            }
-            __syncthreads();  // E, -Et visible
-
-            // phase 3: Delta at the start weights; the writes into the register rows
-            uint32_t ef[NK][4], ktf[NK][4], nef[NK][4];
-#pragma unroll
-            for (int kk = 0; kk < NK; ++kk) {
-                ldsm_x4(EB + rowA * C::ER + (16 * kk + colA) * 2, ef[kk][0], ef[kk][1], ef[kk][2], ef[kk][3]);
-                ldsm_x4_t(tK + mtoff<D>(rowA, 16 * kk + colA), ktf[kk][0], ktf[kk][1], ktf[kk][2], ktf[kk][3]);
-                ldsm_x4_t(NEB + rowB * C::ER + (16 * kk + colB) * 2, nef[kk][0], nef[kk][1], nef[kk][2], nef[kk][3]);
-            }
-#pragma unroll
-            for (int hg = 0; hg < 2; ++hg) {
-                float dl[2][4] = {};
-#pragma unroll
-                for (int kk = 0; kk < NK; ++kk) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(W2S + (uint32_t)(32 * w + 16 * hg + rowB) * C::W2R + (16 * kk + colB) * 2, b0, b1, b2, b3);
-                    mma_bf16(dl[0], ef[kk][0], ef[kk][1], ef[kk][2], ef[kk][3], b0, b1);
-                    mma_bf16(dl[1], ef[kk][0], ef[kk][1], ef[kk][2], ef[kk][3], b2, b3);
-                }
-                float nd[2][4], cs1[2][2] = {};
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int tok = g + 8 * (i >> 1);
-                        nd[nt][i] = tok < c ? -eta_of(tok) * dl[nt][i] * sp[hg][nt][i] : 0.f;
-                        cs1[nt][i & 1] += nd[nt][i];
-                    }
-                const uint32_t d00 = movmatrix_t(pack_bf16(nd[0][0], nd[0][1]));
-                const uint32_t d01 = movmatrix_t(pack_bf16(nd[1][0], nd[1][1]));
-                const uint32_t d10 = movmatrix_t(pack_bf16(nd[0][2], nd[0][3]));
-                const uint32_t d11 = movmatrix_t(pack_bf16(nd[1][2], nd[1][3]));
-#pragma unroll
-                for (int j2 = 0; j2 < NK; ++j2) {  // W1^T += (-Dt^T) K
-                    mma_bf16(w1[hg][2 * j2], d00, d01, d10, d11, ktf[j2][0], ktf[j2][1]);
-                    mma_bf16(w1[hg][2 * j2 + 1], d00, d01, d10, d11, ktf[j2][2], ktf[j2][3]);
-                }
-                const uint32_t bt00 = movmatrix_t(akp[hg][0]), bt01 = movmatrix_t(akp[hg][1]);
-                const uint32_t bt10 = movmatrix_t(akp[hg][2]), bt11 = movmatrix_t(akp[hg][3]);
-#pragma unroll
-                for (int mt = 0; mt < NK; ++mt) {  // W2 += A_k^T (-Et)
-                    mma_bf16(w2[hg][mt][0], nef[mt][0], nef[mt][1], nef[mt][2], nef[mt][3], bt00, bt01);
-                    mma_bf16(w2[hg][mt][1], nef[mt][0], nef[mt][1], nef[mt][2], nef[mt][3], bt10, bt11);
-                }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        float v = cs1[nt][i];
-                        v += __shfl_xor_sync(0xffffffffu, v, 4);
-                        v += __shfl_xor_sync(0xffffffffu, v, 8);
-                        v += __shfl_xor_sync(0xffffffffu, v, 16);
-                        c1r[hg][nt][i] += v;
-                    }
-            }
-            if (jb == nch - 1) put_w2(W2E);  // the updated W2 for the output pass
-            __syncthreads();  // the stage, A_k, E, -Et are free
-        } else {
-            // ---------------------------------------------------- output pass
-            uint32_t qf[NK][4];
-#pragma unroll
-            for (int kk = 0; kk < NK; ++kk) ldsm_x4(tQ + mtoff<D>(rowA, 16 * kk + colA), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-#pragma unroll
-            for (int hg = 0; hg < 2; ++hg) {  // A_q = SiLU(Q W1' + c1')
-                float hq[2][4] = {};
-#pragma unroll
-                for (int kk = 0; kk < NK; ++kk) {
-                    uint32_t b[4];
-                    w1_b(hg, kk, b);
-                    mma_bf16(hq[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b[0], b[1]);
-                    mma_bf16(hq[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b[2], b[3]);
-                }
-                float aq[2][4];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        aq[nt][i] = act<ACT>(hq[nt][i] + c1r[hg][nt][i & 1]);
-                    }
-                stsm_x4(AX + rowA * C::AR + (32 * w + 16 * hg + colA) * 2, pack_bf16(aq[0][0], aq[0][1]),
-                        pack_bf16(aq[0][2], aq[0][3]), pack_bf16(aq[1][0], aq[1][1]), pack_bf16(aq[1][2], aq[1][3]));
-            }
-            __syncthreads();  // A_q visible
-            if (*abort_flag) break;
-            float pz[2][4] = {};
-            col_product(W2E, AX, pz);  // z = A_q W2' + c2'
-            __nv_bfloat16 *zb = p.z + ((size_t)bh * T + t0) * D + c0 + 2 * t4;
-            if (g < c)
-                *reinterpret_cast<uint32_t *>(zb + (size_t)g * D) =
-                    pack_bf16(pz[0][0] + pz[1][0] + c2r[0], pz[0][1] + pz[1][1] + c2r[1]);
-            if (g + 8 < c)
-                *reinterpret_cast<uint32_t *>(zb + (size_t)(g + 8) * D) =
-                    pack_bf16(pz[0][2] + pz[1][2] + c2r[0], pz[0][3] + pz[1][3] + c2r[1]);
-            __syncthreads();  // the stage and A_q are free
-        }
-    }
-
-    // ------------------------------------------------------------ final state
-#pragma unroll
-    for (int hg = 0; hg < 2; ++hg) {
-        const int h0 = 32 * w + 16 * hg;
-        if (p.W1o) {
-            float *o = p.W1o + (size_t)bh * D * M;
-#pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                const int r = 8 * j + 2 * t4;
-                o[(size_t)r * M + h0 + g] = w1[hg][j][0];
-                o[(size_t)(r + 1) * M + h0 + g] = w1[hg][j][1];
-                o[(size_t)r * M + h0 + g + 8] = w1[hg][j][2];
-                o[(size_t)(r + 1) * M + h0 + g + 8] = w1[hg][j][3];
-            }
-        }
-        if (p.c1o && g == 0) {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int i = 0; i < 2; ++i) p.c1o[(size_t)bh * M + h0 + 8 * nt + 2 * t4 + i] = c1r[hg][nt][i];
-        }
-        if (p.W2o) {
-            float *o = p.W2o + (size_t)bh * M * D;
-#pragma unroll
-            for (int mt = 0; mt < NK; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int hr = h0 + 8 * nt + 2 * t4, dc = 16 * mt + g;
-                    o[(size_t)hr * D + dc] = w2[hg][mt][nt][0];
-                    o[(size_t)(hr + 1) * D + dc] = w2[hg][mt][nt][1];
-                    o[(size_t)hr * D + dc + 8] = w2[hg][mt][nt][2];
-                    o[(size_t)(hr + 1) * D + dc + 8] = w2[hg][mt][nt][3];
-                }
-        }
-    }
-    if (p.c2o && g == 0) {
-        p.c2o[(size_t)bh * D + c0 + 2 * t4] = c2r[0];
-        p.c2o[(size_t)bh * D + c0 + 2 * t4 + 1] = c2r[1];
-    }
-    // make sure no copy is still landing in shared memory when the CTA ends
-    if (warp == 0)
-        for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
-            if (!mbar_wait(bar_full + 8 * (j % NS), (j / NS) & 1, p.status, kSiteDrain)) break;
-}
-
-static int launch_mlp_fb(const MlpArgs &a, const CUtensorMap *maps)
-{
-    using C = FbmCfg;
-    auto kern = a.act ? ttt_mlp_fb_kernel<1> : ttt_mlp_fb_kernel<0>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-        return -4;
-    MlpParams p;
-    p.H = a.H;
-    p.T = a.T;
-    p.b = a.b;
-    p.causal = a.causal;
-    p.per_batch = a.per_batch;
-    p.eta = a.eta;
-    p.eta_scalar = a.eta_scalar;
-    p.W1 = a.W1;
-    p.c1 = a.c1;
-    p.W2 = a.W2;
-    p.c2 = a.c2;
-    p.z = static_cast<__nv_bfloat16 *>(a.z);
-    p.W1o = a.W1o;
-    p.c1o = a.c1o;
-    p.W2o = a.W2o;
-    p.c2o = a.c2o;
-    p.status = a.status;
-    kern<<<a.B * a.H, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -4;
-}
-
 // d in {16, 32, 64} with hidden width m = 4d.
 int launch_mlp_bf16(const MlpArgs &a)
 {
@@ -1240,7 +820,7 @@ int launch_mlp_bf16(const MlpArgs &a)
     case 16: return launch_mlp_t<16>(a, maps);
     case 32: return launch_mlp_t<32>(a, maps);
     case 64:
-        if (!a.causal && a.b >= a.T) return launch_mlp_fb(a, maps);  // one full-batch mini-batch
+        if (!a.causal && a.b >= a.T) return launch_mlp_fb_tc(a);  // one full-batch mini-batch (tcgen05)
         return a.b <= 16 ? launch_mlp_w8(a, maps) : launch_mlp_t<64>(a, maps);
     default: return -2;
     }

@@ -50,7 +50,7 @@ def test_gate_alone_work_model_and_reference_sample():
     ("linear_125m", "ttt_linear_b16_kernel"), ("linear_125m_b1", "ttt_linear_b1_kernel"),
     ("vision_linear", "ttt_linear_fb_tc_kernel"), ("vision_linear_dot", "ttt_linear_fb_tc_kernel"),
     ("vision_linear_3ep", "ttt_linear_fb_kernel"), ("mlp_125m", "ttt_mlp_w8_kernel"),
-    ("vision_mlp", "ttt_mlp_fb_kernel"), ("vision_dwconv", "ttt_dwconv_kernel"),
+    ("vision_mlp", "ttt_mlp_fb_tc_kernel"), ("vision_dwconv", "ttt_dwconv_kernel"),
     ("linear_tiny_f32", "ttt_linear_f32_kernel")])
 def test_kernel_names_follow_the_dispatch(name, kernel):
     small = {"T": 196} if name.startswith("vision") else {"T": 64}

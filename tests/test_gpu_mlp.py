@@ -73,6 +73,17 @@ def test_bf16_full_batch(T):
     _check(inp)
 
 
+@pytest.mark.parametrize("B,H,T,per_batch", [(41, 8, 70, False), (40, 9, 300, True), (39, 8, 128, False)])
+def test_bf16_full_batch_many_chains(B, H, T, per_batch):
+    """Full batch with more (batch, head) chains than SMs, so each CTA of the
+    persistent kernel runs several chains in a row (start weights rewritten between
+    them, token tiles loaded across chain boundaries): one or three 128-token tiles,
+    ragged and exact, shared and per-batch inner weights."""
+    inp = _mlp_inputs(B, H, T, 64, T, False, eta="sigmoid", seed=80 + T, bias=0.1)
+    inp.eta = inp.eta * 0.2
+    _check(inp, per_batch=per_batch)
+
+
 def test_bf16_per_token_eta_and_per_batch_params():
     inp = _mlp_inputs(3, 2, 90, 64, 16, True, eta="sigmoid", seed=21, bias=0.1)
     inp.eta = inp.eta * 0.1  # eta_t = 0.1 sigmoid(g_t): bounded dynamics
