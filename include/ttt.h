@@ -208,8 +208,9 @@ typedef struct {
                                   ttt_linear_desc ("Learning to (Learn at Test Time)"
                                   walkthrough, section 2.2.1); [H,d] fp32 device arrays,
                                   fixed, or both NULL for the plain MLP.  bf16 I/O needs
-                                  d = 64, m = 256, mini_batch <= 16 (the eight-warp
-                                  tensor-core kernel; TTT_ERR_UNSUPPORTED otherwise)     */
+                                  d = 64, m = 256 and mini_batch <= 16 or one
+                                  non-causal full batch (mini_batch >= T); otherwise
+                                  TTT_ERR_UNSUPPORTED                                   */
     const float *ln_beta;
     float ln_eps;              /* > 0 when the norm is used                             */
 } ttt_mlp_desc;

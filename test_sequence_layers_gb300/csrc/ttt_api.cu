@@ -291,8 +291,9 @@ ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc, const void *q, const void *k, c
     if (ln && (!D.ln_gamma || !D.ln_beta || !(D.ln_eps > 0.f))) return TTT_ERR_ARG;
     if (D.d != 16 && D.d != 32 && D.d != 64) return TTT_ERR_UNSUPPORTED;
     if (D.m % 16 != 0) return TTT_ERR_UNSUPPORTED;
-    if (ln && D.io_dtype == TTT_BF16 &&  // the bf16 inner norm: the eight-warp kernel's shapes
-        (D.d != 64 || D.m != 256 || (D.T > 0 && D.mini_batch > D.T ? D.T : D.mini_batch) > 16))
+    if (ln && D.io_dtype == TTT_BF16 &&  // the bf16 inner norm: d = 64, m = 256, mini-batches of at
+        (D.d != 64 || D.m != 256 ||      // most 16 tokens or one non-causal full batch
+         ((D.T > 0 && D.mini_batch > D.T ? D.T : D.mini_batch) > 16 && (D.causal || D.mini_batch < D.T))))
         return TTT_ERR_UNSUPPORTED;
     if (ln && (!aligned(D.ln_gamma, 4) || !aligned(D.ln_beta, 4))) return TTT_ERR_ALIGN;
     if ((long long)D.B * D.H > 0x7fffffffLL) return TTT_ERR_UNSUPPORTED;

@@ -814,8 +814,10 @@ int launch_mlp_bf16(const MlpArgs &a)
     if (a.m != 4 * a.d) return -2;
     CUtensorMap maps[3];
     if (!encode_qkv(maps, a.q, a.k, a.v, a.B * a.H, a.T, a.d, 16)) return -4;
-    if (a.ln_gamma)  // inner norm + residual: the eight-warp kernel (d = 64, mini-batches <= 16)
+    if (a.ln_gamma) {  // inner norm + residual: d = 64, mini-batches <= 16 or one full batch
+        if (a.d == 64 && !a.causal && a.b >= a.T) return launch_mlp_fb_tc(a);
         return a.d == 64 && a.b <= 16 ? launch_mlp_w8(a, maps) : -2;
+    }
     switch (a.d) {
     case 16: return launch_mlp_t<16>(a, maps);
     case 32: return launch_mlp_t<32>(a, maps);

@@ -68,7 +68,8 @@ struct FmtCfg {
     static constexpr int ET_OFF = A_OFF + 4 * TILE;      // bf16 Et [128 rows][64]
     static constexpr int ONES_OFF = ET_OFF + TILE;       // bf16 ones [128][64]
     static constexpr int F_OFF = ONES_OFF + TILE;        // fp32 c1[256], c2[64]
-    static constexpr int BAR_OFF = F_OFF + 4 * (M + D);
+    static constexpr int LN_OFF = F_OFF + 4 * (M + D);   // fp32 inner-norm gamma[64], beta[64]
+    static constexpr int BAR_OFF = LN_OFF + 4 * 2 * D;
     static constexpr int NBAR = 16;
     static constexpr int SMEM = BAR_OFF + NBAR * 8 + 16 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -102,6 +103,9 @@ struct FmtParams {
     __nv_bfloat16 *z;
     float *W1o, *c1o, *W2o, *c2o;
     int *status;
+    const float *ln_gamma, *ln_beta;  // inner norm [H][d] (the LN instantiation)
+    float ln_eps;
+    const __nv_bfloat16 *q;           // the queries, for the residual z = q + LN(y)
 };
 
 // logistic function as (1 + tanh(h / 2)) / 2, the tanh from the hardware approximation
@@ -217,8 +221,10 @@ __device__ __forceinline__ uint32_t swz(int r, int ch)
 }
 
 __device__ __forceinline__ void named_sync_compute() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// the two warps that share a TMEM lane quarter (w and w + 4)
+__device__ __forceinline__ void named_sync_pair(int q) { asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory"); }
 
-template <int ACT>
+template <int ACT, bool LN>
 __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
     ttt_mlp_fb_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, const FmtParams p)
@@ -235,6 +241,7 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
     volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(gb + C::BAR_OFF + C::NBAR * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gb + C::BAR_OFF + C::NBAR * 8 + 4);
     float *c1s = reinterpret_cast<float *>(gb + C::F_OFF), *c2s = c1s + M;
+    float *gms = reinterpret_cast<float *>(gb + C::LN_OFF), *bts = gms + D;  // inner-norm gamma, beta
     const uint32_t sW1 = base + C::W1_OFF, sW2 = base + C::W2_OFF, sA = base + C::A_OFF, sET = base + C::ET_OFF;
     const uint32_t sONE = base + C::ONES_OFF;
     auto BAR = [&](int i) { return bars + 8u * (uint32_t)i; };
@@ -482,10 +489,12 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
         auto store_batch = [&](int b, const uint32_t (&v)[32]) {
             tc_st32(tl + (b < 2 ? C::T_W1 + C::W1C * hh : C::T_W2 + 64u * hh) + 32u * (uint32_t)(b & 1), v);
         };
-        auto load_bias = [&](int bhx, float &c1v, float &c2v) {
+        auto load_bias = [&](int bhx, float &c1v, float &c2v, float &lnv) {
             const size_t ps = p.per_batch ? (size_t)bhx : (size_t)(bhx % p.H);
             c1v = p.c1[ps * M + tid];
             c2v = tid < D ? p.c2[ps * D + tid] : 0.f;
+            if constexpr (LN)  // thread i < 2d: gamma[i] (i < d) or beta[i - d] of the chain's head
+                lnv = tid < 2 * D ? (tid < D ? p.ln_gamma : p.ln_beta)[(size_t)(bhx % p.H) * D + (tid & (D - 1))] : 0.f;
         };
         // bf16 copy of thread h's row of a weight accumulator into a [256][64] operand tile
         auto copy_row = [&](uint32_t tcol, int off) {  // tcol: the row's first column
@@ -525,6 +534,7 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
         };
         uint32_t sp[4][16];  // act'(H) of this thread's row, 32 hidden units per chunk, packed bf16
         float c1_next = 0.f, c2_next = 0.f;  // the next chain's biases (thread h: c1[h], c2[h] for h < d)
+        float ln_next = 0.f;                 // ... and inner-norm parameters (thread i < 2d)
         for (int ci = 0, bh = blockIdx.x; bh < p.BH; ++ci, bh += gridDim.x) {
             // ------------------------------------------------ start weights
             // (the first chain's are loaded here, the later ones' during the previous
@@ -538,7 +548,7 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                         load_batch(bh, b, v);
                         store_batch(b, v);
                     }
-                    load_bias(bh, c1_next, c2_next);
+                    load_bias(bh, c1_next, c2_next, ln_next);
                     tc_st1(tl + C::T_W1 + C::W1C * hh + 64, __float_as_uint(c1_next));
                 }
                 tc_wait_st();
@@ -546,6 +556,7 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                 copy_row(C::T_W2 + 64u * hh, C::W2_OFF);
                 c1s[tid] = c1_next;
                 if (tid < D) c2s[tid] = c2_next;
+                if (LN && tid < 2 * D) gms[tid] = ln_next;  // (bts = gms + d)
             }
             fence_proxy_async();
             named_sync_compute();  // c1, c2 visible to every warp
@@ -593,7 +604,77 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                 wt(B_EFULL, ne & 1, kSiteConsumerReady);
                 ++ne;
                 tc_fence_after();
-                if (ok && active) {
+                if constexpr (LN) {
+                    // with the inner norm the residual row is dl/dy for 1/2 ||k + LN(y) - v||^2,
+                    // y = E + c2: per-token statistics over the row's 64 columns, half of them
+                    // in the partner warp (exchanged through each thread's own Et chunks,
+                    // which it overwrites only after a last pair barrier); the barriers run
+                    // whenever the quarter holds tokens, so both partners always meet
+                    if (active) {
+                        const float et = valid ? (p.eta ? p.eta[(size_t)bh * T + t] : p.eta_scalar) : 0.f;
+                        uint32_t er[32];
+                        tc_ld32_nowait(tl + C::T_E + 32u * (uint32_t)hh, er);
+                        tc_wait_ld();
+                        float y[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(er[j]) + c2s[32 * hh + j];
+                        auto xchg = [&](int slot, float a, float b) -> float2 {  // the partner's (a, b)
+                            *reinterpret_cast<float2 *>(gb + C::ET_OFF + swz(r, 4 * hh + slot)) = make_float2(a, b);
+                            named_sync_pair(q);
+                            return *reinterpret_cast<const float2 *>(gb + C::ET_OFF + swz(r, 4 * (1 - hh) + slot));
+                        };
+                        float s1 = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) s1 += y[j];
+                        const float mu = (s1 + xchg(0, s1, 0.f).x) * (1.f / D);
+                        float s2 = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) s2 = fmaf(y[j] - mu, y[j] - mu, s2);
+                        const float rs = rsqrtf((s2 + xchg(1, s2, 0.f).x) * (1.f / D) + p.ln_eps);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) y[j] = (y[j] - mu) * rs;  // yh
+                        // g = gamma (k + gamma yh + beta - v), recomputed in the second sweep
+                        auto g_of = [&](int j, float kj, float vj) {
+                            const int jc = 32 * hh + j;
+                            return gms[jc] * (kj + fmaf(gms[jc], y[j], bts[jc]) - vj);
+                        };
+                        float g1 = 0.f, g2 = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint4 kk4 = *reinterpret_cast<const uint4 *>(gb + stg + swz(r, 4 * hh + k));
+                            const uint4 vv4 = *reinterpret_cast<const uint4 *>(gb + stg + C::TILE + swz(r, 4 * hh + k));
+                            const uint32_t kw[4] = {kk4.x, kk4.y, kk4.z, kk4.w}, vw[4] = {vv4.x, vv4.y, vv4.z, vv4.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int j = 8 * k + 2 * i;
+                                const float ga = g_of(j, bf16_lo(kw[i]), bf16_lo(vw[i]));
+                                const float gb2 = g_of(j + 1, bf16_hi(kw[i]), bf16_hi(vw[i]));
+                                g1 += ga + gb2;
+                                g2 = fmaf(ga, y[j], fmaf(gb2, y[j + 1], g2));
+                            }
+                        }
+                        const float2 gp = xchg(2, g1, g2);
+                        const float mg = (g1 + gp.x) * (1.f / D), mgy = (g2 + gp.y) * (1.f / D);
+                        named_sync_pair(q);  // the partner has read this thread's exchange slots
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint4 kk4 = *reinterpret_cast<const uint4 *>(gb + stg + swz(r, 4 * hh + k));
+                            const uint4 vv4 = *reinterpret_cast<const uint4 *>(gb + stg + C::TILE + swz(r, 4 * hh + k));
+                            const uint32_t kw[4] = {kk4.x, kk4.y, kk4.z, kk4.w}, vw[4] = {vv4.x, vv4.y, vv4.z, vv4.w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {  // -eta (g - mean g - yh mean(g yh)) / s
+                                const int j = 8 * k + 2 * i;
+                                const float da = (g_of(j, bf16_lo(kw[i]), bf16_lo(vw[i])) - mg - y[j] * mgy) * rs;
+                                const float db = (g_of(j + 1, bf16_hi(kw[i]), bf16_hi(vw[i])) - mg - y[j + 1] * mgy) * rs;
+                                o[i] = pack_bf16(-et * da, -et * db);
+                            }
+                            *reinterpret_cast<uint4 *>(gb + C::ET_OFF + swz(r, 4 * hh + k)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    } else {
+                        zero_row(C::ET_OFF);
+                    }
+                } else if (ok && active) {
                     const float et = valid ? (p.eta ? p.eta[(size_t)bh * T + t] : p.eta_scalar) : 0.f;
                     uint32_t er[32];
                     tc_ld32_nowait(tl + C::T_E + 32u * (uint32_t)hh, er);
@@ -678,7 +759,7 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                 const int bhn = bh + (int)gridDim.x;
                 const bool pre = mt == nt - 1 && bhn < p.BH;
                 const bool wout = mt == 0;  // the final weights leave one batch per chunk
-                if (pre && ok) load_bias(bhn, c1_next, c2_next);
+                if (pre && ok) load_bias(bhn, c1_next, c2_next, ln_next);
 #pragma unroll
                 for (int c = 0; c < 4; ++c, ++jj) {  // A_q,c = act(H_q,c + c1')
                     uint32_t nx[32];
@@ -713,7 +794,47 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                 wt(B_EFULL, ne & 1, kSiteConsumerReady);
                 ++ne;
                 tc_fence_after();
-                if (ok && active) {
+                if constexpr (LN) {  // z = q + LN(y), y = Z + c2' (the idle Et tile carries the exchange)
+                    if (active) {
+                        uint32_t zr[32];
+                        tc_ld32_nowait(tl + C::T_E + 32u * (uint32_t)hh, zr);
+                        tc_wait_ld();
+                        float y[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(zr[j]) + c2s[32 * hh + j];
+                        auto xchg = [&](int slot, float a) -> float {
+                            *reinterpret_cast<float *>(gb + C::ET_OFF + swz(r, 4 * hh + slot)) = a;
+                            named_sync_pair(q);
+                            return *reinterpret_cast<const float *>(gb + C::ET_OFF + swz(r, 4 * (1 - hh) + slot));
+                        };
+                        float s1 = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) s1 += y[j];
+                        const float mu = (s1 + xchg(0, s1)) * (1.f / D);
+                        float s2 = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) s2 = fmaf(y[j] - mu, y[j] - mu, s2);
+                        const float rs = rsqrtf((s2 + xchg(1, s2)) * (1.f / D) + p.ln_eps);
+                        if (valid && ok) {
+                            const uint4 *qr = reinterpret_cast<const uint4 *>(p.q + ((size_t)bh * T + t) * D + 32 * hh);
+                            uint4 *dst = reinterpret_cast<uint4 *>(p.z + ((size_t)bh * T + t) * D + 32 * hh);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint4 q4 = qr[k];
+                                const uint32_t qw[4] = {q4.x, q4.y, q4.z, q4.w};
+                                uint32_t o[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int j = 8 * k + 2 * i, jc = 32 * hh + j;
+                                    o[i] = pack_bf16(bf16_lo(qw[i]) + fmaf(gms[jc], (y[j] - mu) * rs, bts[jc]),
+                                                     bf16_hi(qw[i]) + fmaf(gms[jc + 1], (y[j + 1] - mu) * rs, bts[jc + 1]));
+                                }
+                                dst[k] = make_uint4(o[0], o[1], o[2], o[3]);
+                            }
+                        }
+                        named_sync_pair(q);  // the exchange slots are free again
+                    }
+                } else if (ok && active) {
                     uint32_t zr[32];
                     tc_ld32_nowait(tl + C::T_E + 32u * (uint32_t)hh, zr);
                     tc_wait_ld();
@@ -743,15 +864,16 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
 
 }  // namespace
 
-// One non-causal full-batch mini-batch (b >= T >= 1), d = 64, m = 256, bf16, no inner
-// norm; -2 otherwise.
+// One non-causal full-batch mini-batch (b >= T >= 1), d = 64, m = 256, bf16, with or
+// without the inner norm; -2 otherwise.
 int launch_mlp_fb_tc(const MlpArgs &a)
 {
     using C = FmtCfg;
-    if (a.d != 64 || a.m != 256 || a.causal || a.b < a.T || a.T < 1 || a.ln_gamma) return -2;
+    if (a.d != 64 || a.m != 256 || a.causal || a.b < a.T || a.T < 1) return -2;
     CUtensorMap maps[3];
     if (!encode_qkv(maps, a.q, a.k, a.v, a.B * a.H, a.T, a.d, 32)) return -4;  // 32-row boxes
-    auto kern = a.act ? ttt_mlp_fb_tc_kernel<1> : ttt_mlp_fb_tc_kernel<0>;
+    auto kern = a.ln_gamma ? (a.act ? ttt_mlp_fb_tc_kernel<1, true> : ttt_mlp_fb_tc_kernel<0, true>)
+                           : (a.act ? ttt_mlp_fb_tc_kernel<1, false> : ttt_mlp_fb_tc_kernel<0, false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -4;
     int dev = 0, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -773,6 +895,10 @@ int launch_mlp_fb_tc(const MlpArgs &a)
     p.W2o = a.W2o;
     p.c2o = a.c2o;
     p.status = a.status;
+    p.ln_gamma = a.ln_gamma;
+    p.ln_beta = a.ln_beta;
+    p.ln_eps = a.ln_eps;
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
     const int grid = p.BH < nsm ? p.BH : nsm;
     kern<<<grid, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;

@@ -57,6 +57,8 @@ WORKLOADS = {
     "mlp_125m_ln": ("mlp", 8, 12, 2048, 64, 256, 16, True, torch.bfloat16, 0.1, 14),
     # the 125M TTT-MLP shape at eta = 0.01, whose plain inner GD stays finite
     "mlp_125m_eta001": ("mlp", 8, 12, 2048, 64, 256, 16, True, torch.bfloat16, 0.01, 15),
+    # the full-batch vision TTT-MLP with the inner norm and residual
+    "vision_mlp_ln": ("mlp", 256, 6, 196, 64, 256, 196, False, torch.bfloat16, 1.0, 16),
 }
 
 # options beyond the base layer: inner loss ("dot"), inner epochs, MLP activation,
@@ -69,6 +71,7 @@ OPTIONS = {
     "linear_125m_ln": {"ln": True},                         # x + LN(x W): the walkthrough's TTT-Linear
     "linear_long_gate_x": {"gate": True},                   # eta = eta_base sigma(theta_lr . x)
     "mlp_125m_ln": {"ln": True},                            # x + LN(act(x W1 + c1) W2 + c2)
+    "vision_mlp_ln": {"ln": True},
 }
 
 

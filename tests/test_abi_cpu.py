@@ -110,6 +110,10 @@ def test_mlp_rejects_bad_arguments(L):
     assert _call_mlp(L, _mlp(ln_gamma=g, ln_eps=1e-6)) == -1               # beta missing
     assert _call_mlp(L, _mlp(io_dtype=abi.TTT_F32, ln_gamma=g, ln_beta=g, ln_eps=0.0)) == -1
     assert _call_mlp(L, _mlp(d=32, ln_gamma=g, ln_beta=g, ln_eps=1e-6)) == -2  # bf16 inner norm: d = 64 only
+    # bf16 inner norm: mini-batches of <= 16 tokens or one non-causal full batch
+    assert _call_mlp(L, _mlp(mini_batch=32, ln_gamma=g, ln_beta=g, ln_eps=1e-6)) == -2
+    assert _call_mlp(L, _mlp(T=64, mini_batch=32, causal=0, ln_gamma=g, ln_beta=g, ln_eps=1e-6)) == -2
+    assert _call_mlp(L, _mlp(T=64, mini_batch=64, causal=1, ln_gamma=g, ln_beta=g, ln_eps=1e-6)) == -2
     assert _call_mlp(L, _mlp(io_dtype=abi.TTT_F32, ln_gamma=g + 2, ln_beta=g, ln_eps=1e-6)) == -3
 
 

@@ -255,6 +255,31 @@ def test_bf16_inner_norm_125m_shape(eta, T):
     assert max(errs) <= G.TOL_BF16, errs
 
 
+@pytest.mark.parametrize("activation", ["silu", "gelu"])
+@pytest.mark.parametrize("B,H,T", [(2, 2, 1), (2, 2, 75), (2, 2, 196), (2, 3, 300), (41, 8, 150)])
+def test_bf16_inner_norm_full_batch(B, H, T, activation):
+    """f(x) = x + LN(act(x W1 + c1) W2 + c2) in one non-causal full batch on the
+    tensor-memory kernel: one to three token tiles, ragged lengths, and more chains
+    than SMs (several chains per CTA).  eta = 0.1: at eta >= 0.2 the norm makes z
+    itself sensitive to bf16 rounding (in the fp64 oracle alone, rounding only the
+    start weights to bf16 moves z by 1-2 % on the (41, 8, 150) inputs, 0.15 % at 0.1)."""
+    errs = _bf16_inner_norm_case(B, H, T, T, False, activation, eta=0.1, seed=300 + T + B)
+    assert max(errs) <= G.TOL_BF16, errs
+
+
+def test_bf16_inner_norm_full_batch_vision_shape():
+    """The vision shape (B256 N196 H6, b = N) with the inner norm at eta = 0.1: every
+    chain."""
+    errs = _bf16_inner_norm_case(256, 6, 196, 196, False, "silu", eta=0.1, seed=320)
+    print("vision_mlp with the inner norm rel err z, W1, c1, W2, c2:", errs)
+    assert max(errs) <= G.TOL_BF16, errs
+
+
+def test_bf16_inner_norm_full_batch_per_token_eta():
+    errs = _bf16_inner_norm_case(3, 2, 196, 196, False, "silu", seed=310, per_token_eta=True)
+    assert max(errs) <= G.TOL_BF16, errs
+
+
 def test_bf16_inner_norm_other_shapes_unsupported():
     inp = _mlp_inputs(1, 1, 32, 32, 16, True, seed=95)
     dev = torch.device("cuda")

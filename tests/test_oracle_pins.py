@@ -562,3 +562,31 @@ def test_block_form_triangular_factor_is_a_finite_series(nb):
     for _ in range(nb - 1):
         T = np.eye(n) - L @ T
     np.testing.assert_allclose(T, np.linalg.inv(np.eye(n) + L), rtol=1e-12, atol=1e-13)
+
+
+def _norm_full_batch_spread(eta):
+    """max |z(W) - z(bf16(W))| / max |z| of the fp64 full-batch TTT-MLP with the inner
+    norm on the GPU tests' B2 H8 T150 inputs: only the start weights are rounded."""
+    import torch
+    from test_sequence_layers_gb300 import synth
+    B, H, T, seed = 2, 8, 150, 452
+    inp = synth.make("mlp", B=B, H=H, T=T, d=64, m=256, b=T, causal=False, eta=eta, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1000)
+    inp.params["c1"] = torch.randn(inp.params["c1"].shape, generator=g) * 0.1
+    inp.params["c2"] = torch.randn(inp.params["c2"].shape, generator=g) * 0.1
+    g = torch.Generator().manual_seed(seed + 1)
+    gam = 1.0 + 0.1 * torch.randn((H, 64), generator=g)
+    bet = 0.1 * torch.randn((H, 64), generator=g)
+    P = [inp.params[n] for n in ("W1", "c1", "W2", "c2")]
+    z0, *_ = oracle.mlp(inp.q, inp.k, inp.v, *P, T, False, eta_scalar=eta, ln_gamma=gam, ln_beta=bet)
+    Pb = [x.to(torch.bfloat16).float() for x in P]
+    z1, *_ = oracle.mlp(inp.q, inp.k, inp.v, *Pb, T, False, eta_scalar=eta, ln_gamma=gam, ln_beta=bet)
+    return np.abs(z1 - z0).max() / np.abs(z0).max()
+
+
+def test_mlp_norm_full_batch_conditioning():
+    """The inner norm divides by each output row's spread, so at a large inner step z
+    carries bf16 rounding of the weights on amplified (the reason the full-batch norm
+    GPU tests run at eta = 0.1): > 1 % at eta = 0.2, < 0.5 % at eta = 0.1."""
+    assert _norm_full_batch_spread(0.2) > 0.01
+    assert _norm_full_batch_spread(0.1) < 0.005
