@@ -350,7 +350,6 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                         issue_xw(sK, 0);
                         issue_xw(sK, 1);
                     }
-                    refill();
                     for (int c = 0; c < 4 && ok; ++c) {
                         if (!wt(B_SFREE + ((jh + c) & 1), ((jh + c) >> 1) & 1, kSiteConsumerReady)) break;
                         tc_fence_after();
@@ -360,6 +359,7 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                     }
                     if (!ok) break;
                     tc_commit(BAR(B_EFULL));
+                    refill();  // (here, not at the tile's start: the previous tile's last products are done by now)
                     if (!wt(B_ETREADY, nu & 1, kSiteConsumerReady)) break;
                     tc_fence_after();
                     const int jp = jj;  // the tile's four chunk jobs are jp .. jp + 3
@@ -370,38 +370,49 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                         for (int kk = 0; kk < 4; ++kk) tc_mma(d, dETk + 2 * kk, dW2k + 512 * c + 2 * kk, ID_TOK, kk > 0);
                         finish_job();
                     };
-                    for (int hc = 0; hc < 2 && ok; ++hc) {
-                        issue_p(hc);
-                        if (!ok) break;
+                    auto issue_w2 = [&](int hc) {  // W2 (hidden 128 hc ..) += A^T Et; A half hc is then free
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)  // W2 (hidden 128 hc ..) += A^T Et
+                        for (int kk = 0; kk < 8; ++kk)
                             tc_mma(tmem + C::T_W2 + 64 * hc, dAw + 2048 * hc + 128 * kk, dETm + 128 * kk, ID_W, true);
                         tc_commit(BAR(B_AFREE + hc));
-                    }
+                    };
+                    auto issue_w1 = [&](int hc) {  // [W1^T | c1] (hidden 128 hc ..) += Dl^T [K | 1]: the
+                        const uint64_t da = dAw + 2048 * hc;  // ones tile is the second 64-feature atom of B
+                        const uint64_t dk = sdesc(sK, (uint32_t)(C::ONES_OFF - (g & 1) * C::STAGE));
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc_mma(tmem + C::T_W1 + C::W1C * hc, da + 128 * kk, dk + 128 * kk, ID_W1, true);
+                    };
+                    const uint32_t sKn = base + (uint32_t)((g + 1) & 1) * C::STAGE;
+                    // the products in the order the chunks are consumed: P0, the first W2
+                    // write, P1; then each chunk's slot goes to the product two chunks on,
+                    // the next tile's first two H chunks included
+                    issue_p(0);
                     if (!ok) break;
+                    issue_w2(0);
+                    issue_p(1);
                     for (int c = 0; c < 4 && ok; ++c) {
                         if (!wt(B_SFREE + ((jp + c) & 1), ((jp + c) >> 1) & 1, kSiteConsumerReady)) break;
                         tc_fence_after();
-                        if (c + 2 < 4) issue_p(c + 2);
-                        if (!ok) break;
-                        if (c == 3 && mt + 1 < nt) {  // the next tile's first two H chunks
-                            const uint32_t sKn = base + (uint32_t)((g + 1) & 1) * C::STAGE;
-                            if (!wt(B_FULL + ((g + 1) & 1), ((g + 1) >> 1) & 1, kSiteConsumerFull)) break;
-                            tc_fence_after();
-                            jh = jj;
-                            issue_xw(sKn, 0);
-                            issue_xw(sKn, 1);
+                        if (c == 0) {
+                            issue_p(2);
+                            if (!ok) break;
+                            issue_w2(1);
+                        } else if (c == 1) {
+                            issue_p(3);
+                            if (!ok) break;
+                            issue_w1(0);
+                        } else if (mt + 1 < nt) {  // the next tile's H chunk c - 2
+                            if (c == 2) {
+                                if (!wt(B_FULL + ((g + 1) & 1), ((g + 1) >> 1) & 1, kSiteConsumerFull)) break;
+                                tc_fence_after();
+                                jh = jj;
+                            }
+                            issue_xw(sKn, c - 2);
                             if (!ok) break;
                         }
-                        if (c & 1) {  // [W1^T | c1] (hidden 128 hc ..) += Dl^T [K | 1]: the ones
-                            const int hc = c >> 1;  // tile is the second 64-feature atom of B
-                            const uint64_t da = dAw + 2048 * hc;
-                            const uint64_t dk = sdesc(sK, (uint32_t)(C::ONES_OFF - (g & 1) * C::STAGE));
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk)
-                                tc_mma(tmem + C::T_W1 + C::W1C * hc, da + 128 * kk, dk + 128 * kk, ID_W1, true);
-                        }
                         if (c == 3) {
+                            issue_w1(1);
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk)  // c2 writes: Et^T 1
                                 tc_mma(tmem + C::T_C2, dETm + 128 * kk, dONE + 2 * (kk & 3), ID_C2, mt > 0 || kk > 0);
@@ -703,26 +714,24 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c, ++jj) {
                     wt(B_SFULL + (jj & 1), (jj >> 1) & 1, kSiteConsumerFull);
-                    if (c == 0 || c == 2) wt(B_AFREE + c / 2, nu & 1, kSiteConsumerReady);
                     tc_fence_after();
+                    uint32_t o[16];  // (computed while the W2 write may still be reading A_c)
                     if (ok && active) {
                         uint32_t pr[32];
                         tc_ld32_nowait(tl + C::T_SLOT + 64u * (uint32_t)(jj & 1) + 32u * (uint32_t)hh, pr);
                         tc_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            uint32_t o[4];
+                        for (int i = 0; i < 16; ++i) o[i] = pack2(__fmul2_rn(f2(pr[2 * i], pr[2 * i + 1]), unpack2(sp[c][i])));
+                    } else {
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int j = 8 * k + 2 * i;
-                                o[i] = pack2(__fmul2_rn(f2(pr[j], pr[j + 1]), unpack2(sp[c][j / 2])));
-                            }
-                            *reinterpret_cast<uint4 *>(gb + C::A_OFF + C::TILE * c + swz(r, 4 * hh + k)) =
-                                make_uint4(o[0], o[1], o[2], o[3]);
-                        }
-                    } else if (ok) {
-                        zero_row(C::A_OFF + C::TILE * c);
+                        for (int i = 0; i < 16; ++i) o[i] = 0u;
                     }
+                    if (c == 0 || c == 2) wt(B_AFREE + c / 2, nu & 1, kSiteConsumerReady);
+                    if (ok)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            *reinterpret_cast<uint4 *>(gb + C::A_OFF + C::TILE * c + swz(r, 4 * hh + k)) =
+                                make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
                     release(B_SFREE + (jj & 1));
                 }
             }
