@@ -479,12 +479,33 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
         // Start weights of chain bhx, thread h's rows (h = tid = TMEM lane 32q + lane of
         // weight tile hh), in four batches of 32 values: W1^T features 0-31 and 32-63,
         // then W2 features 0-31 and 32-63; they go to the weight accumulators (fp32).
+        // W2 rows (this warp's 32 hidden units, 32 features a batch) pass through a
+        // per-warp 2 KB piece of the Et tile, which the plain model leaves idle outside
+        // the update pass, 16 features at a time: global memory then sees 64-byte row
+        // pieces four lanes wide instead of one 16-byte piece per lane and row.  The
+        // 16-byte chunks of a row are XOR-swizzled so both sides hit distinct banks.
+        const uint32_t wstg = base + C::ET_OFF + 2048u * (uint32_t)warp;
+        const int hbase = 128 * hh + 32 * q;  // this warp's first hidden unit
+        auto stg_off = [](int row, int c) { return (uint32_t)row * 64u + (((uint32_t)c ^ (((uint32_t)row >> 1) & 3u)) << 4); };
         auto load_batch = [&](int bhx, int b, uint32_t (&v)[32]) {
             const size_t ps = p.per_batch ? (size_t)bhx : (size_t)(bhx % p.H);
             if (b < 2) {
                 const float *w1 = p.W1 + ps * D * M + (size_t)(32 * b) * M + tid;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(w1[(size_t)j * M]);
+            } else if constexpr (!LN) {  // in staging order: row 8i + lane / 4, 16-byte chunk lane % 4
+                const float *w2 = p.W2 + ps * M * D + (size_t)hbase * D + 32 * (b - 2);
+#pragma unroll
+                for (int rho = 0; rho < 2; ++rho)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 f = *reinterpret_cast<const float4 *>(
+                            w2 + (size_t)(8 * i + (lane >> 2)) * D + 16 * rho + 4 * (lane & 3));
+                        v[16 * rho + 4 * i] = __float_as_uint(f.x);
+                        v[16 * rho + 4 * i + 1] = __float_as_uint(f.y);
+                        v[16 * rho + 4 * i + 2] = __float_as_uint(f.z);
+                        v[16 * rho + 4 * i + 3] = __float_as_uint(f.w);
+                    }
             } else {
                 const float4 *w2 = reinterpret_cast<const float4 *>(p.W2 + ps * M * D + (size_t)tid * D) + 8 * (b - 2);
 #pragma unroll
@@ -498,6 +519,30 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
             }
         };
         auto store_batch = [&](int b, const uint32_t (&v)[32]) {
+            if (!LN && b >= 2) {  // back from staging order to this thread's row
+                uint32_t rowv[32];
+#pragma unroll
+                for (int rho = 0; rho < 2; ++rho) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(wstg + stg_off(8 * i + (lane >> 2), lane & 3)),
+                                     "r"(v[16 * rho + 4 * i]), "r"(v[16 * rho + 4 * i + 1]), "r"(v[16 * rho + 4 * i + 2]),
+                                     "r"(v[16 * rho + 4 * i + 3])
+                                     : "memory");
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 u = lds128(wstg + stg_off(lane, c));
+                        rowv[16 * rho + 4 * c] = u.x;
+                        rowv[16 * rho + 4 * c + 1] = u.y;
+                        rowv[16 * rho + 4 * c + 2] = u.z;
+                        rowv[16 * rho + 4 * c + 3] = u.w;
+                    }
+                    __syncwarp();
+                }
+                tc_st32(tl + C::T_W2 + 64u * hh + 32u * (uint32_t)(b & 1), rowv);
+                return;
+            }
             tc_st32(tl + (b < 2 ? C::T_W1 + C::W1C * hh : C::T_W2 + 64u * hh) + 32u * (uint32_t)(b & 1), v);
         };
         auto load_bias = [&](int bhx, float &c1v, float &c2v, float &lnv) {
@@ -536,11 +581,32 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                     for (int j = 0; j < 32; ++j) o[(size_t)j * M] = __uint_as_float(wr[j]);
                 }
             } else if (p.W2o) {
-                float4 *o = reinterpret_cast<float4 *>(p.W2o + ((size_t)bhx * M + tid) * D) + 8 * (b - 2);
+                if constexpr (!LN) {  // through the staging piece, 16 features at a time
+                    float *o = p.W2o + ((size_t)bhx * M + hbase) * D + 32 * (b - 2);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    o[i] = make_float4(__uint_as_float(wr[4 * i]), __uint_as_float(wr[4 * i + 1]),
-                                       __uint_as_float(wr[4 * i + 2]), __uint_as_float(wr[4 * i + 3]));
+                    for (int rho = 0; rho < 2; ++rho) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(wstg + stg_off(lane, c)),
+                                         "r"(wr[16 * rho + 4 * c]), "r"(wr[16 * rho + 4 * c + 1]),
+                                         "r"(wr[16 * rho + 4 * c + 2]), "r"(wr[16 * rho + 4 * c + 3])
+                                         : "memory");
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int row = 8 * i + (lane >> 2);
+                            const uint4 u = lds128(wstg + stg_off(row, lane & 3));
+                            *reinterpret_cast<uint4 *>(o + (size_t)row * D + 16 * rho + 4 * (lane & 3)) = u;
+                        }
+                        __syncwarp();
+                    }
+                } else {
+                    float4 *o = reinterpret_cast<float4 *>(p.W2o + ((size_t)bhx * M + tid) * D) + 8 * (b - 2);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        o[i] = make_float4(__uint_as_float(wr[4 * i]), __uint_as_float(wr[4 * i + 1]),
+                                           __uint_as_float(wr[4 * i + 2]), __uint_as_float(wr[4 * i + 3]));
+                }
             }
         };
         uint32_t sp[4][16];  // act'(H) of this thread's row, 32 hidden units per chunk, packed bf16
