@@ -311,6 +311,7 @@ ttt_status ttt_mlp_fwd(const ttt_mlp_desc *desc, const void *q, const void *k, c
     }
 
     ttt::MlpArgs a;
+    a.test_stall_ns = g_test_stall_ns.load(std::memory_order_relaxed);
     a.B = D.B;
     a.H = D.H;
     a.T = D.T;

@@ -39,6 +39,7 @@ struct MlpArgs {
     float *W1o, *c1o, *W2o, *c2o;
     int *status;
     cudaStream_t stream;
+    unsigned long long test_stall_ns = 0;  // > 0: the timeout test (full-batch kernel)
 };
 
 struct DwconvArgs {

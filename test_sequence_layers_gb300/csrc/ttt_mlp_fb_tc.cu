@@ -70,7 +70,7 @@ struct FmtCfg {
     static constexpr int F_OFF = ONES_OFF + TILE;        // fp32 c1[256], c2[64]
     static constexpr int LN_OFF = F_OFF + 4 * (M + D);   // fp32 inner-norm gamma[64], beta[64]
     static constexpr int BAR_OFF = LN_OFF + 4 * 2 * D;
-    static constexpr int NBAR = 16;
+    static constexpr int NBAR = 17;
     static constexpr int SMEM = BAR_OFF + NBAR * 8 + 16 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     // tensor-memory columns: chunk slots, E / Z, [W1^T | c1] (two 128-row tiles of 64 + 16
@@ -93,6 +93,7 @@ enum : int {
     B_WSTART = 12,   // a chain's start weights in place (8 warps)
     B_STFREE = 13,   // [2] the products have read a stage (commit)
     B_DRAIN = 15,    // end of the issuer's products (commit)
+    B_DEAD = 16,     // nothing arrives here (the timeout test)
 };
 
 struct FmtParams {
@@ -106,6 +107,7 @@ struct FmtParams {
     const float *ln_gamma, *ln_beta;  // inner norm [H][d] (the LN instantiation)
     float ln_eps;
     const __nv_bfloat16 *q;           // the queries, for the residual z = q + LN(y)
+    unsigned long long test_stall_ns;  // > 0: the elementwise warps' first wait is on a dead barrier
 };
 
 // logistic function as (1 + tanh(h / 2)) / 2, the tanh from the hardware approximation
@@ -192,7 +194,7 @@ __device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, volatile in
 // (up to a few microseconds) until the phase completes, leaving issue slots to the
 // issuing thread.
 __device__ __forceinline__ bool fwait_sleep(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status,
-                                            int site)
+                                            int site, unsigned long long limit_ns = kWaitLimitNs)
 {
     const uint64_t t0 = globaltimer();
     for (;;) {
@@ -206,7 +208,7 @@ __device__ __forceinline__ bool fwait_sleep(uint32_t bar, uint32_t parity, volat
             : "memory");
         if (done) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             atomicCAS(status, 0, site);
             *abort_flag = 1;
             return false;
@@ -465,12 +467,17 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
             ok = __all_sync(0xffffffffu, mine);
             return ok;
         };
-        auto release = [&](int b) {  // this warp's shared-memory writes and TMEM reads are done
+        // this warp's shared-memory writes and TMEM reads are done; a warp whose waits
+        // gave up stops arriving, so the issuing thread meets the abort flag at once
+        auto release = [&](int b) {
             fence_proxy_async();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(b));
+            if (ok && lane == 0) mbar_arrive(BAR(b));
         };
+        if (p.test_stall_ns)  // the timeout test: a first wait that can only run out
+            ok = __all_sync(0xffffffffu, fwait_sleep(BAR(B_DEAD), 0, abort_flag, p.status, kSiteConsumerFull,
+                                                     p.test_stall_ns));
         auto zero_row = [&](uint32_t off) {  // this thread's 32 columns of a tile row
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -974,6 +981,7 @@ int launch_mlp_fb_tc(const MlpArgs &a)
     p.ln_beta = a.ln_beta;
     p.ln_eps = a.ln_eps;
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
+    p.test_stall_ns = a.test_stall_ns;
     const int grid = p.BH < nsm ? p.BH : nsm;
     kern<<<grid, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
