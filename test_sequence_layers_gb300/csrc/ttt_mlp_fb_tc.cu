@@ -27,11 +27,12 @@
 // bf16 along the reduction; MN-major: the same rows read across):
 //  * token side, M = 128 rows, N = 64: H chunk c (hidden 64c .. 64c+63) = K W1,
 //    E = sum_c A_c W2_c, P chunk c = Et W2^T, and in the output pass H_q, Z;
-//  * weight side, M = 128 hidden units, N = 64 features, contracted over the
-//    tile's rows: W2 += A^T Et, W1^T += Dl^T K, accumulated in tensor memory that
-//    starts out holding the chain's start weights (fp32);
-//  * bias writes: Dl^T 1 (M = 128 hidden, N = 16) and Et^T 1 (M = 64 features,
-//    N = 16) against a tile of ones.
+//  * weight side, M = 128 hidden units, contracted over the tile's rows:
+//    W2 += A^T Et (N = 64) and [W1^T | c1] += Dl^T [K | 1] (N = 80: a tile of ones
+//    is the second 64-feature atom of B, so the c1 write comes with W1's),
+//    accumulated in tensor memory that starts out holding the chain's start
+//    weights (fp32);
+//  * the c2 write Et^T 1 (M = 64 features, N = 16) against the ones tile.
 // H / P chunks alternate between two 64-column tensor-memory slots, so the
 // elementwise work on one chunk overlaps the product of the next.  Activations A
 // (later Dl, and A_q in the output pass) are written as bf16 into a [128][256]
@@ -41,11 +42,20 @@
 // copies of its rows of the updated W1^T and W2 that the output pass reads, and
 // the final c1, c2; the fp32 rows of W1 and W2 leave one batch per chunk during the
 // first output tile, and during a chain's last output tile the next chain's start
-// weights are loaded, one batch per chunk, into the freed weight accumulators.
+// weights are loaded, one batch per chunk, into the freed weight accumulators (W2
+// rows through a per-warp piece of the idle Et tile, so global memory sees whole
+// row pieces).
+//
+// The LN instantiation carries the inner norm and residual, f(x) = x + LN(y) (the
+// walkthrough's TTT-MLP): the E stage forms the norm's backward and the output pass
+// z = q + LN(y_q), each token's statistics combined from the two warps of its lane
+// quarter at a 64-thread named barrier.
 //
 // Every wait is bounded; a timeout records its site in the status word, raises a
-// CTA-wide abort flag, and all warps unwind through the same barriers, draining
-// copies and products before tensor memory is released.
+// CTA-wide abort flag, and all warps unwind: elementwise warps that gave up stop
+// arriving on mbarriers but pass every named barrier, the issuing thread leaves at
+// its next wait and drains the copies and products it issued before tensor memory
+// is released.
 #include <cuda.h>
 
 #include "ttt_device.cuh"
@@ -110,36 +120,14 @@ struct FmtParams {
     unsigned long long test_stall_ns;  // > 0: the elementwise warps' first wait is on a dead barrier
 };
 
-// logistic function as (1 + tanh(h / 2)) / 2, the tanh from the hardware approximation
-// (one special-function op per element instead of an exponential and a reciprocal)
-__device__ __forceinline__ float logistic(float h)
+// GELU(h) = h Phi(h) with Phi the standard normal CDF through erf (ACT 1), and its
+// derivative GELU' = Phi + h phi(h); SiLU (ACT 0) takes the paired path below.
+__device__ __forceinline__ float gelu_v(float h) { return h * (0.5f + 0.5f * erff(h * 0.70710678118654752f)); }
+__device__ __forceinline__ void gelu_vd(float h, float &a, float &ad)
 {
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * h));
-    return fmaf(0.5f, t, 0.5f);
-}
-
-// act = SiLU (ACT 0: h sigma(h), ViT3 article, observation 4) or GELU (ACT 1:
-// h Phi(h), Phi the standard normal CDF through erf); the derivative
-// SiLU' = sigma + a (1 - sigma) with a = SiLU(h), GELU' = Phi + h phi(h).
-template <int ACT>
-__device__ __forceinline__ float act_v(float h)
-{
-    if constexpr (ACT == 0) return h * logistic(h);
-    else return h * (0.5f + 0.5f * erff(h * 0.70710678118654752f));
-}
-template <int ACT>
-__device__ __forceinline__ void act_vd(float h, float &a, float &ad)
-{
-    if constexpr (ACT == 0) {
-        const float s = logistic(h);
-        a = h * s;
-        ad = fmaf(-a, s, s + a);
-    } else {
-        const float Phi = 0.5f + 0.5f * erff(h * 0.70710678118654752f);
-        a = h * Phi;
-        ad = Phi + h * 0.39894228040143268f * __expf(-0.5f * h * h);
-    }
+    const float Phi = 0.5f + 0.5f * erff(h * 0.70710678118654752f);
+    a = h * Phi;
+    ad = Phi + h * 0.39894228040143268f * __expf(-0.5f * h * h);
 }
 
 // tanh of two values (hardware approximation)
@@ -151,7 +139,9 @@ __device__ __forceinline__ float2 tanh2(float2 x)
     return t;
 }
 
-// SiLU and SiLU' of two values with paired fp32 arithmetic (sigma through tanh)
+// SiLU(h) = h sigma(h) (ViT3 article, observation 4) and SiLU' = sigma + a (1 - sigma),
+// two values at a time with paired fp32 arithmetic, sigma = (1 + tanh(h / 2)) / 2 (one
+// special-function op per value instead of an exponential and a reciprocal)
 __device__ __forceinline__ void silu_d2(float2 h, float2 &a, float2 &ad)
 {
     const float2 half2 = make_float2(0.5f, 0.5f), one2 = make_float2(1.f, 1.f), mone2 = make_float2(-1.f, -1.f);
@@ -669,8 +659,8 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                             if constexpr (ACT == 0) {
                                 silu_d2(h2, a2, d2);
                             } else {
-                                act_vd<ACT>(h2.x, a2.x, d2.x);
-                                act_vd<ACT>(h2.y, a2.y, d2.y);
+                                gelu_vd(h2.x, a2.x, d2.x);
+                                gelu_vd(h2.y, a2.y, d2.y);
                             }
                             ap[i] = pack2(a2);
                             sp[c][i] = pack2(d2);
@@ -858,7 +848,7 @@ __global__ void __launch_bounds__(FmtCfg::THREADS, 1)
                         for (int i = 0; i < 16; ++i) {
                             const float2 h2 = __fadd2_rn(f2(hr[2 * i], hr[2 * i + 1]), cb[i]);
                             if constexpr (ACT == 0) ap[i] = pack2(silu2(h2));
-                            else ap[i] = pack_bf16(act_v<ACT>(h2.x), act_v<ACT>(h2.y));
+                            else ap[i] = pack_bf16(gelu_v(h2.x), gelu_v(h2.y));
                         }
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
