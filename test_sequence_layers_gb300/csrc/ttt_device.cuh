@@ -189,6 +189,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Standard normal CDF Phi(h) = (1 + erf(h / sqrt 2)) / 2, with erf from Abramowitz &
+// Stegun, Handbook of Mathematical Functions, formula 7.1.26 (|error| <= 1.5e-7 for
+// x >= 0; erf is odd); also returns e = exp(-h^2 / 2), the exponential the formula
+// needs and the GELU derivative's density phi(h) = e / sqrt(2 pi) reuses.
+__device__ __forceinline__ float norm_cdf(float h, float &e)
+{
+    const float x = fabsf(h) * 0.70710678118654752f;
+    e = __expf(-0.5f * h * h);
+    const float t = __fdividef(1.f, fmaf(0.3275911f, x, 1.f));
+    const float poly =
+        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+    return 0.5f + copysignf(0.5f * fmaf(-poly, e, 1.f), h);
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
     uint4 v;

@@ -105,14 +105,17 @@ __device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r
 __device__ __forceinline__ float sigmoid_f(float h) { return __fdividef(1.f, 1.f + __expf(-h)); }
 
 // Inner activation: ACT 0 = SiLU(h) = h sigma(h) (ViT3 article, observation 4),
-// ACT 1 = GELU(h) = h Phi(h), Phi the standard normal CDF written with erf (the
-// walkthrough's TTT-MLP, section 2.2.1).  act() gives the value, act_d() the value
+// ACT 1 = GELU(h) = h Phi(h), Phi the standard normal CDF (the walkthrough's TTT-MLP,
+// section 2.2.1; norm_cdf: erf by Abramowitz & Stegun 7.1.26).  act() gives the value, act_d() the value
 // and the derivative (SiLU' = sigma (1 + h (1 - sigma)), GELU' = Phi + h phi).
 template <int ACT>
 __device__ __forceinline__ float act(float h)
 {
     if constexpr (ACT == 0) return h * sigmoid_f(h);
-    else return h * (0.5f + 0.5f * erff(h * 0.70710678118654752f));
+    else {
+        float e;
+        return h * norm_cdf(h, e);
+    }
 }
 
 template <int ACT>
@@ -123,9 +126,10 @@ __device__ __forceinline__ void act_d(float h, float &a, float &ad)
         a = h * sg;
         ad = sg * (1.f + h * (1.f - sg));
     } else {
-        const float Phi = 0.5f + 0.5f * erff(h * 0.70710678118654752f);
+        float e;
+        const float Phi = norm_cdf(h, e);
         a = h * Phi;
-        ad = Phi + h * 0.39894228040143268f * __expf(-0.5f * h * h);
+        ad = fmaf(h * 0.39894228040143268f, e, Phi);
     }
 }
 

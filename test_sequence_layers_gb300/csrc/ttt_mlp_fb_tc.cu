@@ -120,14 +120,19 @@ struct FmtParams {
     unsigned long long test_stall_ns;  // > 0: the elementwise warps' first wait is on a dead barrier
 };
 
-// GELU(h) = h Phi(h) with Phi the standard normal CDF through erf (ACT 1), and its
+// GELU(h) = h Phi(h) with Phi the standard normal CDF (ACT 1, norm_cdf), and its
 // derivative GELU' = Phi + h phi(h); SiLU (ACT 0) takes the paired path below.
-__device__ __forceinline__ float gelu_v(float h) { return h * (0.5f + 0.5f * erff(h * 0.70710678118654752f)); }
+__device__ __forceinline__ float gelu_v(float h)
+{
+    float e;
+    return h * norm_cdf(h, e);
+}
 __device__ __forceinline__ void gelu_vd(float h, float &a, float &ad)
 {
-    const float Phi = 0.5f + 0.5f * erff(h * 0.70710678118654752f);
+    float e;
+    const float Phi = norm_cdf(h, e);
     a = h * Phi;
-    ad = Phi + h * 0.39894228040143268f * __expf(-0.5f * h * h);
+    ad = fmaf(h * 0.39894228040143268f, e, Phi);
 }
 
 // tanh of two values (hardware approximation)
