@@ -100,9 +100,14 @@ __device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r
                  : "memory");
 }
 
-// logistic function with the fast exponential and divide intrinsics (1 + e^-h
-// overflowing to +inf gives 0, the correct limit)
-__device__ __forceinline__ float sigmoid_f(float h) { return __fdividef(1.f, 1.f + __expf(-h)); }
+// logistic function as (1 + tanh(h / 2)) / 2 with the hardware tanh approximation: one
+// special-function op per value instead of an exponential and a reciprocal
+__device__ __forceinline__ float sigmoid_f(float h)
+{
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * h));
+    return fmaf(0.5f, t, 0.5f);
+}
 
 // Inner activation: ACT 0 = SiLU(h) = h sigma(h) (ViT3 article, observation 4),
 // ACT 1 = GELU(h) = h Phi(h), Phi the standard normal CDF (the walkthrough's TTT-MLP,
