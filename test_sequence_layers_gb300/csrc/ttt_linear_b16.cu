@@ -567,8 +567,17 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
         using I1 = std::integral_constant<int, 1>;
         using I2 = std::integral_constant<int, 2>;
         using I3 = std::integral_constant<int, 3>;
-        return chunk(I0{}, fullc, FA, FB, L) && chunk(I1{}, fullc, FB, FA, L) && chunk(I2{}, fullc, FA, FB, L) &&
-               chunk(I3{}, fullc, FB, FA, L);
+        if constexpr (decltype(fullc)::value) {
+            // a full block's first three chunks always have a successor inside the block and
+            // never wait: the four run in sequence, with no branch between them
+            chunk(I0{}, fullc, FA, FB, L);
+            chunk(I1{}, fullc, FB, FA, L);
+            chunk(I2{}, fullc, FA, FB, L);
+            return chunk(I3{}, fullc, FB, FA, L);
+        } else {
+            return chunk(I0{}, fullc, FA, FB, L) && chunk(I1{}, fullc, FB, FA, L) && chunk(I2{}, fullc, FA, FB, L) &&
+                   chunk(I3{}, fullc, FB, FA, L);
+        }
     };
 
     bool first = nblk > 0 && (p.test_stall_ns ? mbar_wait(dead, 0, p.status, kSiteConsumerFull, p.test_stall_ns)
