@@ -56,7 +56,7 @@ struct B16Cfg {
     static constexpr int BAR_OFF = ETA_OFF + NB * 256;
     // full / empty barriers per block slot, then one barrier nothing arrives at (the
     // timeout test of ttt_debug_wait_limit), then the inner-norm partial sums
-    static constexpr int RED_OFF = BAR_OFF + (2 * NB + 1) * 8;  // [3][NCW][16] float2
+    static constexpr int RED_OFF = (BAR_OFF + (2 * NB + 1) * 8 + 15) / 16 * 16;  // [3][NCW][16] float2
     static constexpr int SMEM = RED_OFF + 3 * NCW * 16 * 8 + 1024;
 };
 
@@ -334,20 +334,24 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
         float *redf = reinterpret_cast<float *>(red);
         redf[((buf * C::NCW + w) * 16 + 8 * b4 + 2 * t4 + b3) * 2 + b2] = tot;
         bar_compute(C::NCW * 32);
+        // tokens 8nt + 2t4 and 8nt + 2t4 + 1 sit side by side: one 16-byte load per warp
+        // and token pair, summed over the warps two floats at a time
+        const float4 *red4 = reinterpret_cast<const float4 *>(red);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt) {
+            float4 t = red4[(buf * C::NCW * 16 + 8 * nt + 2 * t4) >> 1];
+            float2 s0 = make_float2(t.x, t.y), s1 = make_float2(t.z, t.w);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float sa = 0.f, sb = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < C::NCW; ++ww) {
-                    const float2 t = red[(buf * C::NCW + ww) * 16 + 8 * nt + 2 * t4 + j];
-                    sa += t.x;
-                    sb += t.y;
-                }
-                a[nt][j] = sa;
-                b[nt][j] = sb;
+            for (int ww = 1; ww < C::NCW; ++ww) {
+                t = red4[((buf * C::NCW + ww) * 16 + 8 * nt + 2 * t4) >> 1];
+                s0 = __fadd2_rn(s0, make_float2(t.x, t.y));
+                s1 = __fadd2_rn(s1, make_float2(t.z, t.w));
             }
+            a[nt][0] = s0.x;
+            b[nt][0] = s0.y;
+            a[nt][1] = s1.x;
+            b[nt][1] = s1.y;
+        }
     };
 
     // one chunk (L, Q) on fragments F; fetches chunk (L, Q+1) or (L+1, 0) into Fn.
@@ -419,53 +423,66 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
             }
         }
         if constexpr (LN) {
-            // e currently holds Y^T = (K W)^T.  Forward statistics of each token's row.
-            float a[2][2], b[2][2], mu[2][2], rs[2][2];
+            // e currently holds Y^T = (K W)^T.  Elements (nt, 2r + j), j = 0, 1, are tokens
+            // 8nt + 2t4 + j of row col0 + g + 8r: pairs over j share the token statistics, so
+            // the norm runs on paired fp32 instructions.  Forward statistics first.
+            auto yp = [&](int nt, int r) { return make_float2(e[0][nt][2 * r], e[0][nt][2 * r + 1]); };
+            const float2 invd = make_float2(1.f / D, 1.f / D), m1 = make_float2(-1.f, -1.f);
+            float a[2][2], b[2][2];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float y0 = e[0][nt][j], y1 = e[0][nt][2 + j];
-                    a[nt][j] = y0 + y1;
-                    b[nt][j] = y0 * y0 + y1 * y1;
-                }
+            for (int nt = 0; nt < 2; ++nt) {
+                const float2 y0 = yp(nt, 0), y1 = yp(nt, 1);
+                const float2 s2 = __fadd2_rn(y0, y1), q2 = __ffma2_rn(y0, y0, __fmul2_rn(y1, y1));
+                a[nt][0] = s2.x;
+                a[nt][1] = s2.y;
+                b[nt][0] = q2.x;
+                b[nt][1] = q2.y;
+            }
             tok_sums_e(0, a, b);
+            float2 rs[2], mr[2];  // per nt: 1 / sigma and -mu / sigma of tokens j = 0, 1
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    mu[nt][j] = a[nt][j] * (1.f / D);
-                    const float var = fmaxf(b[nt][j] * (1.f / D) - mu[nt][j] * mu[nt][j], 0.f);
-                    rs[nt][j] = rsqrtf(var + p.ln_eps);
-                }
+            for (int nt = 0; nt < 2; ++nt) {
+                const float2 mu = __fmul2_rn(make_float2(a[nt][0], a[nt][1]), invd);
+                const float2 var = __ffma2_rn(__fmul2_rn(mu, m1), mu, __fmul2_rn(make_float2(b[nt][0], b[nt][1]), invd));
+                rs[nt] = make_float2(rsqrtf(fmaxf(var.x, 0.f) + p.ln_eps), rsqrtf(fmaxf(var.y, 0.f) + p.ln_eps));
+                mr[nt] = __fmul2_rn(__fmul2_rn(mu, m1), rs[nt]);
+            }
             // residual through the norm, e = k + LN(y) - v, and g = gamma e
-            float yh[2][4], gg[2][4];
+            float2 yh[2][2], gg[2][2];  // [nt][r]
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = i >> 1, j = i & 1;
-                    yh[nt][i] = (e[0][nt][i] - mu[nt][j]) * rs[nt][j];
-                    const float kv = j ? bf16_hi(F.kc[nt][r]) : bf16_lo(F.kc[nt][r]);
-                    const float vv = j ? bf16_hi(F.vv[nt][r]) : bf16_lo(F.vv[nt][r]);
-                    gg[nt][i] = ge[r] * (kv + fmaf(ge[r], yh[nt][i], be[r]) - vv);
+                for (int r = 0; r < 2; ++r) {
+                    yh[nt][r] = __ffma2_rn(yp(nt, r), rs[nt], mr[nt]);
+                    const float2 kv = make_float2(bf16_lo(F.kc[nt][r]), bf16_hi(F.kc[nt][r]));
+                    const float2 vv = make_float2(bf16_lo(F.vv[nt][r]), bf16_hi(F.vv[nt][r]));
+                    const float2 kb = __ffma2_rn(vv, m1, __fadd2_rn(kv, make_float2(be[r], be[r])));
+                    const float2 g2 = make_float2(ge[r], ge[r]);
+                    gg[nt][r] = __fmul2_rn(g2, __ffma2_rn(g2, yh[nt][r], kb));
                 }
             // backward statistics: means of g and g * yh over the row
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    a[nt][j] = gg[nt][j] + gg[nt][2 + j];
-                    b[nt][j] = gg[nt][j] * yh[nt][j] + gg[nt][2 + j] * yh[nt][2 + j];
-                }
+            for (int nt = 0; nt < 2; ++nt) {
+                const float2 s2 = __fadd2_rn(gg[nt][0], gg[nt][1]);
+                const float2 q2 = __ffma2_rn(gg[nt][0], yh[nt][0], __fmul2_rn(gg[nt][1], yh[nt][1]));
+                a[nt][0] = s2.x;
+                a[nt][1] = s2.y;
+                b[nt][0] = q2.x;
+                b[nt][1] = q2.y;
+            }
             tok_sums_e(1, a, b);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt) {
+                const float2 na = __fmul2_rn(make_float2(a[nt][0], a[nt][1]), __fmul2_rn(invd, m1));
+                const float2 bd = __fmul2_rn(make_float2(b[nt][0], b[nt][1]), invd);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int j = i & 1;
-                    e[0][nt][i] = (gg[nt][i] - a[nt][j] * (1.f / D) - yh[nt][i] * (b[nt][j] * (1.f / D))) * rs[nt][j];
+                for (int r = 0; r < 2; ++r) {
+                    // (g - mean g - yh mean(g yh)) / sigma
+                    const float2 x = __fmul2_rn(__ffma2_rn(__fmul2_rn(yh[nt][r], m1), bd, __fadd2_rn(gg[nt][r], na)), rs[nt]);
+                    e[0][nt][2 * r] = x.x;
+                    e[0][nt][2 * r + 1] = x.y;
                 }
+            }
         }
         // -Et^T as an A fragment
         float ne[2][4];
@@ -509,44 +526,44 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
                      pack_bf16(sm[1][0], sm[1][1]), pack_bf16(sm[1][2], sm[1][3]), ea1, ea3);
         }
         if constexpr (LN) {
-            // zc holds Q W_t: z = q + LN(q W_t) per token (rows g, g + 8 of Z)
-            float a[2], b[2];
+            // zc holds Q W_t: z = q + LN(q W_t) per token (rows g, g + 8 of Z; elements
+            // (hh, 2r + j) are columns col0 + 8hh + 2t4 + j of row g + 8r)
+            float v[4];  // (sum, sum of squares) of rows g, g + 8 over this lane's 4 columns
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                a[r] = zc[0][2 * r] + zc[0][2 * r + 1] + zc[1][2 * r] + zc[1][2 * r + 1];
-                b[r] = zc[0][2 * r] * zc[0][2 * r] + zc[0][2 * r + 1] * zc[0][2 * r + 1] +
-                       zc[1][2 * r] * zc[1][2 * r] + zc[1][2 * r + 1] * zc[1][2 * r + 1];
-#pragma unroll
-                for (int m = 1; m < 4; m <<= 1) {
-                    a[r] += __shfl_xor_sync(0xffffffffu, a[r], m);
-                    b[r] += __shfl_xor_sync(0xffffffffu, b[r], m);
-                }
+                const float2 z0 = make_float2(zc[0][2 * r], zc[0][2 * r + 1]);
+                const float2 z1 = make_float2(zc[1][2 * r], zc[1][2 * r + 1]);
+                const float2 s2 = __fadd2_rn(z0, z1), q2 = __ffma2_rn(z0, z0, __fmul2_rn(z1, z1));
+                v[2 * r] = s2.x + s2.y;
+                v[2 * r + 1] = q2.x + q2.y;
             }
-            if (t4 == 0)
+            // reduce-scatter over the row's 4 lanes: value 2r + stat ends in lane t4 = 2r + stat
+            const bool c1 = (t4 >> 1) & 1, c0 = t4 & 1;
+            float u[2];
 #pragma unroll
-                for (int r = 0; r < 2; ++r) red[(2 * C::NCW + w) * 16 + g + 8 * r] = make_float2(a[r], b[r]);
+            for (int k = 0; k < 2; ++k)
+                u[k] = (c1 ? v[2 + k] : v[k]) + __shfl_xor_sync(0xffffffffu, c1 ? v[k] : v[2 + k], 2);
+            const float tot = (c0 ? u[1] : u[0]) + __shfl_xor_sync(0xffffffffu, c0 ? u[0] : u[1], 1);
+            reinterpret_cast<float *>(red)[((2 * C::NCW + w) * 16 + g + 8 * c1) * 2 + c0] = tot;
             bar_compute(C::NCW * 32);
-            float mu[2], rs[2];
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                float sa = 0.f, sb = 0.f;
+                float2 sm = red[(2 * C::NCW) * 16 + g + 8 * r];
 #pragma unroll
-                for (int ww = 0; ww < C::NCW; ++ww) {
-                    const float2 v = red[(2 * C::NCW + ww) * 16 + g + 8 * r];
-                    sa += v.x;
-                    sb += v.y;
+                for (int ww = 1; ww < C::NCW; ++ww) sm = __fadd2_rn(sm, red[(2 * C::NCW + ww) * 16 + g + 8 * r]);
+                const float mu = sm.x * (1.f / D);
+                const float rs = rsqrtf(fmaxf(sm.y * (1.f / D) - mu * mu, 0.f) + p.ln_eps);
+                const float2 rs2 = make_float2(rs, rs), mr2 = make_float2(-mu * rs, -mu * rs);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const float2 zh = __ffma2_rn(make_float2(zc[hh][2 * r], zc[hh][2 * r + 1]), rs2, mr2);
+                    const float2 qv = make_float2(bf16_lo(F.qz[2 * hh + r]), bf16_hi(F.qz[2 * hh + r]));
+                    const float2 zo = __fadd2_rn(qv, __ffma2_rn(make_float2(gz[hh][0], gz[hh][1]), zh,
+                                                              make_float2(bz[hh][0], bz[hh][1])));
+                    zc[hh][2 * r] = zo.x;
+                    zc[hh][2 * r + 1] = zo.y;
                 }
-                mu[r] = sa * (1.f / D);
-                rs[r] = rsqrtf(fmaxf(sb * (1.f / D) - mu[r] * mu[r], 0.f) + p.ln_eps);
             }
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = i >> 1, j = i & 1;
-                    const float qv = j ? bf16_hi(F.qz[2 * hh + r]) : bf16_lo(F.qz[2 * hh + r]);
-                    zc[hh][i] = qv + fmaf(gz[hh][j], (zc[hh][i] - mu[r]) * rs[r], bz[hh][j]);
-                }
         }
         convert();
         if constexpr (QSIDE) {
