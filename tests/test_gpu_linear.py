@@ -55,18 +55,19 @@ def test_short_and_empty_sequences(T):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("T", [48, 64, 128, 130, 191, 250])
+@pytest.mark.parametrize("T", [16, 48, 64, 128, 130, 191, 250, 320])
 def test_b16_d64_block_boundaries(T, causal):
-    """b = 16, d = 64 (outputs formed per 64-token block on the tensor cores):
-    whole blocks, partial last blocks and a partial last mini-batch, per-token eta."""
+    """b = 16, d = 64 (tokens arrive in 64-token blocks; the last mini-batch of a block
+    releases it and loads the next block's first fragments, skipping only the wait past
+    the end): one mini-batch, a block without its last mini-batch, whole last blocks,
+    partial last blocks and a partial last mini-batch, per-token eta."""
     inp = G.synth.make("linear", B=2, H=2, T=T, d=64, b=16, causal=causal, eta="sigmoid", seed=200 + T)
     _check(inp)
 
 
 @pytest.mark.parametrize("B,H", [(1, 1), (1, 3), (3, 3)])
 def test_b16_d64_odd_chain_counts(B, H):
-    """b = 16, d = 64 with an odd number of (batch, head) chains (the chains are
-    served in pairs)."""
+    """b = 16, d = 64 with one, three and nine (batch, head) chains, one CTA each."""
     inp = G.synth.make("linear", B=B, H=H, T=200, d=64, b=16, causal=True, seed=300 + 3 * B + H)
     _check(inp)
 
