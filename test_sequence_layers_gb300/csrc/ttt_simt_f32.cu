@@ -16,6 +16,9 @@ namespace ttt {
 namespace {
 
 constexpr int kThreads = 256;
+// Tokens whose k, v, q and eta are copied into shared memory together: one round trip
+// to memory per tile instead of one per token on the serial path.
+constexpr int kTile = 32;
 
 struct LinF32Params {
     int H, T, d, b, causal, dot, epochs;  // dot: negative dot-product loss; epochs: passes per block
@@ -51,8 +54,9 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
 {
     extern __shared__ float sm[];
     const int D = p.d, T = p.T, tid = threadIdx.x;
-    float *W = sm, *Ws = W + D * D, *kk = Ws + D * D, *vv = kk + D, *qq = vv + D, *ee = qq + D;
+    float *W = sm, *Ws = W + D * D, *ee = Ws + D * D;
     float *yh = ee + D, *gs = yh + D;  // inner norm scratch
+    float *kt = gs + D, *vt = kt + kTile * D, *qt = vt + kTile * D, *et = qt + kTile * D;  // token tile
     const bool ln = p.ln_gamma != nullptr;
     const float *gm = ln ? p.ln_gamma + (size_t)(blockIdx.x % p.H) * D : nullptr;
     const float *bt = ln ? p.ln_beta + (size_t)(blockIdx.x % p.H) * D : nullptr;
@@ -62,6 +66,21 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
     const float *q = p.q + (size_t)bh * T * D, *k = p.k + (size_t)bh * T * D;
     const float *v = p.v + (size_t)bh * T * D;
     float *z = p.z + (size_t)bh * T * D;
+    // tokens [t0, t1) into the tile (q alone for the non-causal output pass)
+    auto load_tile = [&](int t0, int t1, bool q_only) {
+        __syncthreads();  // the previous tile's readers are done
+        const int n = (t1 - t0) * D;
+        for (int i = tid; i < n; i += blockDim.x) {
+            qt[i] = q[(size_t)t0 * D + i];
+            if (!q_only) {
+                kt[i] = k[(size_t)t0 * D + i];
+                vt[i] = v[(size_t)t0 * D + i];
+            }
+        }
+        if (!q_only)
+            for (int i = tid; i < t1 - t0; i += blockDim.x) et[i] = p.eta ? p.eta[(size_t)bh * T + t0 + i] : p.eta_scalar;
+        __syncthreads();
+    };
 
     for (int n0 = 0; n0 < T; n0 += p.b) {
         const int n1 = min(n0 + p.b, T);
@@ -69,13 +88,10 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
         __syncthreads();
         for (int i = tid; i < D * D; i += blockDim.x) Ws[i] = W[i];
         for (int t = n0; t < n1; ++t) {
-            __syncthreads();
-            if (tid < D) {
-                kk[tid] = k[(size_t)t * D + tid];
-                vv[tid] = v[(size_t)t * D + tid];
-                qq[tid] = q[(size_t)t * D + tid];
-            }
-            __syncthreads();
+            if ((t - n0) % kTile == 0) load_tile(t, min(n1, t + kTile), false);
+            const int ti = (t - n0) % kTile;
+            const float *kk = kt + ti * D, *vv = vt + ti * D, *qq = qt + ti * D;
+            __syncthreads();  // the previous token's readers of ee and W are done
             if (tid < D) {  // e = k_t W_start - v_t (dot loss: e = -v_t; norm: y = k_t W_start)
                 float s = 0.f;
                 if (!p.dot)
@@ -101,9 +117,9 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
                 }
                 __syncthreads();
             }
-            const float et = p.eta ? p.eta[(size_t)bh * T + t] : p.eta_scalar;
+            const float eta_t = et[ti];
             for (int i = tid; i < D * D; i += blockDim.x)  // W -= eta k_t^T e
-                W[i] = fmaf(-et * kk[i / D], ee[i % D], W[i]);
+                W[i] = fmaf(-eta_t * kk[i / D], ee[i % D], W[i]);
             if (p.causal) {
                 __syncthreads();
                 float s = 0.f;
@@ -121,8 +137,8 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
         }  // epochs
         if (!p.causal) {
             for (int t = n0; t < n1; ++t) {
-                __syncthreads();
-                if (tid < D) qq[tid] = q[(size_t)t * D + tid];
+                if ((t - n0) % kTile == 0) load_tile(t, min(n1, t + kTile), true);
+                const float *qq = qt + ((t - n0) % kTile) * D;
                 __syncthreads();
                 float s = 0.f;
                 if (tid < D) {
@@ -147,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) ttt_linear_f32_kernel(const LinF32Pa
 int launch_linear_f32(const LinearArgs &a)
 {
     const int D = a.d;
-    const size_t smem = sizeof(float) * (2 * D * D + 6 * D);
+    const size_t smem = sizeof(float) * (2 * D * D + 3 * D + kTile * (3 * D + 1));
     if (cudaFuncSetAttribute(ttt_linear_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return -4;
