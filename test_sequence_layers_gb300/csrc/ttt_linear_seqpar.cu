@@ -98,10 +98,11 @@ std::mutex g_side_mu;
 SideStream g_side[64];
 
 // Per-chunk times of the two preparing roles relative to the output role (b = 16,
-// d = 64, one CTA per SM), used to balance segment lengths: the state chain alone
-// (measured on the GB300 with the B2 H32 T32768 workload: 169 ns per 16-token chunk
-// against 242 ns for the output role) and a map (the chain on twice the columns).
-constexpr double kChainToOutput = 0.70;
+// d = 64, one CTA per SM), used to balance segment lengths: the state chain alone and
+// a map (the chain on twice the columns).  The chain's ratio is fitted on the GB300 with
+// the B2 H32 T32768 workload: 0.45 / 0.50 / 0.55 / 0.60 / 0.65 / 0.70 / 0.75 / 0.80 gave
+// 336 / 334 / 329 / 325 / 336 / 349 / 362 / 376 us per call.
+constexpr double kChainToOutput = 0.60;
 constexpr double kMapToOutput = 0.95;
 
 // Modelled time (in output-chunk units) of a split with segment 0 of len0 tokens and
