@@ -125,6 +125,32 @@ def block_form_linear(q, k, v, W0, eta, b, nb):
     return z, W
 
 
+def chunked_delta_rule(q, k, v, W0, eta, C=16):
+    """The delta rule (mini-batches of one token) in chunks of C tokens, numpy fp64, one
+    chain (q,k,v [T,d], eta [T]), in the order of the chunked kernel's steps.  With W the
+    chunk's start weights and R = K W - V, token t's residual at its own weights is
+    e_t = r_t - sum_{s<t} eta_s (k_t . k_s) e_s, i.e. (I + A) E = R with A strictly lower,
+    A_ts = (k_t . k_s) eta_s, solved by forward substitution (after e_s is final, every
+    later row loses A_ts e_s).  Then, as in a mini-batch step with the solved E,
+        Z = Q W - tril(Q K^T) diag(eta) E      (tril keeps key s <= query t)
+        W <- W - K^T diag(eta) E."""
+    T, d = q.shape
+    W = W0.copy()
+    z = np.zeros((T, d))
+    for n0 in range(0, T, C):
+        n1 = min(n0 + C, T)
+        n = n1 - n0
+        Q, K, V, et = q[n0:n1], k[n0:n1], v[n0:n1], eta[n0:n1]
+        E = K @ W - V
+        A = np.tril(K @ K.T, -1) * et[None, :]
+        for s in range(n - 1):
+            E[s + 1:] -= A[s + 1:, s:s + 1] * E[s:s + 1]
+        Et = et[:, None] * E
+        z[n0:n1] = Q @ W - (np.tril(np.ones((n, n))) * (Q @ K.T)) @ Et
+        W = W - K.T @ Et
+    return z, W
+
+
 def dual_mlp(q, k, v, W1, c1, W2, c2, eta, b, causal, activation="silu"):
     """TTT-MLP mini-batch step in matrix form (numpy fp64, one chain).  The "+1"
     terms carry the bias writes: c_t = c - sum_{s<=t} eta_s * grad_c l_s."""

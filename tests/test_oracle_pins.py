@@ -547,6 +547,23 @@ def test_linear_block_form_equals_token_loop(T, b, nb):
         np.testing.assert_allclose(Wb, Wf[0, h], rtol=1e-9, atol=1e-10)
 
 
+@pytest.mark.parametrize("T,C", [(16, 16), (48, 16), (57, 16), (5, 16), (40, 8)])
+def test_chunked_delta_rule_equals_token_loop(T, C):
+    """The delta rule (b = 1) in chunks of C tokens, as the chunked kernel computes it: the
+    residuals at the chunk's start weights, a forward substitution through the strictly
+    lower (k_t . k_s) eta_s, then the mini-batch output and update with the solved
+    residuals; equal to the oracle's token loop to fp64 rounding, ragged tails included."""
+    B, H, d = 1, 2, 8
+    q, k, v = _qkv(B, H, T, d)
+    eta = rng.uniform(0.1, 1.0, (B, H, T))
+    W0 = rng.standard_normal((H, d, d)) * 0.3
+    z, Wf = oracle.linear(q, k, v, W0, 1, causal=True, eta=eta)
+    for h in range(H):
+        zc, Wc = _defs.chunked_delta_rule(q[0, h], k[0, h], v[0, h], W0[h], eta[0, h], C)
+        np.testing.assert_allclose(zc, z[0, h], rtol=1e-9, atol=1e-10)
+        np.testing.assert_allclose(Wc, Wf[0, h], rtol=1e-9, atol=1e-10)
+
+
 @pytest.mark.parametrize("nb", [1, 2, 4])
 def test_block_form_triangular_factor_is_a_finite_series(nb):
     """L is block-strictly-lower over nb mini-batches, so L^nb = 0 and (I + L)^-1 is the
