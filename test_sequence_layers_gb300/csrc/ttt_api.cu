@@ -200,9 +200,10 @@ int launch_linear(const ttt::LinearArgs &a, ttt_dtype io)
         rc = ttt::launch_linear_fb_tc(a);  // full-batch mini-batch: no serial chain
         if (rc == TTT_ERR_UNSUPPORTED) rc = ttt::launch_linear_fb(a);  // several epochs
         if (rc == TTT_ERR_UNSUPPORTED && a.epochs == 1)  // repeated epochs: the full-batch kernel only
-            rc = a.b == 1                    ? ttt::launch_linear_b1(a)  // delta rule: column-parallel
-                 : (a.b == 16 && a.d <= 64) ? ttt::launch_linear_b16(a)
-                                            : ttt::launch_linear_bf16(a);
+            rc = (a.b == 1 && a.d <= 64 && !a.loss) ? ttt::launch_linear_b16(a)  // delta rule in 16-token chunks
+                 : a.b == 1                          ? ttt::launch_linear_b1(a)   // column-parallel
+                 : (a.b == 16 && a.d <= 64)          ? ttt::launch_linear_b16(a)
+                                                     : ttt::launch_linear_bf16(a);
     } else
         rc = ttt::launch_linear_f32(a);
     return rc;

@@ -57,7 +57,9 @@ struct B16Cfg {
     // full / empty barriers per block slot, then one barrier nothing arrives at (the
     // timeout test of ttt_debug_wait_limit), then the inner-norm partial sums
     static constexpr int RED_OFF = (BAR_OFF + (2 * NB + 1) * 8 + 15) / 16 * 16;  // [3][NCW][16] float2
-    static constexpr int SMEM = RED_OFF + 3 * NCW * 16 * 8 + 1024;
+    // delta rule: each compute warp's coupling matrix of the chunk, [16 s][16 t] fp32
+    static constexpr int DA_OFF = RED_OFF + 3 * NCW * 16 * 8;
+    static constexpr int SMEM = DA_OFF + NCW * 1024 + 1024;
 };
 
 // Offset of element (r, c) inside a 64-token block written by TMA with the swizzle
@@ -80,6 +82,7 @@ struct Frag {
     float et[2][2];          // eta of tokens 8nt + 2t4 + i of the chunk
     uint32_t kc[2][2];       // inner norm: K^T of this warp's columns in accumulator layout
     uint32_t qz[4];          // inner norm: Q of this warp's columns in the layout of Z
+    uint32_t ka[D / 16][4];  // delta rule: K as the A operand of K K^T
 };
 
 enum { kRoleOut = 0, kRoleChain = 1, kRoleMap = 2 };
@@ -128,7 +131,11 @@ __device__ __forceinline__ bool bar_compute_and(int nthreads, bool v)
 // One unit (chain bh, segment seg) in role ROLE; the CTA has at least the role's
 // warps (extra warps leave after the barrier set-up).
 // VAR 0: the MSE loss on f(x) = x W.  VAR 1 (DOT): the negative dot-product
-// loss, whose residual is -V whatever W is (no product K W on the chain).  VAR 2
+// loss, whose residual is -V whatever W is (no product K W on the chain).  VAR 3
+// (DELTA, output role only): mini-batches of one token, the delta rule, in chunks of
+// 16: the residuals at the chunk's start weights R = K W - V become the tokens' own
+// residuals through a forward substitution, e_t = r_t - sum_{s<t} (k_t . k_s) eta_s e_s,
+// after which the chunk's output and update are those of a 16-token mini-batch.  VAR 2
 // (inner norm, output role only): f(x) = x + LN(x W); the per-token layer-norm
 // statistics over the d columns, which four warps hold 16 apiece, are summed
 // through shared memory with the compute warps' named barrier (forward statistics
@@ -139,8 +146,9 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
                                          const B16Params &p, const int bh, const int seg)
 {
     constexpr bool MAP = ROLE == kRoleMap, QSIDE = ROLE == kRoleOut;
-    constexpr bool DOT = VAR == 1, LN = VAR == 2;
+    constexpr bool DOT = VAR == 1, LN = VAR == 2, DELTA = VAR == 3;
     static_assert(!LN || QSIDE, "the inner norm runs in the output role");
+    static_assert(!DELTA || QSIDE, "the chunked delta rule runs in the output role");
     using C = B16Cfg<D, MAP>;
     constexpr int NJ = C::NJ, NK = C::NK, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
@@ -286,6 +294,10 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
             ldsm_x4_t(st + C::BLK + offV, F.kc[0][0], F.kc[0][1], F.kc[1][0], F.kc[1][1]);
             ldsm_x4(st + offQz, F.qz[0], F.qz[1], F.qz[2], F.qz[3]);
         }
+        if constexpr (DELTA)
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk)
+                ldsm_x4(st + C::BLK + offA[kk], F.ka[kk][0], F.ka[kk][1], F.ka[kk][2], F.ka[kk][3]);
         if (has_eta) {
             const float *e = reinterpret_cast<const float *>(gbase + C::ETA_OFF + (L & (NB - 1)) * 256) +
                              16 * Q + 2 * t4;
@@ -390,6 +402,12 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
             mma_bf16(sc[0], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], F.kB[kk][0], F.kB[kk][1]);
             mma_bf16(sc[1], F.qa[kk][0], F.qa[kk][1], F.qa[kk][2], F.qa[kk][3], F.kB[kk][2], F.kB[kk][3]);
         }
+        [[maybe_unused]] float gk[2][4] = {};  // delta rule: K K^T of the chunk (inputs only)
+#pragma unroll
+        for (int kk = 0; kk < NK && DELTA; ++kk) {
+            mma_bf16(gk[0], F.ka[kk][0], F.ka[kk][1], F.ka[kk][2], F.ka[kk][3], F.kB[kk][0], F.kB[kk][1]);
+            mma_bf16(gk[1], F.ka[kk][0], F.ka[kk][1], F.ka[kk][2], F.ka[kk][3], F.kB[kk][2], F.kB[kk][3]);
+        }
         // next chunk's fragments: inside a block the load is unconditional (reads of
         // the ring past the sequence end stay in bounds and are never used), so the
         // chunk body stays one basic block; crossing into the next block waits for it
@@ -482,6 +500,40 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
                     e[0][nt][2 * r] = x.x;
                     e[0][nt][2 * r + 1] = x.y;
                 }
+            }
+        }
+        if constexpr (DELTA) {
+            // e holds R^T = (K W - V)^T at the chunk's start weights.  Coupling of the
+            // chunk, A[t][s] = (k_t . k_s) eta_s for s < t, stored as [s][t] in this
+            // warp's 1 KB: the accumulator element (t = g + 8(i>>1), s = 8nt + 2t4 + (i&1))
+            float *As = reinterpret_cast<float *>(gbase + C::DA_OFF) + w * 256;
+            __syncwarp();  // the previous chunk's reads of As are done
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = g + 8 * (i >> 1), sk = 8 * nt + 2 * t4 + (i & 1);
+                    As[sk * 16 + t] = (sk < t && (FULL || t < c)) ? gk[nt][i] * F.et[nt][i & 1] : 0.f;
+                }
+            __syncwarp();
+            // forward substitution: once token s's residual is final (columns g, g + 8 in
+            // lane t4 = (s mod 8) / 2 of each row group), every token t of the lane loses
+            // A[t][s] e_s (zero unless t > s)
+#pragma unroll
+            for (int si = 0; si < 15; ++si) {
+                const int src = (lane & ~3) | ((si & 7) >> 1);
+                const float v0 = __shfl_sync(0xffffffffu, e[0][si >> 3][si & 1], src);
+                const float v1 = __shfl_sync(0xffffffffu, e[0][si >> 3][2 + (si & 1)], src);
+                const float2 a0 = *reinterpret_cast<const float2 *>(As + si * 16 + 2 * t4);
+                const float2 a1 = *reinterpret_cast<const float2 *>(As + si * 16 + 8 + 2 * t4);
+                e[0][0][0] = fmaf(-a0.x, v0, e[0][0][0]);
+                e[0][0][1] = fmaf(-a0.y, v0, e[0][0][1]);
+                e[0][0][2] = fmaf(-a0.x, v1, e[0][0][2]);
+                e[0][0][3] = fmaf(-a0.y, v1, e[0][0][3]);
+                e[0][1][0] = fmaf(-a1.x, v0, e[0][1][0]);
+                e[0][1][1] = fmaf(-a1.y, v0, e[0][1][1]);
+                e[0][1][2] = fmaf(-a1.x, v1, e[0][1][2]);
+                e[0][1][3] = fmaf(-a1.y, v1, e[0][1][3]);
             }
         }
         // -Et^T as an A fragment
@@ -657,10 +709,11 @@ template <int D, bool PREP>
 int launch_b16_t(const LinearArgs &a, const B16Params &p, int units, const CUtensorMap *maps)
 {
     using C = B16Cfg<D, PREP>;
-    auto kern = PREP     ? ttt_linear_b16_prep_kernel<D>
-                : a.ln_gamma ? ttt_linear_b16_kernel<D, 2>
-                : a.loss     ? ttt_linear_b16_kernel<D, 1>
-                             : ttt_linear_b16_kernel<D, 0>;
+    auto kern = PREP       ? ttt_linear_b16_prep_kernel<D>
+                : a.ln_gamma   ? ttt_linear_b16_kernel<D, 2>
+                : a.loss       ? ttt_linear_b16_kernel<D, 1>
+                : a.b == 1     ? ttt_linear_b16_kernel<D, 3>
+                               : ttt_linear_b16_kernel<D, 0>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return -4;
     kern<<<units, C::THREADS, C::SMEM, a.stream>>>(maps[0], maps[1], maps[2], p);
@@ -673,7 +726,7 @@ B16Params b16_params(const LinearArgs &a)
     p.BH = a.B * a.H;
     p.H = a.H;
     p.T = a.T;
-    p.causal = a.causal;
+    p.causal = a.b == 1 ? 1 : a.causal;  // one-token mini-batches: every query reads its own write
     p.eta = a.eta;
     p.eta_scalar = a.eta_scalar;
     p.W0 = a.W0;

@@ -72,10 +72,11 @@ def test_b16_d64_odd_chain_counts(B, H):
     _check(inp)
 
 
-@pytest.mark.parametrize("d", [16, 32, 128])
-@pytest.mark.parametrize("T", [0, 1, 63, 64, 65, 129])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("T", [0, 1, 15, 17, 63, 64, 65, 129])
 def test_b1_delta_rule_lengths(d, T):
-    """b = 1 (the delta rule, column-parallel kernel): lengths around its 64-token
+    """b = 1 (the delta rule: d <= 64 in 16-token chunks with a forward substitution,
+    d = 128 on the column-parallel kernel): lengths around 16-token chunks and 64-token
     blocks, per-token eta, per-batch W0, both masks (a one-token mini-batch reads its
     own write either way)."""
     for causal in (True, False):
