@@ -132,7 +132,10 @@ def kernel_name(inp):
         if not inp.causal and inp.b >= inp.T and inp.d == 64 and inp.T <= 256:
             return "ttt_linear_fb_tc_kernel" if inp.options.get("epochs", 1) == 1 else "ttt_linear_fb_kernel"
         if inp.b == 1 and inp.options.get("epochs", 1) == 1 and not inp.options.get("ln"):
-            return "ttt_linear_b1_kernel"
+            # the delta rule: 16-token chunks on the b = 16 kernel (d <= 64, MSE), else the
+            # column-parallel kernel
+            dot = inp.options.get("loss", "mse") == "dot"
+            return "ttt_linear_b16_kernel" if inp.d <= 64 and not dot else "ttt_linear_b1_kernel"
         return "ttt_linear_b16_kernel" if min(inp.b, inp.T) == 16 and inp.d <= 64 else "ttt_linear_bf16_kernel"
     if inp.d == 64 and not inp.causal and inp.b >= inp.T:
         return "ttt_mlp_fb_tc_kernel"

@@ -135,9 +135,10 @@ ttt_status ttt_linear_fwd(const ttt_linear_desc *desc,
  * weights, and the segments' outputs are computed in parallel from those.  The
  * first segment runs from W0 while the maps are formed.
  *
- * Applies to io_dtype TTT_BF16 with mini_batch 16 and d in {16, 32, 64} when the
- * GPU has at least two SMs per chain; otherwise the call runs ttt_linear_fwd
- * (workspace unused, may be NULL).
+ * Applies to io_dtype TTT_BF16 with mini_batch 16, or 1 (the delta rule, whose
+ * 16-token chunks are affine in the weights as well), d in {16, 32, 64} and the MSE
+ * loss, when the GPU has at least two SMs per chain; otherwise the call runs
+ * ttt_linear_fwd (workspace unused, may be NULL).
  *   workspace       : device scratch owned by the caller, 256-byte aligned, at least
  *                     ttt_linear_seqpar_workspace(desc) bytes; it holds the maps and
  *                     start weights and must not be touched until the work queued

@@ -132,7 +132,7 @@ __device__ __forceinline__ bool bar_compute_and(int nthreads, bool v)
 // warps (extra warps leave after the barrier set-up).
 // VAR 0: the MSE loss on f(x) = x W.  VAR 1 (DOT): the negative dot-product
 // loss, whose residual is -V whatever W is (no product K W on the chain).  VAR 3
-// (DELTA, output role only): mini-batches of one token, the delta rule, in chunks of
+// (DELTA, every role): mini-batches of one token, the delta rule, in chunks of
 // 16: the residuals at the chunk's start weights R = K W - V become the tokens' own
 // residuals through a forward substitution, e_t = r_t - sum_{s<t} (k_t . k_s) eta_s e_s,
 // after which the chunk's output and update are those of a 16-token mini-batch.  VAR 2
@@ -148,7 +148,6 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
     constexpr bool MAP = ROLE == kRoleMap, QSIDE = ROLE == kRoleOut;
     constexpr bool DOT = VAR == 1, LN = VAR == 2, DELTA = VAR == 3;
     static_assert(!LN || QSIDE, "the inner norm runs in the output role");
-    static_assert(!DELTA || QSIDE, "the chunked delta rule runs in the output role");
     using C = B16Cfg<D, MAP>;
     constexpr int NJ = C::NJ, NK = C::NK, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
@@ -506,7 +505,7 @@ __device__ __forceinline__ void b16_unit(const CUtensorMap *tq, const CUtensorMa
             // e holds R^T = (K W - V)^T at the chunk's start weights.  Coupling of the
             // chunk, A[t][s] = (k_t . k_s) eta_s for s < t, stored as [s][t] in this
             // warp's 1 KB: the accumulator element (t = g + 8(i>>1), s = 8nt + 2t4 + (i&1))
-            float *As = reinterpret_cast<float *>(gbase + C::DA_OFF) + w * 256;
+            float *As = reinterpret_cast<float *>(gbase + C::DA_OFF) + warp * 256;
             __syncwarp();  // the previous chunk's reads of As are done
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -693,23 +692,23 @@ __global__ void __launch_bounds__(B16Cfg<D, false>::THREADS, 1)
 // The work before a split run's later segments: CTAs 0 .. BH-1 run the state chain
 // of each chain's first segment, the others the affine maps of segments
 // 1 .. nsplit-2 (chain (u - BH) / (nsplit - 2)).
-template <int D>
+template <int D, int VAR>
 __global__ void __launch_bounds__(B16Cfg<D, true>::THREADS, 1)
     ttt_linear_b16_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                                const __grid_constant__ CUtensorMap tv, const B16Params p)
 {
     const int u = blockIdx.x;
     if (u < p.BH)
-        b16_unit<D, kRoleChain>(&tq, &tk, &tv, p, u, 0);
+        b16_unit<D, kRoleChain, VAR>(&tq, &tk, &tv, p, u, 0);
     else
-        b16_unit<D, kRoleMap>(&tq, &tk, &tv, p, (u - p.BH) / (p.nsplit - 2), 1 + (u - p.BH) % (p.nsplit - 2));
+        b16_unit<D, kRoleMap, VAR>(&tq, &tk, &tv, p, (u - p.BH) / (p.nsplit - 2), 1 + (u - p.BH) % (p.nsplit - 2));
 }
 
 template <int D, bool PREP>
 int launch_b16_t(const LinearArgs &a, const B16Params &p, int units, const CUtensorMap *maps)
 {
     using C = B16Cfg<D, PREP>;
-    auto kern = PREP       ? ttt_linear_b16_prep_kernel<D>
+    auto kern = PREP       ? (a.b == 1 ? ttt_linear_b16_prep_kernel<D, 3> : ttt_linear_b16_prep_kernel<D, 0>)
                 : a.ln_gamma   ? ttt_linear_b16_kernel<D, 2>
                 : a.loss       ? ttt_linear_b16_kernel<D, 1>
                 : a.b == 1     ? ttt_linear_b16_kernel<D, 3>

@@ -40,39 +40,84 @@ namespace {
 
 // Start weights of segments 2 .. nsplit-1 of one chain: W_{s+1} = A_s W_s + B_s
 // in fp32, from W_1 (written by the state chain of segment 0).  One CTA of 256
-// threads per chain.
+// threads per chain, a 16 x 16 grid of threads each holding a TS x TS tile of the
+// product (register blocking: per four steps along k, one 16-byte load of each of its
+// rows of A and TS-wide loads of four rows of W feed 16 TS^2 FMAs).  The steps are
+// serial, so the next map is fetched during the current product: A_{s+1} into the
+// other shared buffer (cp.async), this thread's tile of B_{s+1} into registers.
 template <int D>
 __global__ void __launch_bounds__(256) ttt_linear_scan_kernel(const float *__restrict__ maps,
                                                               float *__restrict__ Wst, int nsplit)
 {
-    constexpr int TPR = 256 / D;      // threads per output row
-    constexpr int PER = D / TPR;      // outputs per thread
-    __shared__ float sW[D * D], sA[D * D];
-    const int bh = blockIdx.x, t = threadIdx.x;
-    const int r = t / TPR, c0 = t % TPR;
+    constexpr int TS = D / 16;  // tile side
+    __shared__ __align__(16) float sW[D * D], sA[2][D * D];
+    const int bh = blockIdx.x, t = threadIdx.x, ty = t / 16, tx = t % 16;
+    const int r0 = TS * ty, c0 = TS * tx;
     float *W = Wst + (size_t)bh * (nsplit - 1) * D * D;
-    for (int i = t; i < D * D; i += 256) sW[i] = W[i];
-    for (int s = 1; s + 1 < nsplit; ++s) {
-        const float *A = maps + ((size_t)bh * (nsplit - 2) + s - 1) * 2 * D * D;
-        const float *B = A + D * D;
-        for (int i = t; i < D * D; i += 256) sA[i] = A[i];
-        __syncthreads();
-        float acc[PER];
-#pragma unroll
-        for (int m = 0; m < PER; ++m) acc[m] = B[(size_t)r * D + c0 + TPR * m];
-#pragma unroll 8
-        for (int k = 0; k < D; ++k) {
-            const float a = sA[r * D + k];
-#pragma unroll
-            for (int m = 0; m < PER; ++m) acc[m] = fmaf(a, sW[k * D + c0 + TPR * m], acc[m]);
+    auto map_a = [&](int s) { return maps + ((size_t)bh * (nsplit - 2) + s - 1) * 2 * D * D; };
+    auto fetch_a = [&](int s, float *dst) {  // 16-byte pieces of A_s, committed as one group
+        const float *A = map_a(s);
+        for (int i = t; i < D * D / 4; i += 256) {
+            const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst + 4 * i));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(A + 4 * i) : "memory");
         }
-        __syncthreads();  // every read of sW and sA is done
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    float bn[TS][TS];  // this thread's tile of the next B
+    auto fetch_b = [&](int s) {
+        const float *B = map_a(s) + D * D;
+#pragma unroll
+        for (int i = 0; i < TS; ++i)
+#pragma unroll
+            for (int j = 0; j < TS; ++j) bn[i][j] = B[(size_t)(r0 + i) * D + c0 + j];
+    };
+    for (int i = t; i < D * D; i += 256) sW[i] = W[i];
+    if (nsplit > 2) {
+        fetch_a(1, sA[0]);
+        fetch_b(1);
+    }
+    for (int s = 1; s + 1 < nsplit; ++s) {
+        const float *sa = sA[(s - 1) & 1];
+        float acc[TS][TS];
+#pragma unroll
+        for (int i = 0; i < TS; ++i)
+#pragma unroll
+            for (int j = 0; j < TS; ++j) acc[i][j] = bn[i][j];
+        if (s + 2 < nsplit) {  // the next map while this one multiplies
+            fetch_a(s + 1, sA[s & 1]);
+            fetch_b(s + 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();  // A_s and the previous step's W are complete
+#pragma unroll 4
+        for (int k = 0; k < D; k += 4) {
+            float4 a[TS];
+#pragma unroll
+            for (int i = 0; i < TS; ++i) a[i] = *reinterpret_cast<const float4 *>(sa + (r0 + i) * D + k);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                float w[TS];
+#pragma unroll
+                for (int j = 0; j < TS; ++j) w[j] = sW[(k + kk) * D + c0 + j];
+#pragma unroll
+                for (int i = 0; i < TS; ++i) {
+                    const float ak = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+#pragma unroll
+                    for (int j = 0; j < TS; ++j) acc[i][j] = fmaf(ak, w[j], acc[i][j]);
+                }
+            }
+        }
+        __syncthreads();  // every read of sW and of this step's A is done
         float *out = W + (size_t)s * D * D;
 #pragma unroll
-        for (int m = 0; m < PER; ++m) {
-            sW[r * D + c0 + TPR * m] = acc[m];
-            out[(size_t)r * D + c0 + TPR * m] = acc[m];
-        }
+        for (int i = 0; i < TS; ++i)
+#pragma unroll
+            for (int j = 0; j < TS; ++j) {
+                sW[(r0 + i) * D + c0 + j] = acc[i][j];
+                out[(size_t)(r0 + i) * D + c0 + j] = acc[i][j];
+            }
     }
 }
 
@@ -105,15 +150,32 @@ SideStream g_side[64];
 constexpr double kChainToOutput = 0.60;
 constexpr double kMapToOutput = 0.95;
 
+// The split's cost model, in units of one output-role chunk: the preparing roles' chunk
+// costs, a fixed cost per launch and the scan's cost per map.  Mini-batches of 16: the
+// ratios above (the fixed costs are small against the long sequences that split).
+// Mini-batches of one token (the delta rule, whose chunks carry a forward substitution:
+// 0.62 us per output chunk on the GB300): from the launch lists of linear_125m_b1, the
+// state chain 0.86 and a map 1.85 of an output chunk (a map's eight warps share the
+// sub-partitions), about 5 us per launch, and the scan about 1.5 us per map.
+struct SplitCosts {
+    double chain, map, launch, scan_map;
+};
+constexpr SplitCosts kCosts16 = {kChainToOutput, kMapToOutput, 0.0, 0.0};
+constexpr SplitCosts kCosts1 = {0.86, 1.85, 8.0, 2.5};
+
 // Modelled time (in output-chunk units) of a split with segment 0 of len0 tokens and
-// nsplit - 1 later segments of len1 tokens.
-double split_time(int len0, int len1, int nsplit)
+// nsplit - 1 later segments of len1 tokens: segment 0's outputs on the caller's stream
+// against the preparing launch, the scan (with maps) and the later segments' outputs on
+// the side stream.
+double split_time(int len0, int len1, int nsplit, const SplitCosts &k)
 {
     const double c0 = len0 / 16.0, c1 = len1 / 16.0;
-    double prep = c0 * kChainToOutput;
-    if (nsplit > 2 && c1 * kMapToOutput > prep) prep = c1 * kMapToOutput;
-    const double later = prep + c1;
-    return c0 > later ? c0 : later;
+    double prep = c0 * k.chain;
+    if (nsplit > 2 && c1 * k.map > prep) prep = c1 * k.map;
+    const double scan = nsplit > 2 ? k.launch + (nsplit - 2) * k.scan_map : 0.0;
+    const double later = k.launch + prep + scan + k.launch + c1;
+    const double first = k.launch + c0;
+    return first > later ? first : later;
 }
 
 }  // namespace
@@ -121,8 +183,10 @@ double split_time(int len0, int len1, int nsplit)
 bool seqpar_plan(const LinearArgs &a, SeqparPlan &pl)
 {
     pl = SeqparPlan{};
-    // (the inner norm makes a step non-affine in W: no maps)
-    if (a.b != 16 || (a.d != 16 && a.d != 32 && a.d != 64) || a.loss != 0 || a.epochs != 1 || a.ln_gamma)
+    // (the inner norm makes a step non-affine in W: no maps).  Mini-batches of 16, or of
+    // one token (the delta rule, in 16-token chunks: each chunk is affine in W as well)
+    if ((a.b != 16 && a.b != 1) || (a.d != 16 && a.d != 32 && a.d != 64) || a.loss != 0 || a.epochs != 1 ||
+        a.ln_gamma)
         return false;
     int dev = 0, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -134,14 +198,15 @@ bool seqpar_plan(const LinearArgs &a, SeqparPlan &pl)
     // BH (nsplit - 2) map CTAs) share the GPU: nsplit BH <= SMs
     int pmax = (int)(nsm / (BH > 0 ? BH : 1));
     if (pmax > 8) pmax = 8;
-    double best = T / 16.0 * 0.9;  // a split must save at least a tenth
+    const SplitCosts &kc = a.b == 1 ? kCosts1 : kCosts16;
+    double best = (kc.launch + T / 16.0) * 0.9;  // a split must save at least a tenth
     for (int P = 2; P <= pmax; ++P) {
         for (int len0 = 64; len0 < T; len0 += 64) {
             const int rest = T - len0;
             const int len1 = ((rest + (P - 1) - 1) / (P - 1) + 63) / 64 * 64;
-            if (len1 < 256) continue;  // segments shorter than four blocks do not pay
+            if (len1 < (a.b == 1 ? 128 : 256)) continue;  // segments too short to pay
             const int nseg = 1 + (rest + len1 - 1) / len1;
-            const double t = split_time(len0, len1, nseg);
+            const double t = split_time(len0, len1, nseg, kc);
             if (t < best) {
                 best = t;
                 pl.nsplit = nseg;
@@ -203,7 +268,8 @@ int launch_linear_seqpar(const LinearArgs &a, const SeqparPlan &pl, void *ws)
 bool seqpar_plan_serial(const LinearArgs &a, SeqparPlan &pl)
 {
     pl = SeqparPlan{};
-    if (a.b != 16 || (a.d != 16 && a.d != 32 && a.d != 64) || a.loss != 0 || a.epochs != 1 || a.ln_gamma)
+    if ((a.b != 16 && a.b != 1) || (a.d != 16 && a.d != 32 && a.d != 64) || a.loss != 0 || a.epochs != 1 ||
+        a.ln_gamma)
         return false;
     int dev = 0, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||

@@ -47,7 +47,7 @@ def test_gate_alone_work_model_and_reference_sample():
 
 
 @pytest.mark.parametrize("name,kernel", [
-    ("linear_125m", "ttt_linear_b16_kernel"), ("linear_125m_b1", "ttt_linear_b1_kernel"),
+    ("linear_125m", "ttt_linear_b16_kernel"), ("linear_125m_b1", "ttt_linear_b16_kernel"),
     ("vision_linear", "ttt_linear_fb_tc_kernel"), ("vision_linear_dot", "ttt_linear_fb_tc_kernel"),
     ("vision_linear_3ep", "ttt_linear_fb_kernel"), ("mlp_125m", "ttt_mlp_w8_kernel"),
     ("vision_mlp", "ttt_mlp_fb_tc_kernel"), ("vision_dwconv", "ttt_dwconv_kernel"),

@@ -66,6 +66,22 @@ def test_segments_noncausal_and_per_batch_w0(causal):
     _check(inp, per_batch_w0=True)
 
 
+@pytest.mark.parametrize("d,T,H", [(64, 1000, 2), (32, 2048, 2), (16, 1500, 3), (64, 4096, 2)])
+def test_delta_rule_segments_match_oracle(d, T, H):
+    """b = 1 (the delta rule, 16-token chunks with a forward substitution) cut into
+    segments: the chunks are affine in the weights, so the state chain, the maps and the
+    scan apply unchanged; two or more segments, ragged lengths, per-token eta."""
+    inp = G.synth.make("linear", B=1, H=H, T=T, d=d, b=1, causal=True, eta="sigmoid", seed=650 + d + T)
+    _check(inp)
+
+
+def test_workload_125m_delta_rule_split_every_chain():
+    """linear_125m_b1 (B1 H12 T2048 d64, b = 1) through the split, every chain."""
+    inp = G.synth.workload("linear_125m_b1")
+    ez, eW = _check(inp)
+    print(f"linear_125m_b1 (split) rel err z {ez:.3e} W {eW:.3e}")
+
+
 def test_split_equals_unsplit_up_to_rounding():
     """The split and the one-unit-per-chain path evaluate the same rule: outputs and
     final weights agree far inside the bf16 tolerance."""
