@@ -6,7 +6,10 @@
 // The algebra is that of ttt_linear_bf16.cu (dual form of one mini-batch:
 // E = K W - V, Z = Q W - (mask .* Q K^T) diag(eta) E, W -= K^T diag(eta) E, with W^T
 // held as mma.sync accumulators, 16 output columns per warp).  With b = 16 every
-// 16-token chunk is exactly one mini-batch, which allows a leaner schedule:
+// 16-token chunk is exactly one mini-batch.  The same chunks also carry the delta rule
+// (b = 1): a forward substitution turns the residuals at the chunk's start weights into
+// each token's own (VAR 3 below), after which the chunk is a mini-batch step.  This
+// allows a leaner schedule:
 //  * tokens arrive in 64-token blocks (one TMA box per tensor per four chunks);
 //    the four chunks of a block are unrolled, so every fragment address is a
 //    per-lane constant plus a compile-time offset from the block's base;
