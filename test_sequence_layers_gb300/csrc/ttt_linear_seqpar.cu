@@ -156,7 +156,9 @@ constexpr double kMapToOutput = 0.95;
 // Mini-batches of one token (the delta rule, whose chunks carry a forward substitution:
 // 0.62 us per output chunk on the GB300): from the launch lists of linear_125m_b1, the
 // state chain 0.86 and a map 1.85 of an output chunk (a map's eight warps share the
-// sub-partitions), about 5 us per launch, and the scan about 1.5 us per map.
+// sub-partitions) and about 5 us per launch.  The scan's 2.5 chunks per map is below the
+// ~4 us a map took in those launch lists (6.5 chunks); for linear_125m_b1 both values
+// give the same plan, while 6.5 would leave short two-chain sequences unsplit.
 struct SplitCosts {
     double chain, map, launch, scan_map;
 };
